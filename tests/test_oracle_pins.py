@@ -1,0 +1,373 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself
+(closed forms, invariants the mathematics fixes, special cases that reduce to a
+torch library routine, and an independently written brute-force forward).
+
+Each test names the page and passage it pins (maya2_mlx/backbone.py
+``Backbone``; @mlx-bun/inference qwen3-moe.ts ``Qwen3MoeSparseMoeBlock``).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import (Qwen3Oracle, rnd, rms_norm, rope, rope_table, softmax, attention_probs,
+                    silu, dequant_affine, router_topk)
+from qwen3_decoder_layer_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+TINY = I.with_sizes(I.TINY_FP32, name="pin_tiny", num_layers=2, hidden=64, n_heads=4,
+                    n_kv_heads=2, head_dim=16, intermediate=96, capacity=32)
+TINY_MOE = I.with_sizes(TINY, name="pin_tiny_moe", num_experts=8, top_k=2,
+                        moe_intermediate=32, rope_theta=1e7)
+
+
+# ---------------------------------------------------------------- rounding
+def test_bf16_rounding_matches_torch_cast():
+    """rnd(., 'bf16') is round-to-nearest-even to 8 significant bits: it must
+    agree with torch's float32 -> bfloat16 cast on fp32 inputs, ties included."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(200000).astype(np.float32) * np.float32(3.0)
+    # exact ties: bf16 value + half an ulp, for even and odd last kept bits
+    bits = (rng.integers(0x3f000000, 0x40ffffff, 5000, dtype=np.uint32) & 0xFFFF0000) | 0x8000
+    ties = bits.view(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(rnd(x.astype(np.float64), "bf16"), ref)
+
+
+def test_fp32_rounding_matches_numpy_cast():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(100000) * 100.0
+    assert np.array_equal(rnd(x, "fp32"), x.astype(np.float32).astype(np.float64))
+
+
+# ---------------------------------------------------------------- RMSNorm
+def test_rmsnorm_scale_invariance():
+    """RMS(c v) = RMS(v) with eps = 0 (exact mode)."""
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((5, 64))
+    g = 1 + 0.1 * rng.standard_normal(64)
+    base = rms_norm(v, g, 0.0, "exact")
+    for c in (1e-3, 7.0, 1e3):
+        assert np.max(np.abs(rms_norm(c * v, g, 0.0, "exact") - base)) < 1e-12
+
+
+def test_rmsnorm_closed_forms():
+    """Constant vector a*1 with unit gain gives a / sqrt(a^2 + eps); the hand-worked
+    example in tests/golden/closed_forms.json matches; torch's rms_norm agrees."""
+    for a in (0.5, -3.0, 1e-3):
+        out = rms_norm(np.full(8, a), np.ones(8), 1e-6, "exact")
+        assert np.allclose(out, a / math.sqrt(a * a + 1e-6), rtol=0, atol=1e-15)
+    gold = json.load(open(os.path.join(GOLDEN, "closed_forms.json")))["rmsnorm"]
+    out = rms_norm(np.array(gold["x"]), np.array(gold["gain"]), gold["eps"], "exact")
+    assert np.allclose(out, gold["out"], rtol=0, atol=1e-12)
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal((3, 32))
+    g = rng.standard_normal(32)
+    ref = F.rms_norm(torch.from_numpy(v), (32,), torch.from_numpy(g), eps=1e-5).numpy()
+    assert np.max(np.abs(rms_norm(v, g, 1e-5, "exact") - ref)) < 1e-12
+
+
+# ---------------------------------------------------------------- RoPE
+def _rope_at(x, p, D, theta, prec):
+    c, s = rope_table(p + 1, D, theta, prec)
+    return rope(x, c[p], s[p], prec)
+
+
+def test_rope_norm_preservation_and_identity():
+    rng = np.random.default_rng(5)
+    D = 64
+    x = rng.standard_normal(D)
+    for p in (0, 1, 17, 500):
+        assert abs(np.linalg.norm(_rope_at(x, p, D, 1e6, "exact")) - np.linalg.norm(x)) < 1e-12
+    # p = 0 is the identity in every table precision (cos 0 = 1, sin 0 = 0 exactly)
+    for prec in ("exact", "fp32", "bf16"):
+        xr = rnd(x, prec)
+        assert np.array_equal(_rope_at(xr, 0, D, 1e6, prec), xr)
+
+
+def test_rope_relative_position_identity():
+    """<rope(q, m), rope(k, n)> depends only on m - n."""
+    rng = np.random.default_rng(6)
+    D = 32
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    c, s = rope_table(200, D, 1e4, "exact")
+    ref = rope(q, c[9], s[9], "exact") @ rope(k, c[4], s[4], "exact")
+    for shift in (1, 30, 150):
+        got = rope(q, c[9 + shift], s[9 + shift], "exact") @ rope(k, c[4 + shift], s[4 + shift], "exact")
+        assert abs(got - ref) < 1e-10
+
+
+def test_rope_golden_and_complex_form():
+    """Hand-worked D=4, theta=1e4 example (tests/golden/closed_forms.json), and the
+    rotate-half rotation equals multiplying (x_i + i x_{i+D/2}) by exp(i p f_i)."""
+    gold = json.load(open(os.path.join(GOLDEN, "closed_forms.json")))["rope"]
+    out = _rope_at(np.array(gold["x"]), gold["p"], 4, gold["theta"], "exact")
+    assert np.allclose(out, gold["out"], rtol=0, atol=1e-12)
+    rng = np.random.default_rng(7)
+    D, theta, p = 16, 1e6, 37
+    x = rng.standard_normal(D)
+    f = theta ** (-np.arange(D // 2) * 2.0 / D)
+    z = (x[:D // 2] + 1j * x[D // 2:]) * np.exp(1j * p * f)
+    assert np.allclose(_rope_at(x, p, D, theta, "exact"), np.concatenate([z.real, z.imag]), atol=1e-12)
+
+
+def test_rope_bf16_table_uses_rounded_inv_freq():
+    """bf16 table: inv_freq rounded to bf16 before the angle (Backbone.__init__)."""
+    D, theta, p = 128, 1e6, 4000
+    c, s = rope_table(p + 1, D, theta, "bf16")
+    inv = rnd(theta ** (-2.0 * np.arange(D // 2) / D), "bf16")
+    assert np.array_equal(c[p, :D // 2], rnd(np.cos(p * inv), "bf16"))
+    assert np.array_equal(c[p, D // 2:], c[p, :D // 2])
+    assert np.array_equal(s[p, D // 2:], s[p, :D // 2])
+
+
+# ---------------------------------------------------------------- softmax / attention
+def test_softmax_rows_sum_to_one_and_masking():
+    rng = np.random.default_rng(8)
+    s = rng.standard_normal((7, 33)) * 10
+    s[:, 20:] = -np.inf
+    P = softmax(s)
+    assert np.allclose(P.sum(-1), 1.0, atol=1e-14)
+    assert np.all(P[:, 20:] == 0)
+
+
+def test_attention_single_key_returns_v_and_identical_keys_give_mean():
+    rng = np.random.default_rng(9)
+    q, k = rng.standard_normal(16), rng.standard_normal((1, 16))
+    assert np.array_equal(attention_probs(q, k, 0.25), [1.0])
+    K = np.tile(rng.standard_normal(16), (10, 1))
+    V = rng.standard_normal((10, 16))
+    P = attention_probs(q, K, 0.25)
+    assert np.allclose(P @ V, V.mean(0), atol=1e-14)
+
+
+@pytest.mark.parametrize("prec", ["exact", "fp32", "bf16"])
+def test_decode_at_position_zero_returns_v_exactly(prec):
+    """T=1 at position 0 with one cached key: softmax weight 1, so the attention
+    output equals v bit for bit in every precision (q head h reads kv head h//G)."""
+    cfg = I.with_sizes(TINY, dtype="bf16" if prec == "bf16" else "fp32")
+    w = I.make_weights(cfg, seed=11)
+    o = Qwen3Oracle(cfg, w, prec=prec)
+    tr = []
+    o.forward(I.make_rows(cfg, 1, seed=12), trace=tr)
+    G = cfg.n_heads // cfg.n_kv_heads
+    for L in tr:
+        for h in range(cfg.n_heads):
+            assert np.array_equal(L["a"][0, h], L["v"][0, h // G])
+
+
+def test_gqa_attention_matches_torch_sdpa():
+    """One layer's attention (exact mode) against torch's scaled_dot_product_attention
+    with the kv heads repeated G times (repeat_kv) and an explicit causal mask."""
+    cfg = TINY
+    w = I.make_weights(cfg, seed=13)
+    o = Qwen3Oracle(cfg, w, prec="exact")
+    T = 9
+    tr = []
+    o.forward(I.make_rows(cfg, T, seed=14), trace=tr)
+    G = cfg.n_heads // cfg.n_kv_heads
+    for L in tr:
+        q = torch.from_numpy(L["q"]).permute(1, 0, 2)[None]          # [1, H, T, D] (post RoPE)
+        k = torch.from_numpy(L["k"]).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+        v = torch.from_numpy(L["v"]).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+        mask = torch.ones(T, T, dtype=torch.bool).tril()
+        a = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=cfg.head_dim ** -0.5)
+        assert np.max(np.abs(a[0].permute(1, 0, 2).numpy() - L["a"])) < 1e-12
+
+
+# ---------------------------------------------------------------- whole stack
+def _brute_force(cfg, w, x):
+    """Independent fp64 torch forward of a prefill from an empty cache: separate
+    q/k/v and gate/up matmuls, complex-number RoPE, full T x T masked attention
+    with repeat_kv materialised, torch rms_norm and silu, torch.topk router."""
+    d = lambda t: t.detach().double()
+    H, KV, D, hid = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.hidden
+    T = x.shape[0]
+    eps = cfg.rms_eps
+    f = cfg.rope_theta ** (-torch.arange(D // 2, dtype=torch.float64) * 2.0 / D)
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * f[None]
+    rot = torch.polar(torch.ones_like(ang), ang)                           # [T, D/2]
+
+    def rope_c(t):                                                         # t [T, heads, D]
+        z = torch.complex(t[..., :D // 2], t[..., D // 2:]) * rot[:, None, :]
+        return torch.cat([z.real, z.imag], -1)
+
+    h = d(x)
+    for li, L in enumerate(w["layers"]):
+        Wqkv = d(L["qkv"]["w"])
+        Wq, Wk, Wv = Wqkv[:H * D], Wqkv[H * D:(H + KV) * D], Wqkv[(H + KV) * D:]
+        y = F.rms_norm(h, (hid,), d(L["in_norm"]), eps)
+        q = F.rms_norm((y @ Wq.T).view(T, H, D), (D,), d(L["q_norm"]), eps)
+        k = F.rms_norm((y @ Wk.T).view(T, KV, D), (D,), d(L["k_norm"]), eps)
+        v = (y @ Wv.T).view(T, KV, D)
+        q, k = rope_c(q), rope_c(k)
+        k = k.repeat_interleave(H // KV, dim=1)
+        v = v.repeat_interleave(H // KV, dim=1)
+        S = torch.einsum("thd,uhd->htu", q, k) / math.sqrt(D)
+        S = S.masked_fill(~torch.ones(T, T, dtype=torch.bool).tril(), float("-inf"))
+        a = torch.einsum("htu,uhd->thd", torch.softmax(S, -1), v).reshape(T, H * D)
+        h = h + a @ d(L["o"]["w"]).T
+        y2 = F.rms_norm(h, (hid,), d(L["post_norm"]), eps)
+        if cfg.is_moe_layer(li):
+            mI = cfg.moe_intermediate
+            P = torch.softmax(y2 @ d(L["router"]["w"]).T, -1)
+            wk, ik = torch.topk(P, cfg.top_k, dim=-1)
+            wk = wk / wk.sum(-1, keepdim=True)
+            out = torch.zeros_like(h)
+            for t in range(T):
+                for s in range(cfg.top_k):
+                    e = int(ik[t, s])
+                    Wgu = d(L["exp_gate_up"]["w"][e])
+                    m = F.silu(y2[t] @ Wgu[:mI].T) * (y2[t] @ Wgu[mI:].T)
+                    out[t] += wk[t, s] * (m @ d(L["exp_down"]["w"][e]).T)
+            h = h + out
+        else:
+            Wgu = d(L["gate_up"]["w"])
+            n = cfg.intermediate
+            h = h + (F.silu(y2 @ Wgu[:n].T) * (y2 @ Wgu[n:].T)) @ d(L["down"]["w"]).T
+    return F.rms_norm(h, (hid,), d(w["final_norm"]), eps).numpy()
+
+
+@pytest.mark.parametrize("cfg", [TINY, I.with_sizes(TINY, n_kv_heads=4, name="mha"), TINY_MOE],
+                         ids=["gqa", "mha", "moe"])
+def test_stack_matches_brute_force(cfg):
+    w = I.make_weights(cfg, seed=21)
+    x = I.make_rows(cfg, 12, seed=22)
+    got = Qwen3Oracle(cfg, w, prec="exact").forward(x)
+    assert np.max(np.abs(got - _brute_force(cfg, w, x))) < 1e-12
+
+
+@pytest.mark.parametrize("cfg", [TINY, TINY_MOE], ids=["dense", "moe"])
+def test_chunked_prefill_equals_token_by_token_equals_one_pass(cfg):
+    w = I.make_weights(cfg, seed=31)
+    x = I.make_rows(cfg, 16, seed=32)
+    one = Qwen3Oracle(cfg, w, prec="exact").forward(x)
+    o = Qwen3Oracle(cfg, w, prec="exact")
+    chunked = np.concatenate([o.forward(x[i:i + 4]) for i in range(0, 16, 4)])
+    o = Qwen3Oracle(cfg, w, prec="exact")
+    tok = np.concatenate([o.forward(x[i:i + 1]) for i in range(16)])
+    assert np.max(np.abs(chunked - one)) < 1e-12
+    assert np.max(np.abs(tok - one)) < 1e-12
+
+
+def test_batched_sequences_are_independent():
+    """Rows of different sequences in one forward equal separate forwards."""
+    cfg = I.with_sizes(TINY, max_seqs=3)
+    w = I.make_weights(cfg, seed=41)
+    xs = [I.make_rows(cfg, 5, seed=42 + s) for s in range(3)]
+    sep = []
+    for s in range(3):
+        o = Qwen3Oracle(cfg, w, prec="exact")
+        sep.append(o.forward(xs[s][:4]))
+        sep.append(o.forward(xs[s][4:5]))
+    o = Qwen3Oracle(cfg, w, prec="exact")
+    for s in range(3):
+        o.forward(xs[s][:4], seq_ids=[s] * 4)
+    step = o.forward(torch.cat([xs[s][4:5] for s in range(3)]), seq_ids=[0, 1, 2])
+    for s in range(3):
+        assert np.max(np.abs(step[s] - sep[2 * s + 1][0])) < 1e-12
+
+
+def test_capacity_and_position_errors_leave_state_unchanged():
+    cfg = TINY
+    o = Qwen3Oracle(cfg, I.make_weights(cfg, seed=51), prec="exact")
+    o.forward(I.make_rows(cfg, 30, seed=52))
+    with pytest.raises(ValueError):
+        o.forward(I.make_rows(cfg, 3, seed=53))               # 33 > capacity 32
+    assert o.length(0) == 30
+    with pytest.raises(ValueError):
+        o.forward(I.make_rows(cfg, 1, seed=54), positions=[31])
+    assert o.length(0) == 30
+
+
+# ---------------------------------------------------------------- MoE router / experts
+def test_router_weights_sum_to_one_and_ties_go_to_lowest_index():
+    rng = np.random.default_rng(61)
+    for _ in range(50):
+        l = rng.standard_normal(128)
+        idx, w, P = router_topk(l, 8, True)
+        assert abs(w.sum() - 1) < 1e-14
+        assert np.all(np.diff(l[idx]) <= 0)
+        assert l[idx].min() >= np.delete(l, idx).max()
+    l = np.zeros(16)
+    l[[3, 5, 9, 12]] = 2.0                      # four-way tie for the top, k = 3
+    idx, _, _ = router_topk(l, 3, True)
+    assert list(idx) == [3, 5, 9]
+    l = np.array([1.0, 5.0, 1.0, 1.0, 0.0])     # tie for the last slot
+    idx, _, _ = router_topk(l, 3, False)
+    assert list(idx) == [1, 0, 2]
+
+
+def test_moe_with_all_experts_is_the_full_softmax_mixture():
+    """k = E with renormalisation: sum over all experts of softmax(l)_e * expert_e(x)."""
+    cfg = I.with_sizes(TINY_MOE, top_k=8, num_layers=1)
+    w = I.make_weights(cfg, seed=71)
+    o = Qwen3Oracle(cfg, w, prec="exact")
+    y2 = np.random.default_rng(72).standard_normal((3, cfg.hidden))
+    pend, idx, wt = o.moe_block(0, y2)
+    L = o.layers[0]
+    P = softmax(y2 @ L["router"]["w"].astype(np.float64).T)
+    ref = np.zeros_like(pend)
+    mI = cfg.moe_intermediate
+    for e in range(cfg.num_experts):
+        Wgu = L["exp_gate_up"]["w"][e].astype(np.float64)
+        m = silu(y2 @ Wgu[:mI].T) * (y2 @ Wgu[mI:].T)
+        ref += P[:, e:e + 1] * (m @ L["exp_down"]["w"][e].astype(np.float64).T)
+    assert np.max(np.abs(pend - ref)) < 1e-12
+
+
+def test_moe_one_expert_reduces_to_dense_mlp_bitwise():
+    """E = 1, k = 1: weight 1, so the MoE block is the dense SwiGLU MLP, rounding for
+    rounding, when the expert holds the dense weights (bf16 emulation)."""
+    cfg = I.with_sizes(TINY, dtype="bf16", num_layers=1)
+    w = I.make_weights(cfg, seed=81)
+    mcfg = I.with_sizes(cfg, num_experts=1, top_k=1, moe_intermediate=cfg.intermediate)
+    L = w["layers"][0]
+    wm = {"final_norm": w["final_norm"], "layers": [dict(L)]}
+    wm["layers"][0]["router"] = {"w": torch.ones(1, cfg.hidden, dtype=torch.bfloat16)}
+    wm["layers"][0]["exp_gate_up"] = {"w": L["gate_up"]["w"][None]}
+    wm["layers"][0]["exp_down"] = {"w": L["down"]["w"][None]}
+    y2 = rnd(np.random.default_rng(82).standard_normal((4, cfg.hidden)), "bf16")
+    dense = Qwen3Oracle(cfg, w).dense_mlp(Qwen3Oracle(cfg, w).layers[0], y2)
+    moe, idx, wt = Qwen3Oracle(mcfg, wm).moe_block(0, y2)
+    assert np.array_equal(dense, moe) and np.all(idx == 0) and np.all(wt == 1.0)
+
+
+# ---------------------------------------------------------------- int8
+def test_dequant_affine_closed_forms():
+    rng = np.random.default_rng(91)
+    codes = rng.integers(0, 256, (3, 128))
+    scale = rng.uniform(0.001, 0.01, (3, 2))
+    bias = rng.uniform(-1, 1, (3, 2))
+    W = dequant_affine(codes, scale, bias, 64)
+    for o in range(3):
+        for i in range(128):
+            assert W[o, i] == scale[o, i // 64] * codes[o, i] + bias[o, i // 64]
+    mid = dequant_affine(np.full((2, 64), 128), np.full((2, 1), 0.5), np.full((2, 1), -64.0), 64)
+    assert np.all(mid == 0.0)
+
+
+def test_int8_stack_equals_dense_stack_on_dequantised_weights():
+    """An int8 stack is the dense stack run on the dequantised matrices."""
+    cfg = I.with_sizes(TINY, dtype="bf16", weight_format="int8", group_size=16)
+    w = I.make_weights(cfg, seed=101)
+    dense = {"final_norm": w["final_norm"], "layers": []}
+    for L in w["layers"]:
+        D2 = {}
+        for k, v in L.items():
+            if isinstance(v, dict) and "scale" in v:
+                D2[k] = {"w": torch.from_numpy(dequant_affine(
+                    v["w"].numpy(), v["scale"].double().numpy(), v["bias"].double().numpy(), 16))}
+            else:
+                D2[k] = v
+        dense["layers"].append(D2)
+    x = I.make_rows(cfg, 6, seed=102)
+    a = Qwen3Oracle(cfg, w, prec="exact").forward(x)
+    b = Qwen3Oracle(I.with_sizes(cfg, weight_format="dense"), dense, prec="exact").forward(x)
+    assert np.max(np.abs(a - b)) < 1e-12
