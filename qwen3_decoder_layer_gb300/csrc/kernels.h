@@ -1,0 +1,206 @@
+// Internal launch interface between the host runtime (runtime.cpp) and the
+// CUDA kernels.  Plain structs of device pointers and sizes; no torch types.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q3 {
+
+enum DType { DT_F32 = 0, DT_BF16 = 1 };
+enum WFmt { W_DT = 0, W_U8 = 1 };  // weights in the model dtype, or affine int8 codes
+enum Epi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_RESIDUAL = 2, EPI_SWIGLU = 3 };
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  bool pdl;      // programmatic dependent launch attribute on every launch
+  int num_sms;
+};
+
+// h_out = R(h_in + pend) (pend may be NULL: h_out = h_in); y = RMSNorm(h_out) * gain.
+// h_out may alias h_in.  y may be NULL.  One block per row.
+struct NormArgs {
+  const void* h_in;
+  const void* pend;
+  void* h_out;
+  void* y;
+  const void* gain;
+  int rows, hidden;
+  float eps;
+};
+cudaError_t launch_add_rmsnorm(const LaunchCtx& c, int dt, const NormArgs& a);
+
+// Per-head RMSNorm of q and k, RoPE of q and k at each row's position, and
+// the cache append of k and v.  q_out dt [T, H, D]; caches: layer base of
+// sequence 0, sequence stride `seq_stride` elements, [KV][capacity][D] inside.
+struct QkRopeArgs {
+  const void* qkv;
+  int T, H, KV, D;
+  void* q_out;
+  void* kcache;
+  void* vcache;
+  long long seq_stride;
+  int capacity;
+  const void* q_gain;
+  const void* k_gain;
+  const float* cos_t;  // [capacity][D]
+  const float* sin_t;
+  const int* row_seq;  // [T]
+  const int* row_pos;  // [T]
+  float eps;
+};
+cudaError_t launch_qk_rope_cache(const LaunchCtx& c, int dt, const QkRopeArgs& a);
+
+// Weight-streaming GEMV for a few rows: out[t, n] = sum_k x[t, k] W[n, k].
+struct GemvArgs {
+  int T;       // rows of x (shared weights, 1..4) or slots (gather mode)
+  int K;       // input features
+  int N;       // outputs per row (EPI_SWIGLU: pairs; the weight has 2N rows, gate first)
+  const void* w;
+  const void* scale;   // W_U8 only: bf16 [rows, K/group]
+  const void* bias;
+  int group;
+  // gather mode (MoE experts): slot b uses the matrix w + slot_expert[b] * w_stride
+  // and x row b / slot_div.  slot_expert == NULL: one matrix shared by all T rows.
+  const int* slot_expert;
+  long long w_stride;
+  int slot_div;
+  int x_rows;          // rows of x staged in shared memory
+  // input: prologue 0: x given (dt [x_rows, K]); 1: x = RMSNorm(h_in); 2: h_out = R(h_in + pend)
+  // (h_in alone when pend is NULL), x = RMSNorm(h_out); block 0 writes h_out, which must not alias h_in.
+  int prologue;
+  const void* x;
+  const void* h_in;
+  const void* pend;
+  void* h_out;
+  const void* gain;
+  float eps;
+  int epilogue;        // Epi
+  void* out;
+  int ldo;
+};
+cudaError_t launch_gemv(const LaunchCtx& c, int dt, int wfmt, const GemvArgs& a);
+size_t gemv_smem_bytes(const GemvArgs& a);
+
+// Tiled CUDA-core GEMM C[M, N] = A[M, K] B[N, K]^T with fp32 accumulation.
+// Grouped mode (tile_start != NULL): rows are sorted by group; group g owns
+// sorted rows row_off[g] .. row_off[g] + row_cnt[g] and its own weight matrix
+// w + g * w_stride; tile_start is the prefix sum of its row tiles.
+struct GemmArgs {
+  int M, N, K;
+  const void* a;
+  int lda;
+  const int* a_rows;   // A row of output row m (NULL = m)
+  const void* w;
+  const void* scale;
+  const void* bias;
+  int group;
+  long long w_stride;
+  const int* tile_start;
+  const int* row_off;
+  const int* row_cnt;
+  int n_groups;
+  int max_tiles;       // grouped: upper bound of row tiles (grid size)
+  int epilogue;
+  void* out;
+  int ldo;
+  const int* c_rows;   // output row of row m (NULL = m)
+};
+cudaError_t launch_gemm_simt(const LaunchCtx& c, int dt, int wfmt, const GemmArgs& a);
+int gemm_simt_tile_m();
+
+// Attention over the cache.  Work: query blocks (rows of one sequence at
+// consecutive positions) x key chunks x kv heads; each item writes a partial
+// (max, sum, unnormalised output) and the last item of a (query block, kv
+// head) combines them.
+struct AttnQBlock {
+  int seq, row0, nrows, pos0, n_chunks, part_base;
+};
+struct AttnItem {
+  int qb, chunk;
+};
+struct AttnArgs {
+  const void* q;
+  const void* kc;
+  const void* vc;
+  long long seq_stride;
+  int capacity, H, KV, D;
+  float scale;
+  const AttnQBlock* qblocks;
+  const AttnItem* items;
+  const int* n_items;  // device scalar
+  int chunk;           // keys per chunk
+  int nq_max;          // query vectors per block (rows x G), partial stride
+  float* part_o;       // [parts * KV][nq_max][D]
+  float* part_ml;      // [parts * KV][nq_max][2]
+  int* counters;       // [n_qblocks * KV], zero between calls
+  void* out;           // dt [T, H * D]
+  int grid_x;          // persistent grid width
+};
+cudaError_t launch_attention_decode(const LaunchCtx& c, int dt, const AttnArgs& a);
+cudaError_t launch_attention_prefill(const LaunchCtx& c, int dt, const AttnArgs& a);
+// chunk sizes and query-vector limits each attention kernel is built for
+int attn_decode_chunk();
+int attn_decode_nq_max();
+int attn_prefill_chunk();
+int attn_prefill_nq_max();
+
+// MoE router: softmax over all experts, top-k by logit (ties to the lower
+// index), optional renormalisation; per-expert counts (atomics) if counts != NULL.
+struct RouterArgs {
+  const float* logits;  // [T, E]
+  int T, E, k, norm;
+  int* idx;             // [T, k]
+  float* w;             // [T, k]
+  int* counts;          // [E] (zeroed by the caller's scan kernel of the previous use)
+};
+cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a);
+
+// Exclusive scan of expert counts -> row offsets and tile prefix; zeroes cursors.
+struct MoeScanArgs {
+  int* counts;   // [E] read, then zeroed for the next call
+  int E, bm;
+  int* row_off;     // [E]
+  int* row_cnt;     // [E]
+  int* tile_start;  // [E + 1]
+  int* cursor;      // [E] zeroed
+};
+cudaError_t launch_moe_scan(const LaunchCtx& c, const MoeScanArgs& a);
+
+// Place each (token, slot) at its expert's next free sorted row.
+struct MoeScatterArgs {
+  const int* idx;
+  int T, k;
+  const int* row_off;
+  int* cursor;
+  int* sorted_tok;  // [T k] token of each sorted row
+  int* sorted_src;  // [T k] flat (token * k + slot) of each sorted row
+};
+cudaError_t launch_moe_scatter(const LaunchCtx& c, const MoeScatterArgs& a);
+
+// out[t] = R(sum_i w[t, i] z[t k + i]) in fp32.
+struct MoeCombineArgs {
+  const void* z;
+  const float* w;
+  int T, k, hidden;
+  void* out;
+};
+cudaError_t launch_moe_combine(const LaunchCtx& c, int dt, const MoeCombineArgs& a);
+
+// Shared launch helper: cudaLaunchKernelEx with the PDL attribute when asked.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchCtx& c,
+                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = c.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace q3

@@ -1,0 +1,141 @@
+// Qwen3-MoE router and token-by-expert permutation (@mlx-bun/inference
+// qwen3-moe.ts: Qwen3MoeSparseMoeBlock.forward -- "precise" softmax over all
+// experts, argpartition top-k, take_along_axis, renormalise when
+// norm_topk_prob, weighted sum; Qwen3SortedExperts -- rows sorted by expert,
+// gathered, projected, and put back with the inverse permutation).
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int kMaxEPerLane = 8;  // E <= 256
+
+// One warp per token.  Expert e lives in lane e % 32, register e / 32.
+// Top-k is taken on the fp32 logits (softmax is monotone), larger first,
+// ties to the lower expert index; weights are the softmax probabilities of
+// the chosen experts, divided by their sum when norm != 0.
+__global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
+  pdl_wait();
+  pdl_launch();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const float* lg = a.logits + (size_t)t * a.E;
+  float v[kMaxEPerLane];
+  float m = -CUDART_INF_F;
+#pragma unroll
+  for (int r = 0; r < kMaxEPerLane; ++r) {
+    const int e = r * 32 + lane;
+    v[r] = e < a.E ? lg[e] : -CUDART_INF_F;
+    m = fmaxf(m, v[r]);
+  }
+  m = warp_max(m);
+  float s = 0.f;
+#pragma unroll
+  for (int r = 0; r < kMaxEPerLane; ++r)
+    if (r * 32 + lane < a.E) s += expf(v[r] - m);
+  s = warp_sum(s);
+  uint32_t taken = 0;
+  float wsum = 0.f, wmine = 0.f;
+  int emine = 0;
+  for (int sel = 0; sel < a.k; ++sel) {
+    float bv = -CUDART_INF_F;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int r = 0; r < kMaxEPerLane; ++r) {
+      const int e = r * 32 + lane;
+      if (e < a.E && !(taken >> r & 1u) && (v[r] > bv || be == 0x7fffffff)) { bv = v[r]; be = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    const float p = expf(bv - m) / s;
+    wsum += p;
+    if (lane == sel) { wmine = p; emine = be; }
+  }
+  if (lane < a.k) {
+    a.idx[(size_t)t * a.k + lane] = emine;
+    a.w[(size_t)t * a.k + lane] = a.norm ? wmine / wsum : wmine;
+    if (a.counts) atomicAdd(a.counts + emine, 1);
+  }
+}
+
+// Single block: offsets and row-tile prefix of the experts' sorted rows.
+__global__ void moe_scan_kernel(MoeScanArgs a) {
+  pdl_wait();
+  pdl_launch();
+  if (threadIdx.x == 0) {
+    int off = 0, tiles = 0;
+    for (int e = 0; e < a.E; ++e) {
+      const int c = a.counts[e];
+      a.row_off[e] = off;
+      a.row_cnt[e] = c;
+      a.tile_start[e] = tiles;
+      off += c;
+      tiles += (c + a.bm - 1) / a.bm;
+    }
+    a.tile_start[a.E] = tiles;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    a.cursor[e] = 0;
+    a.counts[e] = 0;
+  }
+}
+
+__global__ void moe_scatter_kernel(MoeScatterArgs a) {
+  pdl_wait();
+  pdl_launch();
+  const int f = blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= a.T * a.k) return;
+  const int e = a.idx[f];
+  const int pos = a.row_off[e] + atomicAdd(a.cursor + e, 1);
+  a.sorted_tok[pos] = f / a.k;
+  a.sorted_src[pos] = f;
+}
+
+template <typename Dt>
+__global__ void moe_combine_kernel(MoeCombineArgs a) {
+  pdl_wait();
+  pdl_launch();
+  const int t = blockIdx.x;
+  const Dt* z = static_cast<const Dt*>(a.z) + (size_t)t * a.k * a.hidden;
+  const float* w = a.w + (size_t)t * a.k;
+  Dt* out = static_cast<Dt*>(a.out) + (size_t)t * a.hidden;
+  for (int n = threadIdx.x; n < a.hidden; n += blockDim.x) {
+    float acc = 0.f;
+    for (int i = 0; i < a.k; ++i) acc = fmaf(w[i], to_f(z[(size_t)i * a.hidden + n]), acc);
+    out[n] = from_f<Dt>(acc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a) {
+  if (a.E > 32 * kMaxEPerLane || a.k > 32 || a.k > a.E) return cudaErrorInvalidValue;
+  return launch_k(router_topk_kernel, dim3((a.T + 7) / 8), dim3(256), 0, c, a);
+}
+
+cudaError_t launch_moe_scan(const LaunchCtx& c, const MoeScanArgs& a) {
+  return launch_k(moe_scan_kernel, dim3(1), dim3(256), 0, c, a);
+}
+
+cudaError_t launch_moe_scatter(const LaunchCtx& c, const MoeScatterArgs& a) {
+  const int n = a.T * a.k;
+  return launch_k(moe_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, c, a);
+}
+
+cudaError_t launch_moe_combine(const LaunchCtx& c, int dt, const MoeCombineArgs& a) {
+  if (dt == DT_BF16) return launch_k(moe_combine_kernel<bf16>, dim3(a.T), dim3(256), 0, c, a);
+  return launch_k(moe_combine_kernel<float>, dim3(a.T), dim3(256), 0, c, a);
+}
+
+}  // namespace q3

@@ -1,0 +1,938 @@
+// Host runtime behind the C ABI of include/qwen3.h: configuration and
+// argument validation (before any state change, as Backbone.forward raises
+// before mutating), ownership of the static KV cache and the RoPE table,
+// workspaces, the per-call launch plan, CUDA-graph replay and kernel timing.
+//
+// Plan of one qwen3_forward (maya2_mlx/backbone.py, Backbone.forward), per layer:
+//   T <= 4 rows ("decode"):  GEMV(qkv, prologue h = R(h + pend), RMSNorm)
+//                            -> q/k norm + RoPE + cache append -> attention
+//                            -> GEMV(o, epilogue h = R(h + R(.)))
+//                            -> GEMV(gate|up, prologue RMSNorm, epilogue SiLU*up) -> GEMV(down)
+//   T > 4 rows ("prefill"):  add+RMSNorm -> GEMM(qkv) -> q/k norm + RoPE + cache
+//                            -> attention -> GEMM(o, residual) -> RMSNorm
+//                            -> GEMM(gate|up, SiLU*up) -> GEMM(down)
+//   MoE layers replace the MLP with RMSNorm -> router logits (fp32) -> top-k
+//   -> experts (gathered GEMVs for few rows, sorted grouped GEMMs otherwise)
+//   -> weighted combine (@mlx-bun/inference qwen3-moe.ts Qwen3MoeSparseMoeBlock).
+// and finally add + RMSNorm with the final norm into `out`.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "qwen3.h"
+
+using namespace q3;
+
+namespace {
+
+struct DevBuf {
+  void* p = nullptr;
+  size_t bytes = 0;
+};
+
+struct ProfEvent {
+  const char* name;
+  cudaEvent_t a, b;
+};
+
+struct GraphKey {
+  int T;
+  int kind;
+  const void* x;
+  const void* out;
+  bool operator<(const GraphKey& o) const {
+    if (T != o.T) return T < o.T;
+    if (kind != o.kind) return kind < o.kind;
+    if (x != o.x) return x < o.x;
+    return out < o.out;
+  }
+};
+
+}  // namespace
+
+struct qwen3_handle {
+  qwen3_config cfg{};
+  std::vector<int32_t> mlp_only;
+  std::vector<qwen3_layer_weights> layers;
+  const void* final_norm = nullptr;
+  int device = 0, num_sms = 0;
+  size_t esz = 0;
+  int dt = 0, wfmt = 0;
+  void* kcache = nullptr;
+  void* vcache = nullptr;
+  size_t seq_stride = 0;    // elements between sequences in a cache
+  size_t layer_stride = 0;  // elements between layers
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  std::vector<int32_t> lengths;
+  std::string err;
+  // options
+  bool use_graphs = true, profile = false, pdl = true;
+  // workspace buffers (grow only)
+  DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
+      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc;
+  int ws_generation = 0;
+  // descriptor staging (pinned ring)
+  static constexpr int kRing = 4;
+  void* pinned[kRing] = {};
+  size_t pinned_bytes[kRing] = {};
+  cudaEvent_t pinned_ev[kRing] = {};
+  int ring_pos = 0;
+  // graphs
+  cudaStream_t gstream = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+  std::map<GraphKey, std::pair<cudaGraphExec_t, int>> graphs;  // exec, ws generation
+  // profiling
+  std::vector<ProfEvent> prof_pending;
+  std::vector<cudaEvent_t> ev_pool;
+  std::map<std::string, std::pair<int64_t, double>> prof_acc;
+  std::vector<std::string> prof_names;
+  int64_t launches = 0;
+  int64_t last_launches = 0;
+};
+
+namespace {
+
+qwen3_status fail(qwen3_handle* h, qwen3_status s, const std::string& msg) {
+  if (h) h->err = msg;
+  return s;
+}
+
+qwen3_status cuda_fail(qwen3_handle* h, cudaError_t e, const char* what) {
+  return fail(h, QWEN3_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool is_moe_layer(const qwen3_handle* h, int layer) {
+  const qwen3_config& c = h->cfg;
+  if (c.num_experts <= 0) return false;
+  for (int32_t l : h->mlp_only)
+    if (l == layer) return false;
+  return (layer + 1) % c.decoder_sparse_step == 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Round a double to the model dtype, ties to even: x = m * 2^e with
+// 0.5 <= |m| < 1; keep 8 (bf16) or 24 (fp32) significant bits of m.
+double round_to_dtype(double x, int dt) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int e = 0;
+  const double m = std::frexp(x, &e);
+  const int bits = dt == QWEN3_DTYPE_BF16 ? 8 : 24;
+  return std::ldexp(std::nearbyint(std::ldexp(m, bits)), e - bits);
+}
+
+qwen3_status ensure(qwen3_handle* h, DevBuf& b, size_t bytes, bool zero = false) {
+  if (bytes <= b.bytes) return QWEN3_OK;
+  size_t nb = std::max(bytes, b.bytes + b.bytes / 2);
+  nb = (nb + 255) & ~size_t(255);
+  void* p = nullptr;
+  if (cudaMalloc(&p, nb) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, QWEN3_E_OOM, "device allocation of " + std::to_string(nb) + " bytes failed");
+  }
+  if (zero) cudaMemset(p, 0, nb);
+  if (b.p) {
+    cudaDeviceSynchronize();
+    cudaFree(b.p);
+  }
+  b.p = p;
+  b.bytes = nb;
+  h->ws_generation++;
+  return QWEN3_OK;
+}
+
+// ---------------------------------------------------------------- profiling
+cudaEvent_t pool_event(qwen3_handle* h) {
+  if (!h->ev_pool.empty()) {
+    cudaEvent_t e = h->ev_pool.back();
+    h->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct Launcher {
+  qwen3_handle* h;
+  LaunchCtx ctx;
+  int count = 0;
+};
+
+// Every kernel launch of a forward goes through here so that profiling can
+// bracket it with events and the launch count is known.
+template <typename F>
+cudaError_t launch(Launcher& L, const char* name, F&& fn) {
+  qwen3_handle* h = L.h;
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (h->profile) {
+    a = pool_event(h);
+    b = pool_event(h);
+    cudaEventRecord(a, L.ctx.stream);
+  }
+  cudaError_t e = fn();
+  L.count++;
+  if (h->profile) {
+    cudaEventRecord(b, L.ctx.stream);
+    h->prof_pending.push_back({name, a, b});
+  }
+  return e;
+}
+
+}  // namespace
+
+// ======================================================================
+// C ABI
+// ======================================================================
+extern "C" {
+
+const char* qwen3_status_string(qwen3_status s) {
+  switch (s) {
+    case QWEN3_OK: return "ok";
+    case QWEN3_E_ARG: return "invalid argument";
+    case QWEN3_E_DTYPE: return "dtype must be fp32 or bf16";
+    case QWEN3_E_CAPACITY: return "context exceeds capacity";
+    case QWEN3_E_POSITION: return "positions do not continue the cache";
+    case QWEN3_E_SEQ: return "bad sequence id";
+    case QWEN3_E_OOM: return "out of device memory";
+    case QWEN3_E_CUDA: return "CUDA error";
+    case QWEN3_E_UNSUPPORTED: return "unsupported configuration";
+    case QWEN3_E_DEVICE: return "no usable device";
+  }
+  return "unknown status";
+}
+
+const char* qwen3_last_error(const qwen3_handle* h) { return h ? h->err.c_str() : "null handle"; }
+
+qwen3_status qwen3_check_config(const qwen3_config* c) {
+  if (!c) return QWEN3_E_ARG;
+  if (c->dtype != QWEN3_DTYPE_F32 && c->dtype != QWEN3_DTYPE_BF16) return QWEN3_E_DTYPE;
+  if (c->num_layers < 1 || c->hidden < 64 || c->hidden % 64 || c->hidden > 8192) return QWEN3_E_ARG;
+  if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) return QWEN3_E_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return QWEN3_E_UNSUPPORTED;
+  if (c->n_heads / c->n_kv_heads > 16) return QWEN3_E_UNSUPPORTED;
+  if ((c->n_heads * c->head_dim) % 64 || c->n_heads * c->head_dim > 8192) return QWEN3_E_UNSUPPORTED;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 1.0)) return QWEN3_E_ARG;
+  if (c->capacity < 1 || c->max_seqs < 1) return QWEN3_E_ARG;
+  if (c->weight_format != QWEN3_WEIGHTS_DENSE && c->weight_format != QWEN3_WEIGHTS_INT8) return QWEN3_E_ARG;
+  if (c->weight_format == QWEN3_WEIGHTS_INT8) {
+    if (c->dtype != QWEN3_DTYPE_BF16) return QWEN3_E_UNSUPPORTED;
+    if (c->group_size < 16 || c->group_size % 16 || c->hidden % c->group_size) return QWEN3_E_ARG;
+  }
+  if (c->num_experts < 0) return QWEN3_E_ARG;
+  const bool has_dense = c->num_experts == 0 || c->decoder_sparse_step != 1 || c->n_mlp_only_layers > 0;
+  if (has_dense) {
+    if (c->intermediate < 64 || c->intermediate % 64 || c->intermediate > 16384) return QWEN3_E_ARG;
+    if (c->weight_format == QWEN3_WEIGHTS_INT8 && c->intermediate % c->group_size) return QWEN3_E_ARG;
+  }
+  if (c->num_experts > 0) {
+    if (c->num_experts > 256 || c->top_k < 1 || c->top_k > c->num_experts || c->top_k > 32) return QWEN3_E_ARG;
+    if (c->moe_intermediate < 64 || c->moe_intermediate % 64 || c->moe_intermediate > 8192) return QWEN3_E_ARG;
+    if (c->decoder_sparse_step < 1) return QWEN3_E_ARG;
+    if (c->weight_format != QWEN3_WEIGHTS_DENSE) return QWEN3_E_UNSUPPORTED;
+    if (c->n_mlp_only_layers < 0 || (c->n_mlp_only_layers > 0 && !c->mlp_only_layers)) return QWEN3_E_ARG;
+  }
+  const double cache_elems = 2.0 * c->max_seqs * c->num_layers * c->n_kv_heads * (double)c->capacity * c->head_dim;
+  if (cache_elems > 1.2e12) return QWEN3_E_ARG;
+  return QWEN3_OK;
+}
+
+qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* layers, const void* final_norm,
+                          qwen3_handle** out) {
+  if (!out) return QWEN3_E_ARG;
+  *out = nullptr;
+  qwen3_status st = qwen3_check_config(cfg);
+  if (st != QWEN3_OK) return st;
+  if (!layers || !final_norm) return QWEN3_E_ARG;
+  qwen3_handle* h = new qwen3_handle();
+  h->cfg = *cfg;
+  if (cfg->n_mlp_only_layers > 0) h->mlp_only.assign(cfg->mlp_only_layers, cfg->mlp_only_layers + cfg->n_mlp_only_layers);
+  h->cfg.mlp_only_layers = nullptr;
+  h->layers.assign(layers, layers + cfg->num_layers);
+  h->final_norm = final_norm;
+  h->dt = cfg->dtype == QWEN3_DTYPE_BF16 ? DT_BF16 : DT_F32;
+  h->wfmt = cfg->weight_format == QWEN3_WEIGHTS_INT8 ? W_U8 : W_DT;
+  h->esz = cfg->dtype == QWEN3_DTYPE_BF16 ? 2 : 4;
+  const bool int8 = cfg->weight_format == QWEN3_WEIGHTS_INT8;
+  auto bad = [&](const char* what, int l) {
+    h->err = std::string("layer ") + std::to_string(l) + ": " + what;
+    return QWEN3_E_ARG;
+  };
+  if (!aligned16(final_norm)) { delete h; return QWEN3_E_ARG; }
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const qwen3_layer_weights& w = layers[l];
+    qwen3_status s = QWEN3_OK;
+    auto lin_ok = [&](const qwen3_linear& L) {
+      if (!L.w || !aligned16(L.w)) return false;
+      if (int8 && (!L.scale || !L.bias)) return false;
+      return true;
+    };
+    if (!w.in_norm || !w.post_norm || !w.q_norm || !w.k_norm || !aligned16(w.in_norm) || !aligned16(w.post_norm))
+      s = bad("missing or misaligned norm gain", l);
+    else if (!lin_ok(w.qkv) || !lin_ok(w.o)) s = bad("missing attention weights", l);
+    else if (is_moe_layer(h, l)) {
+      if (!w.router || !w.exp_gate_up || !w.exp_down || !aligned16(w.router) || !aligned16(w.exp_gate_up) ||
+          !aligned16(w.exp_down))
+        s = bad("missing MoE weights", l);
+    } else if (!lin_ok(w.gate_up) || !lin_ok(w.down)) {
+      s = bad("missing MLP weights", l);
+    }
+    if (s != QWEN3_OK) {
+      qwen3_status r = s;
+      delete h;
+      return r;
+    }
+  }
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    delete h;
+    return QWEN3_E_DEVICE;
+  }
+  cudaGetDevice(&h->device);
+  cudaDeviceProp prop;
+  cudaGetDeviceProperties(&prop, h->device);
+  if (prop.major < 10) {
+    delete h;
+    return QWEN3_E_DEVICE;
+  }
+  h->num_sms = prop.multiProcessorCount;
+  const qwen3_config& c = h->cfg;
+  h->layer_stride = (size_t)c.n_kv_heads * c.capacity * c.head_dim;
+  h->seq_stride = h->layer_stride * c.num_layers;
+  const size_t cache_bytes = h->seq_stride * c.max_seqs * h->esz;
+  if (cudaMalloc(&h->kcache, cache_bytes) != cudaSuccess || cudaMalloc(&h->vcache, cache_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    qwen3_destroy(h);
+    return QWEN3_E_OOM;
+  }
+  cudaMemset(h->kcache, 0, cache_bytes);
+  cudaMemset(h->vcache, 0, cache_bytes);
+  // RoPE table: inv_freq_i = theta^(-2i/D) rounded to dt; angle p * inv_freq in
+  // double; cos / sin rounded to dt; both halves of a row repeat the frequencies.
+  const int D = c.head_dim, half = D / 2;
+  std::vector<double> inv(half);
+  for (int i = 0; i < half; ++i) inv[i] = round_to_dtype(std::pow(c.rope_theta, -2.0 * i / D), c.dtype);
+  std::vector<float> cs((size_t)c.capacity * D), sn((size_t)c.capacity * D);
+  for (int p = 0; p < c.capacity; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double ang = (double)p * inv[i];
+      const float cv = (float)round_to_dtype(std::cos(ang), c.dtype);
+      const float sv = (float)round_to_dtype(std::sin(ang), c.dtype);
+      cs[(size_t)p * D + i] = cs[(size_t)p * D + i + half] = cv;
+      sn[(size_t)p * D + i] = sn[(size_t)p * D + i + half] = sv;
+    }
+  if (cudaMalloc(&h->rope_cos, cs.size() * 4) != cudaSuccess ||
+      cudaMalloc(&h->rope_sin, sn.size() * 4) != cudaSuccess) {
+    cudaGetLastError();
+    qwen3_destroy(h);
+    return QWEN3_E_OOM;
+  }
+  cudaMemcpy(h->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
+  cudaMemcpy(h->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
+  h->lengths.assign(c.max_seqs, 0);
+  for (int i = 0; i < qwen3_handle::kRing; ++i) cudaEventCreateWithFlags(&h->pinned_ev[i], cudaEventDisableTiming);
+  cudaStreamCreateWithFlags(&h->gstream, cudaStreamNonBlocking);
+  cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming);
+  cudaEventCreateWithFlags(&h->ev_out, cudaEventDisableTiming);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    qwen3_destroy(h);
+    return QWEN3_E_CUDA;
+  }
+  *out = h;
+  return QWEN3_OK;
+}
+
+void qwen3_destroy(qwen3_handle* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
+  DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
+                    &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
+                    &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc};
+  for (DevBuf* b : bufs)
+    if (b->p) cudaFree(b->p);
+  for (int i = 0; i < qwen3_handle::kRing; ++i) {
+    if (h->pinned[i]) cudaFreeHost(h->pinned[i]);
+    if (h->pinned_ev[i]) cudaEventDestroy(h->pinned_ev[i]);
+  }
+  for (auto& p : h->prof_pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (auto e : h->ev_pool) cudaEventDestroy(e);
+  if (h->gstream) cudaStreamDestroy(h->gstream);
+  if (h->ev_in) cudaEventDestroy(h->ev_in);
+  if (h->ev_out) cudaEventDestroy(h->ev_out);
+  if (h->kcache) cudaFree(h->kcache);
+  if (h->vcache) cudaFree(h->vcache);
+  if (h->rope_cos) cudaFree(h->rope_cos);
+  if (h->rope_sin) cudaFree(h->rope_sin);
+  delete h;
+}
+
+qwen3_status qwen3_reset(qwen3_handle* h, int32_t seq, void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  if (seq < -1 || seq >= h->cfg.max_seqs) return fail(h, QWEN3_E_SEQ, "sequence id out of range");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = h->seq_stride * h->esz;
+  const int s0 = seq < 0 ? 0 : seq, s1 = seq < 0 ? h->cfg.max_seqs : seq + 1;
+  for (int i = s0; i < s1; ++i) {
+    cudaError_t e1 = cudaMemsetAsync(static_cast<char*>(h->kcache) + i * bytes, 0, bytes, s);
+    cudaError_t e2 = cudaMemsetAsync(static_cast<char*>(h->vcache) + i * bytes, 0, bytes, s);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) return cuda_fail(h, e1 != cudaSuccess ? e1 : e2, "reset");
+    h->lengths[i] = 0;
+  }
+  return QWEN3_OK;
+}
+
+qwen3_status qwen3_cache_view(qwen3_handle* h, int32_t seq, int32_t layer, void** k, void** v) {
+  if (!h || !k || !v) return QWEN3_E_ARG;
+  if (seq < 0 || seq >= h->cfg.max_seqs) return fail(h, QWEN3_E_SEQ, "sequence id out of range");
+  if (layer < 0 || layer >= h->cfg.num_layers) return fail(h, QWEN3_E_ARG, "layer out of range");
+  const size_t off = (seq * h->seq_stride + layer * h->layer_stride) * h->esz;
+  *k = static_cast<char*>(h->kcache) + off;
+  *v = static_cast<char*>(h->vcache) + off;
+  return QWEN3_OK;
+}
+
+qwen3_status qwen3_set_length(qwen3_handle* h, int32_t seq, int32_t length) {
+  if (!h) return QWEN3_E_ARG;
+  if (seq < 0 || seq >= h->cfg.max_seqs) return fail(h, QWEN3_E_SEQ, "sequence id out of range");
+  if (length < 0 || length > h->cfg.capacity) return fail(h, QWEN3_E_CAPACITY, "length exceeds capacity");
+  h->lengths[seq] = length;
+  return QWEN3_OK;
+}
+
+qwen3_status qwen3_get_length(const qwen3_handle* h, int32_t seq, int32_t* length) {
+  if (!h || !length) return QWEN3_E_ARG;
+  if (seq < 0 || seq >= h->cfg.max_seqs) return QWEN3_E_SEQ;
+  *length = h->lengths[seq];
+  return QWEN3_OK;
+}
+
+qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value) {
+  if (!h) return QWEN3_E_ARG;
+  switch (option) {
+    case QWEN3_OPT_CUDA_GRAPHS: h->use_graphs = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_PROFILE: h->profile = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_PDL: h->pdl = value != 0; return QWEN3_OK;
+  }
+  return fail(h, QWEN3_E_ARG, "unknown option");
+}
+
+qwen3_status qwen3_profile_reset(qwen3_handle* h) {
+  if (!h) return QWEN3_E_ARG;
+  cudaDeviceSynchronize();
+  for (auto& p : h->prof_pending) {
+    h->ev_pool.push_back(p.a);
+    h->ev_pool.push_back(p.b);
+  }
+  h->prof_pending.clear();
+  h->prof_acc.clear();
+  h->prof_names.clear();
+  return QWEN3_OK;
+}
+
+qwen3_status qwen3_profile_read(qwen3_handle* h, int32_t i, const char** name, int64_t* launches, double* total_ms,
+                                int32_t* count) {
+  if (!h) return QWEN3_E_ARG;
+  if (!h->prof_pending.empty()) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, e, "profile sync");
+    for (auto& p : h->prof_pending) {
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, p.a, p.b);
+      auto& acc = h->prof_acc[p.name];
+      acc.first += 1;
+      acc.second += ms;
+      h->ev_pool.push_back(p.a);
+      h->ev_pool.push_back(p.b);
+    }
+    h->prof_pending.clear();
+    h->prof_names.clear();
+    for (auto& kv : h->prof_acc) h->prof_names.push_back(kv.first);
+  }
+  if (count) *count = (int32_t)h->prof_names.size();
+  if (i < 0 || i >= (int32_t)h->prof_names.size()) return QWEN3_OK;
+  const auto& acc = h->prof_acc[h->prof_names[i]];
+  if (name) *name = h->prof_names[i].c_str();
+  if (launches) *launches = acc.first;
+  if (total_ms) *total_ms = acc.second;
+  return QWEN3_OK;
+}
+
+int64_t qwen3_last_launch_count(const qwen3_handle* h) { return h ? h->last_launches : 0; }
+
+}  // extern "C"
+
+// ======================================================================
+// forward
+// ======================================================================
+namespace {
+
+struct Plan {
+  int T = 0;
+  bool decode = false;        // GEMV path for the linears
+  bool attn_prefill = false;  // prefill attention kernel
+  int rows_per_block = 1;
+  int n_qblocks = 0, n_items = 0, n_parts = 0;
+  std::vector<int32_t> blob;  // row_seq[T] row_pos[T] n_items qblocks items
+  size_t off_rowseq = 0, off_rowpos = 0, off_nitems = 0, off_qb = 0, off_items = 0;
+};
+
+// Validate rows and build the attention work list (host only; no state change).
+qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const int32_t* positions, Plan& P) {
+  const qwen3_config& c = h->cfg;
+  const int G = c.n_heads / c.n_kv_heads;
+  struct Seg { int seq, row0, n, pos0; };
+  std::vector<Seg> segs;
+  std::vector<char> seen(c.max_seqs, 0);
+  for (int t = 0; t < T; ++t) {
+    const int s = seq_ids[t];
+    if (s < 0 || s >= c.max_seqs) return fail(h, QWEN3_E_SEQ, "row " + std::to_string(t) + ": sequence id out of range");
+    if (segs.empty() || segs.back().seq != s) {
+      if (seen[s]) return fail(h, QWEN3_E_SEQ, "rows of sequence " + std::to_string(s) + " are not consecutive");
+      seen[s] = 1;
+      segs.push_back({s, t, 0, h->lengths[s]});
+    }
+    Seg& g = segs.back();
+    const int expect = g.pos0 + g.n;
+    if (expect >= c.capacity)
+      return fail(h, QWEN3_E_CAPACITY, "context " + std::to_string(expect + 1) + " exceeds capacity " +
+                                           std::to_string(c.capacity));
+    if (positions[t] != expect)
+      return fail(h, QWEN3_E_POSITION, "row " + std::to_string(t) + " of sequence " + std::to_string(s) +
+                                           " at position " + std::to_string(positions[t]) + ", expected " +
+                                           std::to_string(expect));
+    g.n++;
+  }
+  P.T = T;
+  P.decode = T <= 4;
+  int max_rows = 0;
+  for (auto& g : segs) max_rows = std::max(max_rows, g.n);
+  P.attn_prefill = max_rows * G > attn_decode_nq_max();
+  const int nq_max = P.attn_prefill ? attn_prefill_nq_max() : attn_decode_nq_max();
+  const int CK = P.attn_prefill ? attn_prefill_chunk() : attn_decode_chunk();
+  P.rows_per_block = nq_max / G;
+  std::vector<int32_t> qb, items;
+  int parts = 0, nqb = 0;
+  for (auto& g : segs) {
+    for (int r = 0; r < g.n; r += P.rows_per_block) {
+      const int nr = std::min(P.rows_per_block, g.n - r);
+      const int last_pos = g.pos0 + r + nr - 1;
+      const int nch = (last_pos + 1 + CK - 1) / CK;
+      qb.insert(qb.end(), {g.seq, g.row0 + r, nr, g.pos0 + r, nch, parts});
+      for (int ch = 0; ch < nch; ++ch) items.insert(items.end(), {nqb, ch});
+      parts += nch;
+      nqb++;
+    }
+  }
+  P.n_qblocks = nqb;
+  P.n_items = (int)items.size() / 2;
+  P.n_parts = parts;
+  P.blob.clear();
+  P.off_rowseq = 0;
+  P.blob.insert(P.blob.end(), seq_ids, seq_ids + T);
+  P.off_rowpos = P.blob.size();
+  P.blob.insert(P.blob.end(), positions, positions + T);
+  P.off_nitems = P.blob.size();
+  P.blob.push_back(P.n_items);
+  while (P.blob.size() % 4) P.blob.push_back(0);
+  P.off_qb = P.blob.size();
+  P.blob.insert(P.blob.end(), qb.begin(), qb.end());
+  // room for T query blocks so that the item list sits at an offset fixed by T
+  P.blob.resize(P.off_qb + 6 * (size_t)std::max(T, nqb), 0);
+  P.off_items = P.blob.size();
+  P.blob.insert(P.blob.end(), items.begin(), items.end());
+  return QWEN3_OK;
+}
+
+struct Bufs {  // raw pointers for one forward
+  void *hA, *hB, *pend, *y, *qkv, *q, *attn, *m;
+  float *logits, *wts, *part_o, *part_ml;
+  int *idx, *counts, *row_off, *row_cnt, *tile_start, *cursor, *sorted_tok, *sorted_src, *counters;
+  void *mexp, *zexp;
+  int32_t* desc;
+};
+
+qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
+  const qwen3_config& c = h->cfg;
+  const size_t e = h->esz;
+  const size_t Tz = (size_t)std::max(T, 1);
+  const int nq_max = P.attn_prefill ? attn_prefill_nq_max() : attn_decode_nq_max();
+  qwen3_status s;
+#define ENS(buf, bytes, zero) \
+  if ((s = ensure(h, h->buf, (bytes), zero)) != QWEN3_OK) return s;
+  ENS(hA, Tz * c.hidden * e, false);
+  ENS(hB, Tz * c.hidden * e, false);
+  ENS(pend, Tz * c.hidden * e, false);
+  ENS(y, Tz * c.hidden * e, false);
+  ENS(qkv, Tz * (c.n_heads + 2 * c.n_kv_heads) * c.head_dim * e, false);
+  ENS(q, Tz * c.n_heads * c.head_dim * e, false);
+  ENS(attn, Tz * c.n_heads * c.head_dim * e, false);
+  ENS(mbuf, Tz * std::max(c.intermediate, 64) * e, false);
+  // attention partials: sized for the worst case of this row count when graphs replay it
+  size_t parts = (size_t)std::max(P.n_parts, 1);
+  if (P.decode) {
+    const int CK = P.attn_prefill ? attn_prefill_chunk() : attn_decode_chunk();
+    parts = std::max(parts, (size_t)P.n_qblocks * ((c.capacity + CK - 1) / CK));
+  }
+  ENS(part_o, parts * c.n_kv_heads * nq_max * c.head_dim * 4, false);
+  ENS(part_ml, parts * c.n_kv_heads * nq_max * 2 * 4, false);
+  ENS(counters, (size_t)std::max(P.n_qblocks, T) * c.n_kv_heads * 4, true);
+  if (c.num_experts > 0) {
+    const size_t slots = Tz * c.top_k;
+    ENS(logits, Tz * c.num_experts * 4, false);
+    ENS(idx, slots * 4, false);
+    ENS(wts, slots * 4, false);
+    ENS(counts, (size_t)c.num_experts * 4, true);
+    ENS(row_off, (size_t)c.num_experts * 4, false);
+    ENS(row_cnt, (size_t)c.num_experts * 4, false);
+    ENS(tile_start, (size_t)(c.num_experts + 1) * 4, false);
+    ENS(cursor, (size_t)c.num_experts * 4, true);
+    ENS(sorted_tok, slots * 4, false);
+    ENS(sorted_src, slots * 4, false);
+    ENS(mexp, slots * c.moe_intermediate * e, false);
+    ENS(zexp, slots * c.hidden * e, false);
+  }
+  ENS(desc, P.blob.size() * 4 + 64, false);
+#undef ENS
+  return QWEN3_OK;
+}
+
+Bufs bufs_of(qwen3_handle* h) {
+  Bufs b;
+  b.hA = h->hA.p; b.hB = h->hB.p; b.pend = h->pend.p; b.y = h->y.p; b.qkv = h->qkv.p; b.q = h->q.p;
+  b.attn = h->attn.p; b.m = h->mbuf.p;
+  b.logits = (float*)h->logits.p; b.wts = (float*)h->wts.p; b.part_o = (float*)h->part_o.p;
+  b.part_ml = (float*)h->part_ml.p; b.idx = (int*)h->idx.p; b.counts = (int*)h->counts.p;
+  b.row_off = (int*)h->row_off.p; b.row_cnt = (int*)h->row_cnt.p; b.tile_start = (int*)h->tile_start.p;
+  b.cursor = (int*)h->cursor.p; b.sorted_tok = (int*)h->sorted_tok.p; b.sorted_src = (int*)h->sorted_src.p;
+  b.counters = (int*)h->counters.p; b.mexp = h->mexp.p; b.zexp = h->zexp.p; b.desc = (int32_t*)h->desc.p;
+  return b;
+}
+
+// Upload the plan descriptor through a pinned staging ring.
+qwen3_status upload_plan(qwen3_handle* h, const Plan& P, cudaStream_t s) {
+  const size_t bytes = P.blob.size() * 4;
+  const int i = h->ring_pos;
+  h->ring_pos = (h->ring_pos + 1) % qwen3_handle::kRing;
+  cudaEventSynchronize(h->pinned_ev[i]);
+  if (h->pinned_bytes[i] < bytes) {
+    if (h->pinned[i]) cudaFreeHost(h->pinned[i]);
+    h->pinned[i] = nullptr;
+    const size_t nb = std::max(bytes, (size_t)4096) * 2;
+    if (cudaHostAlloc(&h->pinned[i], nb, cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      h->pinned_bytes[i] = 0;
+      return fail(h, QWEN3_E_OOM, "pinned host allocation failed");
+    }
+    h->pinned_bytes[i] = nb;
+  }
+  std::memcpy(h->pinned[i], P.blob.data(), bytes);
+  cudaError_t e = cudaMemcpyAsync(h->desc.p, h->pinned[i], bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "descriptor upload");
+  cudaEventRecord(h->pinned_ev[i], s);
+  return QWEN3_OK;
+}
+
+// MoE block on y [T, hidden] -> out [T, hidden]; idx/w receive the routing.
+cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, int T, void* out, int* idx, float* w,
+                      const Bufs& B) {
+  const qwen3_config& c = h->cfg;
+  const qwen3_layer_weights& W = h->layers[layer];
+  const int E = c.num_experts, k = c.top_k, mI = c.moe_intermediate, hid = c.hidden;
+  const int dt = h->dt;
+  cudaError_t e;
+  // router logits, fp32, not rounded
+  if (T <= 4) {
+    GemvArgs g{};
+    g.T = T; g.K = hid; g.N = E; g.w = W.router; g.x_rows = T; g.prologue = 0; g.x = y;
+    g.epilogue = EPI_STORE_F32; g.out = B.logits; g.ldo = E;
+    e = launch(L, "gemv_router", [&] { return launch_gemv(L.ctx, dt, W_DT, g); });
+  } else {
+    GemmArgs g{};
+    g.M = T; g.N = E; g.K = hid; g.a = y; g.lda = hid; g.w = W.router; g.epilogue = EPI_STORE_F32;
+    g.out = B.logits; g.ldo = E;
+    e = launch(L, "gemm_router", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, g); });
+  }
+  if (e != cudaSuccess) return e;
+  const int sort_from = (64 + k - 1) / k;  // qwen3-moe.ts: sorted experts from ceil(64 / topK) rows
+  const bool unsorted = T < sort_from && (size_t)T * k * mI * 4 <= 200 * 1024 && T * k <= 64;
+  RouterArgs r{};
+  r.logits = B.logits; r.T = T; r.E = E; r.k = k; r.norm = c.norm_topk_prob; r.idx = idx; r.w = w;
+  r.counts = unsorted ? nullptr : B.counts;
+  e = launch(L, "router_topk", [&] { return launch_router_topk(L.ctx, r); });
+  if (e != cudaSuccess) return e;
+  const int slots = T * k;
+  if (unsorted) {
+    GemvArgs g{};
+    g.T = slots; g.K = hid; g.N = mI; g.w = W.exp_gate_up; g.slot_expert = idx;
+    g.w_stride = (long long)2 * mI * hid; g.slot_div = k; g.x_rows = T; g.prologue = 0; g.x = y;
+    g.epilogue = EPI_SWIGLU; g.out = B.mexp; g.ldo = mI;
+    e = launch(L, "gemv_expert_gate_up", [&] { return launch_gemv(L.ctx, dt, W_DT, g); });
+    if (e != cudaSuccess) return e;
+    GemvArgs d{};
+    d.T = slots; d.K = mI; d.N = hid; d.w = W.exp_down; d.slot_expert = idx; d.w_stride = (long long)hid * mI;
+    d.slot_div = 1; d.x_rows = slots; d.prologue = 0; d.x = B.mexp; d.epilogue = EPI_STORE; d.out = B.zexp;
+    d.ldo = hid;
+    e = launch(L, "gemv_expert_down", [&] { return launch_gemv(L.ctx, dt, W_DT, d); });
+    if (e != cudaSuccess) return e;
+  } else {
+    const int BM = gemm_simt_tile_m();
+    MoeScanArgs sc{};
+    sc.counts = B.counts; sc.E = E; sc.bm = BM; sc.row_off = B.row_off; sc.row_cnt = B.row_cnt;
+    sc.tile_start = B.tile_start; sc.cursor = B.cursor;
+    e = launch(L, "moe_scan", [&] { return launch_moe_scan(L.ctx, sc); });
+    if (e != cudaSuccess) return e;
+    MoeScatterArgs sa{};
+    sa.idx = idx; sa.T = T; sa.k = k; sa.row_off = B.row_off; sa.cursor = B.cursor; sa.sorted_tok = B.sorted_tok;
+    sa.sorted_src = B.sorted_src;
+    e = launch(L, "moe_scatter", [&] { return launch_moe_scatter(L.ctx, sa); });
+    if (e != cudaSuccess) return e;
+    const int max_tiles = (slots + BM - 1) / BM + E;
+    GemmArgs g{};
+    g.M = slots; g.N = mI; g.K = hid; g.a = y; g.lda = hid; g.a_rows = B.sorted_tok; g.w = W.exp_gate_up;
+    g.w_stride = (long long)2 * mI * hid; g.tile_start = B.tile_start; g.row_off = B.row_off;
+    g.row_cnt = B.row_cnt; g.n_groups = E; g.max_tiles = max_tiles; g.epilogue = EPI_SWIGLU; g.out = B.mexp;
+    g.ldo = mI;
+    e = launch(L, "gemm_expert_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, g); });
+    if (e != cudaSuccess) return e;
+    GemmArgs d{};
+    d.M = slots; d.N = hid; d.K = mI; d.a = B.mexp; d.lda = mI; d.w = W.exp_down; d.w_stride = (long long)hid * mI;
+    d.tile_start = B.tile_start; d.row_off = B.row_off; d.row_cnt = B.row_cnt; d.n_groups = E;
+    d.max_tiles = max_tiles; d.epilogue = EPI_STORE; d.out = B.zexp; d.ldo = hid; d.c_rows = B.sorted_src;
+    e = launch(L, "gemm_expert_down", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, d); });
+    if (e != cudaSuccess) return e;
+  }
+  MoeCombineArgs cb{};
+  cb.z = B.zexp; cb.w = w; cb.T = T; cb.k = k; cb.hidden = hid; cb.out = out;
+  return launch(L, "moe_combine", [&] { return launch_moe_combine(L.ctx, dt, cb); });
+}
+
+// Enqueue every kernel of one forward on L.ctx.stream.
+cudaError_t enqueue_forward(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
+  const qwen3_config& c = h->cfg;
+  const int T = P.T, hid = c.hidden, H = c.n_heads, KV = c.n_kv_heads, D = c.head_dim, I = c.intermediate;
+  const int dt = h->dt, wf = h->wfmt;
+  const int qkv_rows = (H + 2 * KV) * D;
+  const int32_t* row_seq = B.desc + P.off_rowseq;
+  const int32_t* row_pos = B.desc + P.off_rowpos;
+  const int32_t* n_items = B.desc + P.off_nitems;
+  cudaError_t e;
+  const void* h_in = x;   // residual stream entering the layer
+  void* h_cur = B.hA;     // residual stream of the current layer
+  bool have_pend = false;
+  for (int l = 0; l < c.num_layers; ++l) {
+    const qwen3_layer_weights& W = h->layers[l];
+    const auto wfmt_of = [&](const qwen3_linear& lin) { return lin.scale ? wf : W_DT; };
+    // --- input RMSNorm + qkv projection
+    if (P.decode) {
+      GemvArgs g{};
+      g.T = T; g.K = hid; g.N = qkv_rows; g.w = W.qkv.w; g.scale = W.qkv.scale; g.bias = W.qkv.bias;
+      // layer 0: the residual stream starts as a copy of x (no pend)
+      g.group = c.group_size; g.x_rows = T; g.prologue = 2; g.h_in = h_in; g.pend = have_pend ? B.pend : nullptr;
+      g.h_out = h_cur; g.gain = W.in_norm; g.eps = c.rms_eps; g.epilogue = EPI_STORE; g.out = B.qkv;
+      g.ldo = qkv_rows;
+      e = launch(L, "gemv_qkv", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.qkv), g); });
+    } else {
+      NormArgs n{};
+      n.h_in = h_in; n.pend = have_pend ? B.pend : nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.in_norm;
+      n.rows = T; n.hidden = hid; n.eps = c.rms_eps;
+      e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
+      if (e != cudaSuccess) return e;
+      GemmArgs g{};
+      g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
+      g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
+      e = launch(L, "gemm_qkv", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.qkv), g); });
+    }
+    if (e != cudaSuccess) return e;
+    // --- q/k norm, RoPE, cache append
+    char* kc = static_cast<char*>(h->kcache) + (size_t)l * h->layer_stride * h->esz;
+    char* vc = static_cast<char*>(h->vcache) + (size_t)l * h->layer_stride * h->esz;
+    {
+      QkRopeArgs r{};
+      r.qkv = B.qkv; r.T = T; r.H = H; r.KV = KV; r.D = D; r.q_out = B.q; r.kcache = kc; r.vcache = vc;
+      r.seq_stride = (long long)h->seq_stride; r.capacity = c.capacity; r.q_gain = W.q_norm; r.k_gain = W.k_norm;
+      r.cos_t = h->rope_cos; r.sin_t = h->rope_sin; r.row_seq = row_seq; r.row_pos = row_pos; r.eps = c.rms_eps;
+      e = launch(L, "qk_rope_cache", [&] { return launch_qk_rope_cache(L.ctx, dt, r); });
+      if (e != cudaSuccess) return e;
+    }
+    // --- attention
+    {
+      AttnArgs a{};
+      a.q = B.q; a.kc = kc; a.vc = vc; a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity;
+      a.H = H; a.KV = KV; a.D = D; a.scale = (float)(1.0 / std::sqrt((double)D));
+      a.qblocks = reinterpret_cast<const AttnQBlock*>(B.desc + P.off_qb);
+      a.items = reinterpret_cast<const AttnItem*>(B.desc + P.off_items);
+      a.n_items = n_items;
+      a.chunk = P.attn_prefill ? attn_prefill_chunk() : attn_decode_chunk();
+      a.nq_max = P.attn_prefill ? attn_prefill_nq_max() : attn_decode_nq_max();
+      a.part_o = B.part_o; a.part_ml = B.part_ml; a.counters = B.counters; a.out = B.attn;
+      a.grid_x = std::max(1, (h->num_sms * 4 + KV - 1) / KV);
+      if (!P.decode) a.grid_x = std::max(1, std::min(a.grid_x * 2, P.n_items));
+      if (P.attn_prefill) e = launch(L, "attn_prefill", [&] { return launch_attention_prefill(L.ctx, dt, a); });
+      else e = launch(L, "attn_decode", [&] { return launch_attention_decode(L.ctx, dt, a); });
+      if (e != cudaSuccess) return e;
+    }
+    // --- o projection + residual
+    if (P.decode) {
+      GemvArgs g{};
+      g.T = T; g.K = H * D; g.N = hid; g.w = W.o.w; g.scale = W.o.scale; g.bias = W.o.bias; g.group = c.group_size;
+      g.x_rows = T; g.prologue = 0; g.x = B.attn; g.epilogue = EPI_RESIDUAL; g.out = h_cur; g.ldo = hid;
+      e = launch(L, "gemv_o", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.o), g); });
+    } else {
+      GemmArgs g{};
+      g.M = T; g.N = hid; g.K = H * D; g.a = B.attn; g.lda = H * D; g.w = W.o.w; g.scale = W.o.scale;
+      g.bias = W.o.bias; g.group = c.group_size; g.epilogue = EPI_RESIDUAL; g.out = h_cur; g.ldo = hid;
+      e = launch(L, "gemm_o", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.o), g); });
+    }
+    if (e != cudaSuccess) return e;
+    // --- MLP
+    if (is_moe_layer(h, l)) {
+      NormArgs n{};
+      n.h_in = h_cur; n.pend = nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.post_norm; n.rows = T;
+      n.hidden = hid; n.eps = c.rms_eps;
+      e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
+      if (e != cudaSuccess) return e;
+      e = moe_block(h, L, l, B.y, T, B.pend, B.idx, B.wts, B);
+      if (e != cudaSuccess) return e;
+    } else if (P.decode) {
+      GemvArgs g{};
+      g.T = T; g.K = hid; g.N = I; g.w = W.gate_up.w; g.scale = W.gate_up.scale; g.bias = W.gate_up.bias;
+      g.group = c.group_size; g.x_rows = T; g.prologue = 1; g.h_in = h_cur; g.gain = W.post_norm;
+      g.eps = c.rms_eps; g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I;
+      e = launch(L, "gemv_gate_up", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.gate_up), g); });
+      if (e != cudaSuccess) return e;
+      GemvArgs d{};
+      d.T = T; d.K = I; d.N = hid; d.w = W.down.w; d.scale = W.down.scale; d.bias = W.down.bias;
+      d.group = c.group_size; d.x_rows = T; d.prologue = 0; d.x = B.m; d.epilogue = EPI_STORE; d.out = B.pend;
+      d.ldo = hid;
+      e = launch(L, "gemv_down", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.down), d); });
+      if (e != cudaSuccess) return e;
+    } else {
+      NormArgs n{};
+      n.h_in = h_cur; n.pend = nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.post_norm; n.rows = T;
+      n.hidden = hid; n.eps = c.rms_eps;
+      e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
+      if (e != cudaSuccess) return e;
+      GemmArgs g{};
+      g.M = T; g.N = I; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.gate_up.w; g.scale = W.gate_up.scale;
+      g.bias = W.gate_up.bias; g.group = c.group_size; g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I;
+      e = launch(L, "gemm_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.gate_up), g); });
+      if (e != cudaSuccess) return e;
+      GemmArgs d{};
+      d.M = T; d.N = hid; d.K = I; d.a = B.m; d.lda = I; d.w = W.down.w; d.scale = W.down.scale;
+      d.bias = W.down.bias; d.group = c.group_size; d.epilogue = EPI_STORE; d.out = B.pend; d.ldo = hid;
+      e = launch(L, "gemm_down", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.down), d); });
+      if (e != cudaSuccess) return e;
+    }
+    have_pend = true;
+    h_in = h_cur;
+    h_cur = (h_cur == B.hA) ? B.hB : B.hA;
+  }
+  // final: out = RMSNorm(R(h + pend)) with the final gain
+  NormArgs n{};
+  n.h_in = h_in; n.pend = B.pend; n.h_out = h_cur; n.y = out; n.gain = h->final_norm; n.rows = T; n.hidden = hid;
+  n.eps = c.rms_eps;
+  return launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
+}
+
+}  // namespace
+
+extern "C" qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T, const int32_t* seq_ids,
+                                      const int32_t* positions, void* out, void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  if (!x || !out || !seq_ids || !positions) return fail(h, QWEN3_E_ARG, "null pointer argument");
+  if (T < 1 || T > (1 << 20)) return fail(h, QWEN3_E_ARG, "row count out of range");
+  if (!aligned16(x) || !aligned16(out)) return fail(h, QWEN3_E_ARG, "x and out must be 16-byte aligned");
+  Plan P;
+  qwen3_status st = build_plan(h, T, seq_ids, positions, P);
+  if (st != QWEN3_OK) return st;
+  st = ensure_workspace(h, P, T);
+  if (st != QWEN3_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = upload_plan(h, P, s);
+  if (st != QWEN3_OK) return st;
+  Bufs B = bufs_of(h);
+  Launcher L{h, {s, h->pdl && !h->profile, h->num_sms}};
+  const bool graph = h->use_graphs && !h->profile && P.decode;
+  cudaError_t e;
+  if (graph) {
+    const GraphKey key{T, (P.attn_prefill ? 1 : 0), x, out};
+    if (h->graphs.size() > 32) {  // callers cycling through buffers: start over
+      for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
+      h->graphs.clear();
+    }
+    auto it = h->graphs.find(key);
+    if (it != h->graphs.end() && it->second.second != h->ws_generation) {
+      cudaGraphExecDestroy(it->second.first);
+      h->graphs.erase(it);
+      it = h->graphs.end();
+    }
+    if (it == h->graphs.end()) {
+      Launcher G{h, {h->gstream, h->pdl, h->num_sms}};
+      cudaGraph_t g = nullptr;
+      e = cudaStreamBeginCapture(h->gstream, cudaStreamCaptureModeThreadLocal);
+      if (e != cudaSuccess) return cuda_fail(h, e, "graph capture begin");
+      cudaError_t ee = enqueue_forward(h, G, P, x, out, B);
+      e = cudaStreamEndCapture(h->gstream, &g);
+      if (ee != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return cuda_fail(h, ee, "graph capture");
+      }
+      if (e != cudaSuccess) return cuda_fail(h, e, "graph capture end");
+      cudaGraphExec_t ex = nullptr;
+      e = cudaGraphInstantiate(&ex, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) return cuda_fail(h, e, "graph instantiate");
+      it = h->graphs.emplace(key, std::make_pair(ex, h->ws_generation)).first;
+      h->launches = G.count;
+    }
+    // x and out are part of the key: a graph is replayed only with the buffers it was captured on.
+    cudaGraphExec_t ex = it->second.first;
+    e = cudaEventRecord(h->ev_in, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->gstream, h->ev_in, 0);
+    if (e == cudaSuccess) e = cudaGraphLaunch(ex, h->gstream);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_out, h->gstream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_out, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "graph launch");
+    h->last_launches = h->launches;
+  } else {
+    e = enqueue_forward(h, L, P, x, out, B);
+    if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+    h->last_launches = L.count;
+  }
+  for (int t = 0; t < T; ++t) h->lengths[seq_ids[t]] = positions[t] + 1;
+  return QWEN3_OK;
+}
+
+extern "C" qwen3_status qwen3_moe_layer(qwen3_handle* h, int32_t layer, const void* y, int32_t T, void* out,
+                                        int32_t* topk_idx, float* topk_w, void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  if (!y || !out || !topk_idx || !topk_w) return fail(h, QWEN3_E_ARG, "null pointer argument");
+  if (layer < 0 || layer >= h->cfg.num_layers || !is_moe_layer(h, layer))
+    return fail(h, QWEN3_E_ARG, "layer is not a MoE layer");
+  if (T < 1 || T > (1 << 20)) return fail(h, QWEN3_E_ARG, "row count out of range");
+  Plan P;
+  P.T = T;
+  P.decode = T <= 4;
+  qwen3_status st = ensure_workspace(h, P, T);
+  if (st != QWEN3_OK) return st;
+  Bufs B = bufs_of(h);
+  Launcher L{h, {static_cast<cudaStream_t>(stream), h->pdl && !h->profile, h->num_sms}};
+  cudaError_t e = moe_block(h, L, layer, y, T, out, topk_idx, topk_w, B);
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  h->last_launches = L.count;
+  return QWEN3_OK;
+}
