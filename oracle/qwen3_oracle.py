@@ -197,7 +197,11 @@ class Qwen3Oracle:
 
     def matmul(self, x, lw):
         """x [T, in] @ W^T, float64 accumulation (Q.mm), not rounded here."""
-        return np.asarray(x, dtype=np.float64) @ self.linear_weight(lw).T
+        return self._mm(x, self.linear_weight(lw))
+
+    def _mm(self, x, W):
+        """x @ W^T for an explicit float64 matrix W [out, in]."""
+        return np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
 
     # -- cache ---------------------------------------------------------------
     def _seq(self, s: int):
@@ -343,13 +347,28 @@ class Qwen3Oracle:
         for e in np.unique(idx):
             tt, ss = np.nonzero(idx == e)
             xe = y2[tt]
-            Wgu = L["exp_gate_up"]["w"][e].astype(np.float64)
-            g = R(xe @ Wgu[:mI].T)
-            u = R(xe @ Wgu[mI:].T)
+            Wgu = L["exp_gate_up"]["w"][e]
+            g = R(self._mm(xe, Wgu[:mI]))
+            u = R(self._mm(xe, Wgu[mI:]))
             m = R(R(silu(g)) * u)
-            z[tt, ss] = R(m @ L["exp_down"]["w"][e].astype(np.float64).T)
+            z[tt, ss] = R(self._mm(m, L["exp_down"]["w"][e]))
         pend = R(np.einsum("tk,tkh->th", w, z))
         return pend, idx, w
+
+
+class Qwen3OracleF32Acc(Qwen3Oracle):
+    """The same forward with every weight product accumulated in float32
+    (NumPy's float32 GEMM) instead of float64 -- NOT a reference.
+
+    Two correct implementations of the bf16 rounding points that differ only
+    in how they sum drift apart: every rounding whose exact value lies within
+    the summation error of a tie can go either way, and a one-ulp change in one
+    input of a wide projection moves every output of the next one.  The distance
+    between this class and Qwen3Oracle on the same inputs measures that drift,
+    which sets the envelope the GPU's bf16 results are held to."""
+
+    def _mm(self, x, W):
+        return (np.asarray(x, dtype=np.float32) @ np.asarray(W, dtype=np.float32).T).astype(np.float64)
 
 
 def _store(t):

@@ -19,6 +19,21 @@ template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __flo
 // Round an fp32 value to the model dtype and back (round to nearest even).
 template <typename Dt> __device__ __forceinline__ float rd(float x) { return to_f(from_f<Dt>(x)); }
 
+// Round a double straight to the model dtype (one rounding, ties to even) and
+// return it as fp32 (exact: the result has at most 24 significant bits).
+// bf16: keep 8 significant bits of the double's 53 by adding half of the
+// dropped 45-bit field (minus one unless the kept lsb is odd) and truncating.
+// Normal-range values only, which is every value rounded here.
+template <typename Dt> __device__ __forceinline__ float rd_d(double x);
+template <> __device__ __forceinline__ float rd_d<float>(double x) { return __double2float_rn(x); }
+template <> __device__ __forceinline__ float rd_d<__nv_bfloat16>(double x) {
+  unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  const unsigned long long lsb = (b >> 45) & 1ull;
+  b += (1ull << 44) - 1ull + lsb;
+  b &= ~((1ull << 45) - 1ull);
+  return (float)__longlong_as_double((long long)b);
+}
+
 // Unpack 16 bytes of a dtype into fp32 (8 bf16 or 4 fp32).
 template <typename Dt> struct Vec16;
 template <> struct Vec16<bf16> {
@@ -97,6 +112,36 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   float t = (lane < nw) ? red[lane] : 0.f;
   return warp_sum(t);
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum of doubles over the block; `red` must hold 32 doubles.
+__device__ __forceinline__ double block_sum_d(double v, double* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_sum_d(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  double t = (lane < nw) ? red[lane] : 0.0;
+  return warp_sum_d(t);
+}
+
+// RMSNorm scale 1/sqrt(mean + eps) from a sum of squares, in double.
+__device__ __forceinline__ double rms_scale(double sumsq, int n, float eps) {
+  return 1.0 / sqrt(sumsq / (double)n + (double)eps);
+}
+
+// Qwen3 RMSNorm output element with its two roundings: R(R(h * rs) * g).
+// h * rs is formed in double and rounded once; R(.) * g is exact in fp32
+// for bf16 operands and rounded once.
+template <typename Dt>
+__device__ __forceinline__ float rms_apply(float h, double rs, float g) {
+  return rd<Dt>(rd_d<Dt>((double)h * rs) * g);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }

@@ -49,7 +49,7 @@ template <typename Dt> struct WTraits<Dt, W_U8> {
 
 // Stage the input rows as fp32 in shared memory, applying the prologue.
 template <typename Dt>
-__device__ void stage_x(const GemvArgs& a, float* xs, float* red) {
+__device__ void stage_x(const GemvArgs& a, float* xs, double* red) {
   const int K = a.K;
   for (int t = 0; t < a.x_rows; ++t) {
     float* xt = xs + (size_t)t * K;
@@ -61,25 +61,25 @@ __device__ void stage_x(const GemvArgs& a, float* xs, float* red) {
     const Dt* hi = static_cast<const Dt*>(a.h_in) + (size_t)t * K;
     const Dt* pe = (a.prologue == 2 && a.pend) ? static_cast<const Dt*>(a.pend) + (size_t)t * K : nullptr;
     Dt* ho = (a.prologue == 2 && blockIdx.x == 0) ? static_cast<Dt*>(a.h_out) + (size_t)t * K : nullptr;
-    float ss = 0.f;
+    double ss = 0.0;
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
       float h = to_f(hi[k]);
       if (pe) h = rd<Dt>(h + to_f(pe[k]));
       if (ho) ho[k] = from_f<Dt>(h);
       xt[k] = h;
-      ss = fmaf(h, h, ss);
+      ss = fma((double)h, (double)h, ss);
     }
-    ss = block_sum(ss, red);
-    const float rs = rsqrtf(ss / (float)K + a.eps);
+    ss = block_sum_d(ss, red);
+    const double rs = rms_scale(ss, K, a.eps);
     const Dt* g = static_cast<const Dt*>(a.gain);
-    for (int k = threadIdx.x; k < K; k += blockDim.x) xt[k] = rd<Dt>(rd<Dt>(xt[k] * rs) * to_f(g[k]));
+    for (int k = threadIdx.x; k < K; k += blockDim.x) xt[k] = rms_apply<Dt>(xt[k], rs, to_f(g[k]));
   }
 }
 
 template <typename Dt, int WF, int NT, int EPI>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
   extern __shared__ float xs[];
-  __shared__ float red[32];
+  __shared__ double red[32];
   using W = WTraits<Dt, WF>;
   constexpr bool PAIR = (EPI == EPI_SWIGLU);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
