@@ -274,15 +274,15 @@ class Qwen3Oracle:
         for li, L in enumerate(self.layers):
             if pend is not None:
                 h = R(h + pend)                                   # one rounding
-            y = rms_norm(h, L["in_norm"], cfg.rms_eps, self.prec)
+            y = self.rms(h, L["in_norm"])
             qkv = R(self.matmul(y, L["qkv"]))
             q = qkv[:, :H * D].reshape(T, H, D)
             k = qkv[:, H * D:(H + KV) * D].reshape(T, KV, D)
             v = qkv[:, (H + KV) * D:].reshape(T, KV, D)
-            q = rms_norm(q, L["q_norm"], cfg.rms_eps, self.prec)    # per head, over D
-            k = rms_norm(k, L["k_norm"], cfg.rms_eps, self.prec)
-            q = rope(q, cos_p, sin_p, self.prec)
-            k = rope(k, cos_p, sin_p, self.prec)
+            q = self.rms(q, L["q_norm"])                            # per head, over D
+            k = self.rms(k, L["k_norm"])
+            q = self.rope(q, cos_p, sin_p)
+            k = self.rope(k, cos_p, sin_p)
             # cache append: post-RoPE k and raw v at each row's position
             for t in range(T):
                 c = self._seq(seq_ids[t])
@@ -300,12 +300,9 @@ class Qwen3Oracle:
                     j = hh // G                                          # GQA: kv head of q head hh
                     Kj = c["K"][li, j, :n_keys].astype(np.float64)
                     Vj = c["V"][li, j, :n_keys].astype(np.float64)
-                    S = (q[rows, hh, :] @ Kj.T) * scale
-                    S = np.where(visible, S, -np.inf)
-                    P = softmax(S, axis=-1)
-                    a[rows, hh, :] = R(P @ Vj)                           # fp32 softmax, one rounding
+                    a[rows, hh, :] = R(self.attend(q[rows, hh, :], Kj, Vj, visible, scale))
             h = R(h + R(self.matmul(a.reshape(T, H * D), L["o"])))
-            y2 = rms_norm(h, L["post_norm"], cfg.rms_eps, self.prec)
+            y2 = self.rms(h, L["post_norm"])
             if cfg.is_moe_layer(li):
                 pend, idx, w = self.moe_block(li, y2)
                 moe_trace.append((idx, w))
@@ -316,8 +313,24 @@ class Qwen3Oracle:
                               "h": h, "y2": y2, "pend": pend})
         for t in range(T):
             self._seq(seq_ids[t])["length"] = positions[t] + 1
-        out = rms_norm(R(h + pend), self.final_norm, cfg.rms_eps, self.prec)
+        out = self.rms(R(h + pend), self.final_norm)
         return (out, moe_trace) if return_moe else out
+
+    # -- the steps, one method each (the twin below restates them in float32)
+    def rms(self, v, gain):
+        return rms_norm(v, gain, self.cfg.rms_eps, self.prec)
+
+    def rope(self, x, cos_p, sin_p):
+        return rope(x, cos_p, sin_p, self.prec)
+
+    def attend(self, q, K, V, visible, scale):
+        """Unrounded attention output of query rows q [n, D] over keys K, V
+        [m, D] with a visibility mask [n, m]: softmax(q K^T * scale) V."""
+        S = np.where(visible, (q @ K.T) * scale, -np.inf)
+        return softmax(S, axis=-1) @ V
+
+    def silu(self, g):
+        return silu(g)
 
     def dense_mlp(self, L, y2):
         """gu = R(y2 Wgu^T); act = R(silu(g)) in wide precision; pend = R(R(act*u) Wd^T)
@@ -325,7 +338,7 @@ class Qwen3Oracle:
         R = lambda a: rnd(a, self.prec)
         I = self.cfg.intermediate
         gu = R(self.matmul(y2, L["gate_up"]))
-        act = R(silu(gu[:, :I]))
+        act = R(self.silu(gu[:, :I]))
         return R(self.matmul(R(act * gu[:, I:]), L["down"]))
 
     def moe_block(self, li: int, y2):
@@ -350,25 +363,54 @@ class Qwen3Oracle:
             Wgu = L["exp_gate_up"]["w"][e]
             g = R(self._mm(xe, Wgu[:mI]))
             u = R(self._mm(xe, Wgu[mI:]))
-            m = R(R(silu(g)) * u)
+            m = R(R(self.silu(g)) * u)
             z[tt, ss] = R(self._mm(m, L["exp_down"]["w"][e]))
         pend = R(np.einsum("tk,tkh->th", w, z))
         return pend, idx, w
 
 
 class Qwen3OracleF32Acc(Qwen3Oracle):
-    """The same forward with every weight product accumulated in float32
-    (NumPy's float32 GEMM) instead of float64 -- NOT a reference.
+    """The same forward restated in float32 arithmetic -- NOT a reference.
 
-    Two correct implementations of the bf16 rounding points that differ only
-    in how they sum drift apart: every rounding whose exact value lies within
-    the summation error of a tie can go either way, and a one-ulp change in one
-    input of a wide projection moves every output of the next one.  The distance
-    between this class and Qwen3Oracle on the same inputs measures that drift,
-    which sets the envelope the GPU's bf16 results are held to."""
+    Every step the pages state in fp32 (RMSNorm statistics, RoPE, the softmax,
+    SiLU) and every weight product (NumPy's float32 GEMM) is computed in
+    float32 here, rounding to the model dtype at the same points.  Two correct
+    implementations of these rounding points that differ only in how they
+    compute between them drift apart: a rounding whose exact value lies within
+    the arithmetic error of a tie can go either way, and a one-ulp change in
+    one input of a wide projection moves every output of the next one.  The
+    distance between this class and Qwen3Oracle on the same inputs measures
+    that drift, and sets the envelope the GPU's bf16 results are held to."""
 
     def _mm(self, x, W):
         return (np.asarray(x, dtype=np.float32) @ np.asarray(W, dtype=np.float32).T).astype(np.float64)
+
+    def rms(self, v, gain):
+        v32 = np.asarray(v, dtype=np.float32)
+        ms = np.mean(v32 * v32, axis=-1, keepdims=True, dtype=np.float32)
+        n = rnd((v32 * (np.float32(1.0) / np.sqrt(ms + np.float32(self.cfg.rms_eps)))).astype(np.float64),
+                self.prec)
+        return rnd((n.astype(np.float32) * np.asarray(gain, dtype=np.float32)).astype(np.float64), self.prec)
+
+    def rope(self, x, cos_p, sin_p):
+        x32 = np.asarray(x, dtype=np.float32)
+        c, s_ = cos_p.astype(np.float32), sin_p.astype(np.float32)
+        half = x32.shape[-1] // 2
+        y1, y2 = x32[..., :half], x32[..., half:]
+        o = np.concatenate([y1 * c[..., :half] - y2 * s_[..., :half],
+                            y2 * c[..., half:] + y1 * s_[..., half:]], axis=-1)
+        return rnd(o.astype(np.float64), self.prec)
+
+    def attend(self, q, K, V, visible, scale):
+        S = (np.asarray(q, np.float32) @ np.asarray(K, np.float32).T) * np.float32(scale)
+        S = np.where(visible, S, np.float32(-np.inf))
+        P = np.exp(S - S.max(axis=-1, keepdims=True))
+        out = (P @ np.asarray(V, np.float32)) / P.sum(axis=-1, keepdims=True, dtype=np.float32)
+        return out.astype(np.float64)
+
+    def silu(self, g):
+        g32 = np.asarray(g, dtype=np.float32)
+        return (g32 / (np.float32(1.0) + np.exp(-g32))).astype(np.float64)
 
 
 def _store(t):

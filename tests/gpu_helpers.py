@@ -2,13 +2,15 @@
 run the library and the oracle on the same values, and check the error metric
 max|gpu - oracle| / rms(oracle) of the final-norm output.
 
-Tolerances.  fp32: 1e-4.  bf16: 2e-2, or 1.5 x the drift between the oracle
-and its float32-accumulating twin (oracle.Qwen3OracleF32Acc) on the same
-inputs, whichever is larger.  The twin term matters only for wide or deep
-stacks: there any two correct bf16 implementations that sum in different
-orders disagree by more than 2e-2 (measured: ~10% max-abs/RMS after 28
-layers of the 1.7B-shaped stack), so no GPU kernel can meet 2e-2 there; on
-small stacks the twin is bit-identical to the oracle and the bound is 2e-2."""
+Tolerances.  fp32: 1e-4.  bf16: 2e-2, or 2 x the drift between the oracle
+and its float32 twin (oracle.Qwen3OracleF32Acc, the same rounding points with
+float32 arithmetic between them) on the same inputs, whichever is larger.
+The twin term matters only for wide or deep stacks: there any two correct
+bf16 implementations disagree by more than 2e-2 (measured: 10-13% max-abs/RMS
+after the 28 layers of the 1.7B-shaped stack, 1-2 bf16 ulps of the largest
+output on a 3-layer 512-wide stack), so no GPU kernel can meet 2e-2 there; on
+the smallest stacks the twin is bit-identical to the oracle and the bound is
+2e-2."""
 import numpy as np
 import torch
 
@@ -17,7 +19,7 @@ from qwen3_decoder_layer_gb300 import binding as Q
 from qwen3_decoder_layer_gb300 import inputs as I
 
 TOL = {"fp32": 1e-4, "bf16": 2e-2}
-TWIN_FACTOR = 1.5
+TWIN_FACTOR = 2.0
 
 
 def as_f64(a):

@@ -60,16 +60,15 @@ def test_chunked_prefill_matches_one_pass(cuda_ok):
     w = I.make_weights(cfg, seed=1400)
     wd = to_device(w)
     x = I.make_rows(cfg, 96, seed=1401).cuda()
-    a, b, c = (Q.Qwen3Stack(cfg, wd) for _ in range(3))
-    one = a.forward(x)
-    chunks = torch.cat([b.forward(x[i:i + 24]) for i in range(0, 96, 24)])
-    toks = torch.cat([c.forward(x[i:i + 1]) for i in range(96)])
-    ref = Qwen3Oracle(cfg, w).forward(x.cpu())
-    for got in (one, chunks, toks):
-        assert rel_err(got, ref) <= TOL["bf16"]
-    assert rel_err(chunks, one) <= TOL["bf16"]
-    for s in (a, b, c):
-        s.close()
+    runs = [Parity(cfg, weights=w, device_weights=wd) for _ in range(3)]
+    one, _ = runs[0].step(x)
+    chunks = torch.cat([runs[1].step(x[i:i + 24])[0] for i in range(0, 96, 24)])
+    toks = torch.cat([runs[2].step(x[i:i + 1])[0] for i in range(96)])
+    for p in runs:
+        p.check()
+        p.close()
+    assert rel_err(chunks, one) <= runs[0].bound()
+    assert rel_err(toks, one) <= runs[0].bound()
 
 
 def test_batched_sequences_with_cached_context(cuda_ok):
