@@ -185,6 +185,12 @@ QWEN3_API qwen3_status qwen3_profile_read(qwen3_handle* h, int32_t i, const char
                                 double* total_ms, int32_t* count);
 QWEN3_API qwen3_status qwen3_profile_reset(qwen3_handle* h);
 
+/* Device-side failure report: synchronises, then returns QWEN3_E_DEVICE with
+ * *code != 0 (and clears it) if a kernel gave up a bounded wait for data it
+ * was owed (a TMA copy that never completed), QWEN3_OK with *code = 0
+ * otherwise.  Kernels never trap; they record the code and return. */
+QWEN3_API qwen3_status qwen3_device_error(qwen3_handle* h, int32_t* code);
+
 /* Number of kernel launches made by the last successful qwen3_forward. */
 QWEN3_API int64_t qwen3_last_launch_count(const qwen3_handle* h);
 

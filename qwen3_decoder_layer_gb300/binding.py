@@ -75,6 +75,7 @@ _SIGS = {
                                   _PI32]),
     "qwen3_profile_reset": (_I32, [_P]),
     "qwen3_last_launch_count": (ctypes.c_int64, [_P]),
+    "qwen3_device_error": (_I32, [_P, _PI32]),
     "qwen3_last_error": (ctypes.c_char_p, [_P]),
     "qwen3_status_string": (ctypes.c_char_p, [_I32]),
 }
@@ -220,6 +221,15 @@ def qwen3_profile_reset(h) -> None:
 
 def qwen3_last_launch_count(h) -> int:
     return int(lib().qwen3_last_launch_count(h))
+
+
+def qwen3_device_error(h) -> int:
+    """0, or the code a kernel recorded when it gave up a bounded wait."""
+    code = ctypes.c_int32()
+    st = lib().qwen3_device_error(h, ctypes.byref(code))
+    if st not in (QWEN3_OK, 9):
+        _check(h, st)
+    return code.value
 
 
 def qwen3_last_error(h) -> str:

@@ -114,6 +114,7 @@ int gemm_simt_tile_m();
 // head) combines them.
 struct AttnQBlock {
   int seq, row0, nrows, pos0, n_chunks, part_base;
+  int seg_row0, seg_pos0, seg_n, pad;  // the block's sequence rows in this call (new keys)
 };
 struct AttnItem {
   int qb, chunk;
@@ -177,14 +178,97 @@ struct MoeScatterArgs {
 };
 cudaError_t launch_moe_scatter(const LaunchCtx& c, const MoeScatterArgs& a);
 
-// out[t] = R(sum_i w[t, i] z[t k + i]) in fp32.
+// pend[t] = R(sum_i w[t, i] z[t k + i]) in fp32; written to `out`, or, when
+// h != NULL, added to the residual in place (h = R(h + pend)) with the row's
+// sum of squares stored to sumsq_out[t].
 struct MoeCombineArgs {
   const void* z;
   const float* w;
   int T, k, hidden;
   void* out;
+  void* h;
+  double* sumsq_out;
 };
 cudaError_t launch_moe_combine(const LaunchCtx& c, int dt, const MoeCombineArgs& a);
+
+// ---------------------------------------------------------------- decode path (T <= 4)
+enum Prologue { PRO_X = 0, PRO_FULL = 1, PRO_SUMSQ = 2 };
+
+// GEMV whose weight rows stream through per-warp shared-memory rings filled by
+// TMA bulk copies; the first copies are issued before waiting on the previous
+// kernel.  Prologues: PRO_X: x given (dt [T, K]); PRO_FULL: h = R(x + pend)
+// (pend optional), block 0 stores h, RMSNorm with a block reduction, block 0
+// also zeroes sumsq_zero[0 .. sumsq_zero_n); PRO_SUMSQ: RMSNorm of h from the
+// precomputed sum of squares sumsq_in[t].  EPI_RESIDUAL updates out (= h) in
+// place and adds the squares of the updated rows to sumsq_out[t].
+struct Gemv2Args {
+  int T, K, N;
+  const void* w;
+  const void* scale;
+  const void* bias;
+  int group;
+  int prologue;
+  const void* x;
+  const void* pend;
+  void* h;
+  const void* gain;
+  float eps;
+  const double* sumsq_in;
+  double* sumsq_zero;
+  int sumsq_zero_n;
+  int epilogue;
+  void* out;
+  int ldo;
+  double* sumsq_out;
+  int stages;
+  int* err;
+};
+cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a);
+// Ring slots per warp that fit, and the dynamic shared memory they need (0 = does not fit).
+int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, size_t* smem);
+
+// Decode attention with the q/k RMSNorm, RoPE and cache append fused in:
+// items as in AttnArgs; K/V chunks stream into a shared-memory ring by TMA;
+// keys appended in this call are computed from qkv inside the kernel (the
+// item that owns the row also writes them to the cache).
+struct AttnDecArgs {
+  const void* qkv;
+  int H, KV, D;
+  const void* q_gain;
+  const void* k_gain;
+  const float* cos_t;
+  const float* sin_t;
+  float eps;
+  void* kc;
+  void* vc;
+  long long seq_stride;
+  int capacity;
+  float scale;
+  const AttnQBlock* qblocks;
+  const AttnItem* items;
+  const int* n_items;
+  float* part_o;
+  float* part_ml;
+  int nq_max;
+  int* counters;
+  void* out;
+  int grid_x;
+  int* err;
+};
+cudaError_t launch_attn_decode2(const LaunchCtx& c, int dt, const AttnDecArgs& a);
+int attn_decode2_chunk(int dt);
+int attn_decode2_nq_max();
+
+// out = RMSNorm(h) * gain with the sum of squares of each row precomputed.
+struct NormApplyArgs {
+  const void* h;
+  const double* sumsq;
+  const void* gain;
+  void* out;
+  int T, hidden;
+  float eps;
+};
+cudaError_t launch_norm_apply(const LaunchCtx& c, int dt, const NormApplyArgs& a);
 
 // Shared launch helper: cudaLaunchKernelEx with the PDL attribute when asked.
 template <typename... KArgs, typename... Args>

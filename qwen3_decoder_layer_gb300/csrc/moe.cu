@@ -104,16 +104,30 @@ __global__ void moe_scatter_kernel(MoeScatterArgs a) {
 
 template <typename Dt>
 __global__ void moe_combine_kernel(MoeCombineArgs a) {
+  __shared__ double red[32];
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
   const Dt* z = static_cast<const Dt*>(a.z) + (size_t)t * a.k * a.hidden;
   const float* w = a.w + (size_t)t * a.k;
-  Dt* out = static_cast<Dt*>(a.out) + (size_t)t * a.hidden;
+  Dt* out = a.out ? static_cast<Dt*>(a.out) + (size_t)t * a.hidden : nullptr;
+  Dt* h = a.h ? static_cast<Dt*>(a.h) + (size_t)t * a.hidden : nullptr;
+  double ss = 0.0;
   for (int n = threadIdx.x; n < a.hidden; n += blockDim.x) {
     float acc = 0.f;
     for (int i = 0; i < a.k; ++i) acc = fmaf(w[i], to_f(z[(size_t)i * a.hidden + n]), acc);
-    out[n] = from_f<Dt>(acc);
+    const float pend = rd<Dt>(acc);
+    if (h) {
+      const float hn = rd<Dt>(to_f(h[n]) + pend);
+      h[n] = from_f<Dt>(hn);
+      ss = fma((double)hn, (double)hn, ss);
+    } else {
+      out[n] = from_f<Dt>(pend);
+    }
+  }
+  if (h) {
+    ss = block_sum_d(ss, red);
+    if (threadIdx.x == 0) a.sumsq_out[t] = ss;
   }
 }
 

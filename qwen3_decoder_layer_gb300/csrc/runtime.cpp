@@ -77,7 +77,7 @@ struct qwen3_handle {
   bool use_graphs = true, profile = false, pdl = true;
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
-      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc;
+      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -358,7 +358,7 @@ void qwen3_destroy(qwen3_handle* h) {
   for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
-                    &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc};
+                    &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -480,15 +480,21 @@ int64_t qwen3_last_launch_count(const qwen3_handle* h) { return h ? h->last_laun
 // ======================================================================
 namespace {
 
+enum AttnKind { ATTN_DECODE = 0, ATTN_PREFILL = 1 };
+
 struct Plan {
   int T = 0;
-  bool decode = false;        // GEMV path for the linears
-  bool attn_prefill = false;  // prefill attention kernel
+  bool gemv = false;           // T <= 4: weight-streaming GEMVs for the linears
+  int attn = ATTN_DECODE;      // attention kernel
   int rows_per_block = 1;
+  int chunk = 64;
+  int nq_max = 16;
   int n_qblocks = 0, n_items = 0, n_parts = 0;
-  std::vector<int32_t> blob;  // row_seq[T] row_pos[T] n_items qblocks items
+  std::vector<int32_t> blob;   // row_seq[T] row_pos[T] n_items qblocks items
   size_t off_rowseq = 0, off_rowpos = 0, off_nitems = 0, off_qb = 0, off_items = 0;
 };
+
+constexpr int kQbInts = sizeof(AttnQBlock) / sizeof(int32_t);
 
 // Validate rows and build the attention work list (host only; no state change).
 qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const int32_t* positions, Plan& P) {
@@ -517,21 +523,21 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
     g.n++;
   }
   P.T = T;
-  P.decode = T <= 4;
+  P.gemv = T <= 4;
   int max_rows = 0;
   for (auto& g : segs) max_rows = std::max(max_rows, g.n);
-  P.attn_prefill = max_rows * G > attn_decode_nq_max();
-  const int nq_max = P.attn_prefill ? attn_prefill_nq_max() : attn_decode_nq_max();
-  const int CK = P.attn_prefill ? attn_prefill_chunk() : attn_decode_chunk();
-  P.rows_per_block = nq_max / G;
+  P.attn = max_rows * G > attn_decode2_nq_max() ? ATTN_PREFILL : ATTN_DECODE;
+  P.nq_max = P.attn == ATTN_PREFILL ? attn_prefill_nq_max() : attn_decode2_nq_max();
+  P.chunk = P.attn == ATTN_PREFILL ? attn_prefill_chunk() : attn_decode2_chunk(h->dt);
+  P.rows_per_block = P.nq_max / G;
   std::vector<int32_t> qb, items;
   int parts = 0, nqb = 0;
   for (auto& g : segs) {
     for (int r = 0; r < g.n; r += P.rows_per_block) {
       const int nr = std::min(P.rows_per_block, g.n - r);
       const int last_pos = g.pos0 + r + nr - 1;
-      const int nch = (last_pos + 1 + CK - 1) / CK;
-      qb.insert(qb.end(), {g.seq, g.row0 + r, nr, g.pos0 + r, nch, parts});
+      const int nch = (last_pos + 1 + P.chunk - 1) / P.chunk;
+      qb.insert(qb.end(), {g.seq, g.row0 + r, nr, g.pos0 + r, nch, parts, g.row0, g.pos0, g.n, 0});
       for (int ch = 0; ch < nch; ++ch) items.insert(items.end(), {nqb, ch});
       parts += nch;
       nqb++;
@@ -551,7 +557,7 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
   P.off_qb = P.blob.size();
   P.blob.insert(P.blob.end(), qb.begin(), qb.end());
   // room for T query blocks so that the item list sits at an offset fixed by T
-  P.blob.resize(P.off_qb + 6 * (size_t)std::max(T, nqb), 0);
+  P.blob.resize(P.off_qb + (size_t)kQbInts * std::max(T, nqb), 0);
   P.off_items = P.blob.size();
   P.blob.insert(P.blob.end(), items.begin(), items.end());
   return QWEN3_OK;
@@ -560,8 +566,9 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
 struct Bufs {  // raw pointers for one forward
   void *hA, *hB, *pend, *y, *qkv, *q, *attn, *m;
   float *logits, *wts, *part_o, *part_ml;
-  int *idx, *counts, *row_off, *row_cnt, *tile_start, *cursor, *sorted_tok, *sorted_src, *counters;
+  int *idx, *counts, *row_off, *row_cnt, *tile_start, *cursor, *sorted_tok, *sorted_src, *counters, *err;
   void *mexp, *zexp;
+  double* sumsq;
   int32_t* desc;
 };
 
@@ -569,7 +576,6 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   const qwen3_config& c = h->cfg;
   const size_t e = h->esz;
   const size_t Tz = (size_t)std::max(T, 1);
-  const int nq_max = P.attn_prefill ? attn_prefill_nq_max() : attn_decode_nq_max();
   qwen3_status s;
 #define ENS(buf, bytes, zero) \
   if ((s = ensure(h, h->buf, (bytes), zero)) != QWEN3_OK) return s;
@@ -581,14 +587,13 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   ENS(q, Tz * c.n_heads * c.head_dim * e, false);
   ENS(attn, Tz * c.n_heads * c.head_dim * e, false);
   ENS(mbuf, Tz * std::max(c.intermediate, 64) * e, false);
+  ENS(sumsq, Tz * (2 * (size_t)c.num_layers + 1) * sizeof(double), true);
+  ENS(dev_err, 64, true);
   // attention partials: sized for the worst case of this row count when graphs replay it
   size_t parts = (size_t)std::max(P.n_parts, 1);
-  if (P.decode) {
-    const int CK = P.attn_prefill ? attn_prefill_chunk() : attn_decode_chunk();
-    parts = std::max(parts, (size_t)P.n_qblocks * ((c.capacity + CK - 1) / CK));
-  }
-  ENS(part_o, parts * c.n_kv_heads * nq_max * c.head_dim * 4, false);
-  ENS(part_ml, parts * c.n_kv_heads * nq_max * 2 * 4, false);
+  if (P.gemv) parts = std::max(parts, (size_t)std::max(P.n_qblocks, T) * ((c.capacity + P.chunk - 1) / P.chunk));
+  ENS(part_o, parts * c.n_kv_heads * P.nq_max * c.head_dim * 4, false);
+  ENS(part_ml, parts * c.n_kv_heads * P.nq_max * 2 * 4, false);
   ENS(counters, (size_t)std::max(P.n_qblocks, T) * c.n_kv_heads * 4, true);
   if (c.num_experts > 0) {
     const size_t slots = Tz * c.top_k;
@@ -618,7 +623,8 @@ Bufs bufs_of(qwen3_handle* h) {
   b.part_ml = (float*)h->part_ml.p; b.idx = (int*)h->idx.p; b.counts = (int*)h->counts.p;
   b.row_off = (int*)h->row_off.p; b.row_cnt = (int*)h->row_cnt.p; b.tile_start = (int*)h->tile_start.p;
   b.cursor = (int*)h->cursor.p; b.sorted_tok = (int*)h->sorted_tok.p; b.sorted_src = (int*)h->sorted_src.p;
-  b.counters = (int*)h->counters.p; b.mexp = h->mexp.p; b.zexp = h->zexp.p; b.desc = (int32_t*)h->desc.p;
+  b.counters = (int*)h->counters.p; b.err = (int*)h->dev_err.p; b.mexp = h->mexp.p; b.zexp = h->zexp.p;
+  b.sumsq = (double*)h->sumsq.p; b.desc = (int32_t*)h->desc.p;
   return b;
 }
 
@@ -646,9 +652,11 @@ qwen3_status upload_plan(qwen3_handle* h, const Plan& P, cudaStream_t s) {
   return QWEN3_OK;
 }
 
-// MoE block on y [T, hidden] -> out [T, hidden]; idx/w receive the routing.
-cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, int T, void* out, int* idx, float* w,
-                      const Bufs& B) {
+// MoE block on y [T, hidden].  The weighted expert sum goes to `out`, or,
+// when h_res is given, is added to the residual h_res in place with the
+// rows' sums of squares stored to sumsq_out.  idx/w receive the routing.
+cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, int T, void* out, void* h_res,
+                      double* sumsq_out, int* idx, float* w, const Bufs& B) {
   const qwen3_config& c = h->cfg;
   const qwen3_layer_weights& W = h->layers[layer];
   const int E = c.num_experts, k = c.top_k, mI = c.moe_intermediate, hid = c.hidden;
@@ -716,120 +724,168 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
     if (e != cudaSuccess) return e;
   }
   MoeCombineArgs cb{};
-  cb.z = B.zexp; cb.w = w; cb.T = T; cb.k = k; cb.hidden = hid; cb.out = out;
+  cb.z = B.zexp; cb.w = w; cb.T = T; cb.k = k; cb.hidden = hid; cb.out = out; cb.h = h_res; cb.sumsq_out = sumsq_out;
   return launch(L, "moe_combine", [&] { return launch_moe_combine(L.ctx, dt, cb); });
 }
 
-// Enqueue every kernel of one forward on L.ctx.stream.
-cudaError_t enqueue_forward(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
+// Attention of layer l for the plan's kernel.
+cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l, const Bufs& B) {
+  const qwen3_config& c = h->cfg;
+  const qwen3_layer_weights& W = h->layers[l];
+  const int dt = h->dt, KV = c.n_kv_heads, D = c.head_dim;
+  char* kc = static_cast<char*>(h->kcache) + (size_t)l * h->layer_stride * h->esz;
+  char* vc = static_cast<char*>(h->vcache) + (size_t)l * h->layer_stride * h->esz;
+  const int32_t* row_seq = B.desc + P.off_rowseq;
+  const int32_t* row_pos = B.desc + P.off_rowpos;
+  const int32_t* n_items = B.desc + P.off_nitems;
+  const AttnQBlock* qbs = reinterpret_cast<const AttnQBlock*>(B.desc + P.off_qb);
+  const AttnItem* items = reinterpret_cast<const AttnItem*>(B.desc + P.off_items);
+  const float scale = (float)(1.0 / std::sqrt((double)D));
+  cudaError_t e;
+  if (P.attn == ATTN_DECODE) {
+    AttnDecArgs a{};
+    a.qkv = B.qkv; a.H = c.n_heads; a.KV = KV; a.D = D; a.q_gain = W.q_norm; a.k_gain = W.k_norm;
+    a.cos_t = h->rope_cos; a.sin_t = h->rope_sin; a.eps = c.rms_eps; a.kc = kc; a.vc = vc;
+    a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity; a.scale = scale; a.qblocks = qbs;
+    a.items = items; a.n_items = n_items; a.part_o = B.part_o; a.part_ml = B.part_ml; a.nq_max = P.nq_max;
+    a.counters = B.counters; a.out = B.attn; a.err = B.err;
+    a.grid_x = std::max(1, (h->num_sms * 2 + KV - 1) / KV);
+    return launch(L, "attn_decode", [&] { return launch_attn_decode2(L.ctx, dt, a); });
+  }
+  QkRopeArgs r{};
+  r.qkv = B.qkv; r.T = P.T; r.H = c.n_heads; r.KV = KV; r.D = D; r.q_out = B.q; r.kcache = kc; r.vcache = vc;
+  r.seq_stride = (long long)h->seq_stride; r.capacity = c.capacity; r.q_gain = W.q_norm; r.k_gain = W.k_norm;
+  r.cos_t = h->rope_cos; r.sin_t = h->rope_sin; r.row_seq = row_seq; r.row_pos = row_pos; r.eps = c.rms_eps;
+  e = launch(L, "qk_rope_cache", [&] { return launch_qk_rope_cache(L.ctx, dt, r); });
+  if (e != cudaSuccess) return e;
+  AttnArgs a{};
+  a.q = B.q; a.kc = kc; a.vc = vc; a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity;
+  a.H = c.n_heads; a.KV = KV; a.D = D; a.scale = scale; a.qblocks = qbs; a.items = items; a.n_items = n_items;
+  a.chunk = P.chunk; a.nq_max = P.nq_max; a.part_o = B.part_o; a.part_ml = B.part_ml; a.counters = B.counters;
+  a.out = B.attn;
+  a.grid_x = std::max(1, std::min((h->num_sms * 8 + KV - 1) / KV, P.n_items));
+  return launch(L, "attn_prefill", [&] { return launch_attention_prefill(L.ctx, dt, a); });
+}
+
+// Decode plan (T <= 4): five kernels per dense layer.  The residual stream
+// lives in hA and is updated in place; sumsq holds, per row, the sum of
+// squares of h entering each RMSNorm: slot 2l (input norm of layer l >= 1),
+// 2l + 1 (post-attention norm of layer l), 2L (final norm).
+cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
+  const qwen3_config& c = h->cfg;
+  const int T = P.T, hid = c.hidden, H = c.n_heads, KV = c.n_kv_heads, D = c.head_dim, I = c.intermediate;
+  const int NL = c.num_layers;
+  const int dt = h->dt, wf = h->wfmt;
+  const int qkv_rows = (H + 2 * KV) * D;
+  void* hres = B.hA;
+  auto slot = [&](int s) { return B.sumsq + (size_t)s * T; };
+  auto wfmt_of = [&](const qwen3_linear& lin) { return lin.scale ? wf : W_DT; };
+  cudaError_t e;
+  for (int l = 0; l < NL; ++l) {
+    const qwen3_layer_weights& W = h->layers[l];
+    {
+      Gemv2Args g{};
+      g.T = T; g.K = hid; g.N = qkv_rows; g.w = W.qkv.w; g.scale = W.qkv.scale; g.bias = W.qkv.bias;
+      g.group = c.group_size; g.gain = W.in_norm; g.eps = c.rms_eps; g.h = hres; g.epilogue = EPI_STORE;
+      g.out = B.qkv; g.ldo = qkv_rows; g.err = B.err;
+      if (l == 0) {
+        g.prologue = PRO_FULL; g.x = x; g.pend = nullptr; g.sumsq_zero = slot(1); g.sumsq_zero_n = 2 * NL * T;
+      } else {
+        g.prologue = PRO_SUMSQ; g.sumsq_in = slot(2 * l);
+      }
+      g.stages = gemv2_plan(dt, wfmt_of(W.qkv), T, hid, c.group_size, false, nullptr);
+      e = launch(L, "gemv_qkv", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.qkv), g); });
+      if (e != cudaSuccess) return e;
+    }
+    e = enqueue_attention(h, L, P, l, B);
+    if (e != cudaSuccess) return e;
+    {
+      Gemv2Args g{};
+      g.T = T; g.K = H * D; g.N = hid; g.w = W.o.w; g.scale = W.o.scale; g.bias = W.o.bias; g.group = c.group_size;
+      g.prologue = PRO_X; g.x = B.attn; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
+      g.sumsq_out = slot(2 * l + 1); g.err = B.err;
+      g.stages = gemv2_plan(dt, wfmt_of(W.o), T, H * D, c.group_size, false, nullptr);
+      e = launch(L, "gemv_o", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.o), g); });
+      if (e != cudaSuccess) return e;
+    }
+    if (is_moe_layer(h, l)) {
+      NormApplyArgs n{};
+      n.h = hres; n.sumsq = slot(2 * l + 1); n.gain = W.post_norm; n.out = B.y; n.T = T; n.hidden = hid;
+      n.eps = c.rms_eps;
+      e = launch(L, "norm_apply", [&] { return launch_norm_apply(L.ctx, dt, n); });
+      if (e != cudaSuccess) return e;
+      e = moe_block(h, L, l, B.y, T, nullptr, hres, slot(2 * l + 2), B.idx, B.wts, B);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    {
+      Gemv2Args g{};
+      g.T = T; g.K = hid; g.N = I; g.w = W.gate_up.w; g.scale = W.gate_up.scale; g.bias = W.gate_up.bias;
+      g.group = c.group_size; g.prologue = PRO_SUMSQ; g.h = hres; g.gain = W.post_norm; g.eps = c.rms_eps;
+      g.sumsq_in = slot(2 * l + 1); g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I; g.err = B.err;
+      g.stages = gemv2_plan(dt, wfmt_of(W.gate_up), T, hid, c.group_size, true, nullptr);
+      e = launch(L, "gemv_gate_up", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.gate_up), g); });
+      if (e != cudaSuccess) return e;
+    }
+    {
+      Gemv2Args g{};
+      g.T = T; g.K = I; g.N = hid; g.w = W.down.w; g.scale = W.down.scale; g.bias = W.down.bias;
+      g.group = c.group_size; g.prologue = PRO_X; g.x = B.m; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
+      g.sumsq_out = slot(2 * l + 2); g.err = B.err;
+      g.stages = gemv2_plan(dt, wfmt_of(W.down), T, I, c.group_size, false, nullptr);
+      e = launch(L, "gemv_down", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.down), g); });
+      if (e != cudaSuccess) return e;
+    }
+  }
+  NormApplyArgs n{};
+  n.h = hres; n.sumsq = slot(2 * NL); n.gain = h->final_norm; n.out = out; n.T = T; n.hidden = hid;
+  n.eps = c.rms_eps;
+  return launch(L, "norm_apply", [&] { return launch_norm_apply(L.ctx, dt, n); });
+}
+
+// Prefill plan (T > 4): add+RMSNorm kernels, tiled GEMMs, ping-pong residual.
+cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
   const qwen3_config& c = h->cfg;
   const int T = P.T, hid = c.hidden, H = c.n_heads, KV = c.n_kv_heads, D = c.head_dim, I = c.intermediate;
   const int dt = h->dt, wf = h->wfmt;
   const int qkv_rows = (H + 2 * KV) * D;
-  const int32_t* row_seq = B.desc + P.off_rowseq;
-  const int32_t* row_pos = B.desc + P.off_rowpos;
-  const int32_t* n_items = B.desc + P.off_nitems;
+  auto wfmt_of = [&](const qwen3_linear& lin) { return lin.scale ? wf : W_DT; };
   cudaError_t e;
   const void* h_in = x;   // residual stream entering the layer
   void* h_cur = B.hA;     // residual stream of the current layer
   bool have_pend = false;
   for (int l = 0; l < c.num_layers; ++l) {
     const qwen3_layer_weights& W = h->layers[l];
-    const auto wfmt_of = [&](const qwen3_linear& lin) { return lin.scale ? wf : W_DT; };
-    // --- input RMSNorm + qkv projection
-    if (P.decode) {
-      GemvArgs g{};
-      g.T = T; g.K = hid; g.N = qkv_rows; g.w = W.qkv.w; g.scale = W.qkv.scale; g.bias = W.qkv.bias;
-      // layer 0: the residual stream starts as a copy of x (no pend)
-      g.group = c.group_size; g.x_rows = T; g.prologue = 2; g.h_in = h_in; g.pend = have_pend ? B.pend : nullptr;
-      g.h_out = h_cur; g.gain = W.in_norm; g.eps = c.rms_eps; g.epilogue = EPI_STORE; g.out = B.qkv;
-      g.ldo = qkv_rows;
-      e = launch(L, "gemv_qkv", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.qkv), g); });
-    } else {
-      NormArgs n{};
-      n.h_in = h_in; n.pend = have_pend ? B.pend : nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.in_norm;
-      n.rows = T; n.hidden = hid; n.eps = c.rms_eps;
-      e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
-      if (e != cudaSuccess) return e;
-      GemmArgs g{};
-      g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
-      g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
-      e = launch(L, "gemm_qkv", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.qkv), g); });
-    }
+    NormArgs n{};
+    n.h_in = h_in; n.pend = have_pend ? B.pend : nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.in_norm;
+    n.rows = T; n.hidden = hid; n.eps = c.rms_eps;
+    e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
     if (e != cudaSuccess) return e;
-    // --- q/k norm, RoPE, cache append
-    char* kc = static_cast<char*>(h->kcache) + (size_t)l * h->layer_stride * h->esz;
-    char* vc = static_cast<char*>(h->vcache) + (size_t)l * h->layer_stride * h->esz;
-    {
-      QkRopeArgs r{};
-      r.qkv = B.qkv; r.T = T; r.H = H; r.KV = KV; r.D = D; r.q_out = B.q; r.kcache = kc; r.vcache = vc;
-      r.seq_stride = (long long)h->seq_stride; r.capacity = c.capacity; r.q_gain = W.q_norm; r.k_gain = W.k_norm;
-      r.cos_t = h->rope_cos; r.sin_t = h->rope_sin; r.row_seq = row_seq; r.row_pos = row_pos; r.eps = c.rms_eps;
-      e = launch(L, "qk_rope_cache", [&] { return launch_qk_rope_cache(L.ctx, dt, r); });
-      if (e != cudaSuccess) return e;
-    }
-    // --- attention
-    {
-      AttnArgs a{};
-      a.q = B.q; a.kc = kc; a.vc = vc; a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity;
-      a.H = H; a.KV = KV; a.D = D; a.scale = (float)(1.0 / std::sqrt((double)D));
-      a.qblocks = reinterpret_cast<const AttnQBlock*>(B.desc + P.off_qb);
-      a.items = reinterpret_cast<const AttnItem*>(B.desc + P.off_items);
-      a.n_items = n_items;
-      a.chunk = P.attn_prefill ? attn_prefill_chunk() : attn_decode_chunk();
-      a.nq_max = P.attn_prefill ? attn_prefill_nq_max() : attn_decode_nq_max();
-      a.part_o = B.part_o; a.part_ml = B.part_ml; a.counters = B.counters; a.out = B.attn;
-      a.grid_x = std::max(1, (h->num_sms * 4 + KV - 1) / KV);
-      if (!P.decode) a.grid_x = std::max(1, std::min(a.grid_x * 2, P.n_items));
-      if (P.attn_prefill) e = launch(L, "attn_prefill", [&] { return launch_attention_prefill(L.ctx, dt, a); });
-      else e = launch(L, "attn_decode", [&] { return launch_attention_decode(L.ctx, dt, a); });
-      if (e != cudaSuccess) return e;
-    }
-    // --- o projection + residual
-    if (P.decode) {
-      GemvArgs g{};
-      g.T = T; g.K = H * D; g.N = hid; g.w = W.o.w; g.scale = W.o.scale; g.bias = W.o.bias; g.group = c.group_size;
-      g.x_rows = T; g.prologue = 0; g.x = B.attn; g.epilogue = EPI_RESIDUAL; g.out = h_cur; g.ldo = hid;
-      e = launch(L, "gemv_o", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.o), g); });
-    } else {
-      GemmArgs g{};
-      g.M = T; g.N = hid; g.K = H * D; g.a = B.attn; g.lda = H * D; g.w = W.o.w; g.scale = W.o.scale;
-      g.bias = W.o.bias; g.group = c.group_size; g.epilogue = EPI_RESIDUAL; g.out = h_cur; g.ldo = hid;
-      e = launch(L, "gemm_o", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.o), g); });
-    }
+    GemmArgs g{};
+    g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
+    g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
+    e = launch(L, "gemm_qkv", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.qkv), g); });
     if (e != cudaSuccess) return e;
-    // --- MLP
+    e = enqueue_attention(h, L, P, l, B);
+    if (e != cudaSuccess) return e;
+    GemmArgs go{};
+    go.M = T; go.N = hid; go.K = H * D; go.a = B.attn; go.lda = H * D; go.w = W.o.w; go.scale = W.o.scale;
+    go.bias = W.o.bias; go.group = c.group_size; go.epilogue = EPI_RESIDUAL; go.out = h_cur; go.ldo = hid;
+    e = launch(L, "gemm_o", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.o), go); });
+    if (e != cudaSuccess) return e;
+    NormArgs n2{};
+    n2.h_in = h_cur; n2.pend = nullptr; n2.h_out = h_cur; n2.y = B.y; n2.gain = W.post_norm; n2.rows = T;
+    n2.hidden = hid; n2.eps = c.rms_eps;
+    e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n2); });
+    if (e != cudaSuccess) return e;
     if (is_moe_layer(h, l)) {
-      NormArgs n{};
-      n.h_in = h_cur; n.pend = nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.post_norm; n.rows = T;
-      n.hidden = hid; n.eps = c.rms_eps;
-      e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
-      if (e != cudaSuccess) return e;
-      e = moe_block(h, L, l, B.y, T, B.pend, B.idx, B.wts, B);
-      if (e != cudaSuccess) return e;
-    } else if (P.decode) {
-      GemvArgs g{};
-      g.T = T; g.K = hid; g.N = I; g.w = W.gate_up.w; g.scale = W.gate_up.scale; g.bias = W.gate_up.bias;
-      g.group = c.group_size; g.x_rows = T; g.prologue = 1; g.h_in = h_cur; g.gain = W.post_norm;
-      g.eps = c.rms_eps; g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I;
-      e = launch(L, "gemv_gate_up", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.gate_up), g); });
-      if (e != cudaSuccess) return e;
-      GemvArgs d{};
-      d.T = T; d.K = I; d.N = hid; d.w = W.down.w; d.scale = W.down.scale; d.bias = W.down.bias;
-      d.group = c.group_size; d.x_rows = T; d.prologue = 0; d.x = B.m; d.epilogue = EPI_STORE; d.out = B.pend;
-      d.ldo = hid;
-      e = launch(L, "gemv_down", [&] { return launch_gemv(L.ctx, dt, wfmt_of(W.down), d); });
+      e = moe_block(h, L, l, B.y, T, B.pend, nullptr, nullptr, B.idx, B.wts, B);
       if (e != cudaSuccess) return e;
     } else {
-      NormArgs n{};
-      n.h_in = h_cur; n.pend = nullptr; n.h_out = h_cur; n.y = B.y; n.gain = W.post_norm; n.rows = T;
-      n.hidden = hid; n.eps = c.rms_eps;
-      e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
-      if (e != cudaSuccess) return e;
-      GemmArgs g{};
-      g.M = T; g.N = I; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.gate_up.w; g.scale = W.gate_up.scale;
-      g.bias = W.gate_up.bias; g.group = c.group_size; g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I;
-      e = launch(L, "gemm_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.gate_up), g); });
+      GemmArgs gu{};
+      gu.M = T; gu.N = I; gu.K = hid; gu.a = B.y; gu.lda = hid; gu.w = W.gate_up.w; gu.scale = W.gate_up.scale;
+      gu.bias = W.gate_up.bias; gu.group = c.group_size; gu.epilogue = EPI_SWIGLU; gu.out = B.m; gu.ldo = I;
+      e = launch(L, "gemm_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.gate_up), gu); });
       if (e != cudaSuccess) return e;
       GemmArgs d{};
       d.M = T; d.N = hid; d.K = I; d.a = B.m; d.lda = I; d.w = W.down.w; d.scale = W.down.scale;
@@ -846,6 +902,10 @@ cudaError_t enqueue_forward(qwen3_handle* h, Launcher& L, const Plan& P, const v
   n.h_in = h_in; n.pend = B.pend; n.h_out = h_cur; n.y = out; n.gain = h->final_norm; n.rows = T; n.hidden = hid;
   n.eps = c.rms_eps;
   return launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
+}
+
+cudaError_t enqueue_forward(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
+  return P.gemv ? enqueue_decode(h, L, P, x, out, B) : enqueue_prefill(h, L, P, x, out, B);
 }
 
 }  // namespace
@@ -866,10 +926,10 @@ extern "C" qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T,
   if (st != QWEN3_OK) return st;
   Bufs B = bufs_of(h);
   Launcher L{h, {s, h->pdl && !h->profile, h->num_sms}};
-  const bool graph = h->use_graphs && !h->profile && P.decode;
+  const bool graph = h->use_graphs && !h->profile && P.gemv;
   cudaError_t e;
   if (graph) {
-    const GraphKey key{T, (P.attn_prefill ? 1 : 0), x, out};
+    const GraphKey key{T, P.attn, x, out};
     if (h->graphs.size() > 32) {  // callers cycling through buffers: start over
       for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
       h->graphs.clear();
@@ -926,13 +986,29 @@ extern "C" qwen3_status qwen3_moe_layer(qwen3_handle* h, int32_t layer, const vo
   if (T < 1 || T > (1 << 20)) return fail(h, QWEN3_E_ARG, "row count out of range");
   Plan P;
   P.T = T;
-  P.decode = T <= 4;
+  P.gemv = T <= 4;
   qwen3_status st = ensure_workspace(h, P, T);
   if (st != QWEN3_OK) return st;
   Bufs B = bufs_of(h);
   Launcher L{h, {static_cast<cudaStream_t>(stream), h->pdl && !h->profile, h->num_sms}};
-  cudaError_t e = moe_block(h, L, layer, y, T, out, topk_idx, topk_w, B);
+  cudaError_t e = moe_block(h, L, layer, y, T, out, nullptr, nullptr, topk_idx, topk_w, B);
   if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
   h->last_launches = L.count;
+  return QWEN3_OK;
+}
+
+extern "C" qwen3_status qwen3_device_error(qwen3_handle* h, int32_t* code) {
+  if (!h || !code) return QWEN3_E_ARG;
+  *code = 0;
+  if (!h->dev_err.p) return QWEN3_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "device error poll");
+  int v = 0;
+  cudaMemcpy(&v, h->dev_err.p, sizeof(int), cudaMemcpyDeviceToHost);
+  if (v) {
+    cudaMemset(h->dev_err.p, 0, sizeof(int));
+    *code = v;
+    return fail(h, QWEN3_E_DEVICE, "a kernel gave up waiting for its data (code " + std::to_string(v) + ")");
+  }
   return QWEN3_OK;
 }
