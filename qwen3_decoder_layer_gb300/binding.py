@@ -20,7 +20,8 @@ QWEN3_OK = 0
 STATUS = {0: "QWEN3_OK", 1: "QWEN3_E_ARG", 2: "QWEN3_E_DTYPE", 3: "QWEN3_E_CAPACITY",
           4: "QWEN3_E_POSITION", 5: "QWEN3_E_SEQ", 6: "QWEN3_E_OOM", 7: "QWEN3_E_CUDA",
           8: "QWEN3_E_UNSUPPORTED", 9: "QWEN3_E_DEVICE"}
-QWEN3_OPT_CUDA_GRAPHS, QWEN3_OPT_PROFILE, QWEN3_OPT_PDL = 1, 2, 3
+QWEN3_OPT_CUDA_GRAPHS, QWEN3_OPT_PROFILE, QWEN3_OPT_PDL, QWEN3_OPT_TENSOR_CORES = 1, 2, 3, 4
+QWEN3_OPT_L2_PREFETCH = 5
 
 
 class Qwen3Error(RuntimeError):

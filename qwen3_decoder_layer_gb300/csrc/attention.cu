@@ -21,7 +21,6 @@ namespace q3 {
 
 namespace {
 
-constexpr int DEC_CK = 64, DEC_NQ = 16, DEC_THREADS = 128;
 constexpr int PRE_CK = 64, PRE_NQ = 32, PRE_THREADS = 128;
 
 // Merge the partials of one (query block, kv head); called by the whole block.
@@ -66,87 +65,6 @@ __device__ void finish_item(const AttnArgs& a, const AttnQBlock& qb, int qbi, in
     if (threadIdx.x == 0) a.counters[(size_t)qbi * a.KV + j] = 0;
   }
   __syncthreads();
-}
-
-// Decode: a few query vectors (rows x G <= 16) per item.  Scores: one warp per
-// key, lanes across head_dim; output: one thread per head_dim element.
-template <typename Dt, int D>
-__global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(AttnArgs a) {
-  constexpr int EPL = D / 32;
-  __shared__ float qs[DEC_NQ][D];
-  __shared__ float sc[DEC_NQ][DEC_CK];
-  __shared__ float ml[DEC_NQ][2];
-  __shared__ int flag;
-  pdl_wait();
-  pdl_launch();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j = blockIdx.y;
-  const int G = a.H / a.KV;
-  const int n_items = *a.n_items;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const AttnItem item = a.items[it];
-    const AttnQBlock qb = a.qblocks[item.qb];
-    const int nq = qb.nrows * G;
-    const int key0 = item.chunk * DEC_CK;
-    const int key1 = min(key0 + DEC_CK, qb.pos0 + qb.nrows);
-    const int nk = key1 - key0;
-    for (int idx = tid; idx < nq * D; idx += DEC_THREADS) {
-      const int i = idx / D, d = idx % D;
-      qs[i][d] = to_f(static_cast<const Dt*>(a.q)[((size_t)(qb.row0 + i / G) * a.H + j * G + i % G) * D + d]);
-    }
-    __syncthreads();
-    const size_t slab = (size_t)qb.seq * a.seq_stride + (size_t)j * a.capacity * D;
-    const Dt* Kb = static_cast<const Dt*>(a.kc) + slab;
-    const Dt* Vb = static_cast<const Dt*>(a.vc) + slab;
-    for (int u = key0 + warp; u < key1; u += DEC_THREADS / 32) {
-      float kv[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) kv[e] = to_f(Kb[(size_t)u * D + lane * EPL + e]);
-      for (int i = 0; i < nq; ++i) {
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) s = fmaf(qs[i][lane * EPL + e], kv[e], s);
-        s = warp_sum(s);
-        if (lane == 0) sc[i][u - key0] = (u <= qb.pos0 + i / G) ? s * a.scale : -CUDART_INF_F;
-      }
-    }
-    __syncthreads();
-    for (int i = warp; i < nq; i += DEC_THREADS / 32) {
-      float m = -CUDART_INF_F;
-      for (int u = lane; u < nk; u += 32) m = fmaxf(m, sc[i][u]);
-      m = warp_max(m);
-      float l = 0.f;
-      for (int u = lane; u < nk; u += 32) {
-        const float s = sc[i][u];
-        const float p = (s == -CUDART_INF_F) ? 0.f : expf(s - m);
-        sc[i][u] = p;
-        l += p;
-      }
-      l = warp_sum(l);
-      if (lane == 0) { ml[i][0] = m; ml[i][1] = l; }
-    }
-    __syncthreads();
-    const size_t part0 = ((size_t)(qb.part_base + item.chunk) * a.KV + j) * a.nq_max;
-    for (int d = tid; d < D; d += DEC_THREADS) {
-      float o[DEC_NQ];
-#pragma unroll
-      for (int i = 0; i < DEC_NQ; ++i) o[i] = 0.f;
-      for (int u = 0; u < nk; ++u) {
-        const float v = to_f(Vb[(size_t)(key0 + u) * D + d]);
-#pragma unroll
-        for (int i = 0; i < DEC_NQ; ++i)
-          if (i < nq) o[i] = fmaf(sc[i][u], v, o[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < DEC_NQ; ++i)
-        if (i < nq) a.part_o[(part0 + i) * D + d] = o[i];
-    }
-    if (tid < nq) {
-      a.part_ml[(part0 + tid) * 2] = ml[tid][0];
-      a.part_ml[(part0 + tid) * 2 + 1] = ml[tid][1];
-    }
-    finish_item<Dt, D>(a, qb, item.qb, j, &flag);
-  }
 }
 
 // Prefill: 32 query vectors per item, 64-key chunks staged in shared memory;
@@ -266,23 +184,8 @@ template <int D> size_t prefill_smem() {
 
 }  // namespace
 
-int attn_decode_chunk() { return DEC_CK; }
-int attn_decode_nq_max() { return DEC_NQ; }
 int attn_prefill_chunk() { return PRE_CK; }
 int attn_prefill_nq_max() { return PRE_NQ; }
-
-cudaError_t launch_attention_decode(const LaunchCtx& c, int dt, const AttnArgs& a) {
-  const dim3 grid(a.grid_x, a.KV), block(DEC_THREADS);
-  if (a.D == 128) {
-    if (dt == DT_BF16) return launch_k(attn_decode_kernel<bf16, 128>, grid, block, 0, c, a);
-    return launch_k(attn_decode_kernel<float, 128>, grid, block, 0, c, a);
-  }
-  if (a.D == 64) {
-    if (dt == DT_BF16) return launch_k(attn_decode_kernel<bf16, 64>, grid, block, 0, c, a);
-    return launch_k(attn_decode_kernel<float, 64>, grid, block, 0, c, a);
-  }
-  return cudaErrorInvalidValue;
-}
 
 template <typename Dt, int D>
 static cudaError_t launch_pre(const LaunchCtx& c, const AttnArgs& a) {

@@ -1,0 +1,293 @@
+// Tensor-core GEMM for the prefill linears (maya2_mlx/backbone.py,
+// Backbone.forward: the fused q|k|v, o_proj, fused gate|up with SiLU * up and
+// down_proj products for T > 4 rows), bf16 in, fp32 accumulate, on sm_103a:
+//
+//   C[M, N] = A[M, K] . B[N, K]^T      (A: activations, B: nn.Linear weight; both K-major)
+//
+// One CTA computes a 128 x 256 tile with tcgen05.mma (cta_group::1,
+// kind::f16, M = 128, N = 256, K = 16 per instruction) accumulating in
+// tensor memory.  A 4-stage ring of 128 x 64 (A) and 256 x 64 (B) bf16 tiles
+// is filled by 2-D TMA loads with 128-byte swizzle; mbarriers hand stages
+// from the TMA warp to the MMA warp (full) and back (empty, signalled by
+// tcgen05.commit).  Four epilogue warps read the accumulator with
+// tcgen05.ld (warp q owns TMEM lanes 32q..32q+31, i.e. rows of the tile),
+// apply the fused epilogue (rounding / residual add / SiLU * up) and store.
+// For SiLU * up the B tile is two 128-row boxes: gate rows n0.. and up rows
+// N + n0.., so TMEM columns 0..127 hold g and 128..255 hold u of the same
+// output columns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_THREADS = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr uint32_t TC_TMEM_COLS = 256;
+constexpr size_t TC_A_BYTES = (size_t)TC_BM * TC_BK * 2;   // 16 KB
+constexpr size_t TC_B_BYTES = (size_t)TC_BN * TC_BK * 2;   // 32 KB
+constexpr size_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
+constexpr size_t TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 1024 /* align */ + 256 /* barriers */;
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte rows,
+// 128-byte swizzle and 8-row groups 1024 bytes apart (the layout TMA writes
+// for a {64, rows} bf16 box with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);       // start address
+  d |= (uint64_t)1 << 16;                         // leading-dimension byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;               // stride-dimension byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                         // descriptor version
+  d |= (uint64_t)2 << 61;                         // swizzle mode: 128 B
+  return d;
+}
+
+// Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TC_BN >> 3) << 17) |
+                            ((uint32_t)(TC_BM >> 4) << 24);
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   GemmTcArgs a) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_STAGES * TC_STAGE_BYTES);
+  uint64_t* empty = full + TC_STAGES;
+  uint64_t* accum = empty + TC_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * TC_BM;
+  const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;  // output columns of this tile
+  const int n0 = blockIdx.x * ncol;
+  const int nk = a.K / TC_BK;
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    mbar_fence_init();
+  }
+  if (warp == 5) tmem_alloc(tmem_slot, TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_launch();
+
+  bool ok = true;
+  if (warp == 4) {
+    if (lane == 0) {  // TMA producer
+      for (int kt = 0; kt < nk && ok; ++kt) {
+        const int s = kt % TC_STAGES;
+        if (kt >= TC_STAGES) ok = mbar_wait(&empty[s], (uint32_t)((kt / TC_STAGES - 1) & 1), a.err, 3);
+        if (!ok) break;
+        uint8_t* sa = smem + s * TC_STAGE_BYTES;
+        uint8_t* sb = sa + TC_A_BYTES;
+        mbar_expect_tx(&full[s], (uint32_t)TC_STAGE_BYTES);
+        tma_load_2d(sa, &map_a, kt * TC_BK, m0, &full[s]);
+        if (EPI == EPI_SWIGLU) {
+          tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
+          tma_load_2d(sb + TC_B_BYTES / 2, &map_b, kt * TC_BK, a.N + n0, &full[s]);
+        } else {
+          tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {  // MMA issuer
+      for (int kt = 0; kt < nk && ok; ++kt) {
+        const int s = kt % TC_STAGES;
+        ok = mbar_wait(&full[s], (uint32_t)((kt / TC_STAGES) & 1), a.err, 4);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * TC_STAGE_BYTES);
+        const uint32_t sb = sa + (uint32_t)TC_A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < TC_BK / 16; ++kk)
+          mma_bf16(tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc, (kt | kk) != 0);
+        mma_commit(&empty[s]);
+      }
+      if (ok) mma_commit(accum);
+    }
+  } else {  // epilogue: warp q reads TMEM lanes 32q .. 32q + 31 = tile rows
+    ok = __all_sync(0xffffffffu, mbar_wait(accum, 0, a.err, 5));
+    tc_fence_after();
+    const int row = m0 + warp * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    if (ok) {
+      if (EPI == EPI_SWIGLU) {
+        for (int c = 0; c < TC_BN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tl + c, g);
+          tmem_ld32(tl + TC_BN / 2 + c, u);
+          if (row < a.M) {
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gv = rd<bf16>(__uint_as_float(g[i])), uv = rd<bf16>(__uint_as_float(u[i]));
+              o[i] = rd<bf16>(silu_f(gv)) * uv;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(a.out) + (size_t)row * a.ldo + n0 + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = Vec16<bf16>::pack(o + 8 * q);
+          }
+        }
+      } else {
+        for (int c = 0; c < TC_BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tl + c, r);
+          if (row < a.M) {
+            bf16* p = static_cast<bf16*>(a.out) + (size_t)row * a.ldo + n0 + c;
+            float o[32];
+            if (EPI == EPI_RESIDUAL) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float hv[8];
+                Vec16<bf16>::unpack(reinterpret_cast<const uint4*>(p)[q], hv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[8 * q + i] = hv[i] + rd<bf16>(__uint_as_float(r[8 * q + i]));
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(p)[q] = Vec16<bf16>::pack(o + 8 * q);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TC_TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix with row pitch `ld`
+// elements, box {64 columns, box_rows rows}, 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t tc_launch(const LaunchCtx& c, const CUtensorMap& ma, const CUtensorMap& mb, const GemmTcArgs& a) {
+  auto kern = gemm_tc_kernel<EPI>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
+  const dim3 grid(a.N / ncol, (a.M + TC_BM - 1) / TC_BM);
+  return launch_k(kern, grid, dim3(TC_THREADS), TC_SMEM, c, ma, mb, a);
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int M, int N, int K, int epilogue) {
+  if (!encode_fn()) return false;
+  if (M < 1 || K % TC_BK) return false;
+  if (epilogue == EPI_SWIGLU) return N % (TC_BN / 2) == 0;
+  if (epilogue == EPI_STORE || epilogue == EPI_RESIDUAL) return N % TC_BN == 0;
+  return false;
+}
+
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a) {
+  if (!gemm_tc_supported(a.M, a.N, a.K, a.epilogue)) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.a) & 15) || (reinterpret_cast<uintptr_t>(a.w) & 15) || (a.lda % 8) ||
+      (a.ldo % 8))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  const uint64_t wrows = a.epilogue == EPI_SWIGLU ? 2ull * a.N : (uint64_t)a.N;
+  if (!make_map(&ma, a.a, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, TC_BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, a.w, wrows, (uint64_t)a.K, (uint64_t)a.K, a.epilogue == EPI_SWIGLU ? TC_BN / 2 : TC_BN))
+    return cudaErrorInvalidValue;
+  switch (a.epilogue) {
+    case EPI_STORE: return tc_launch<EPI_STORE>(c, ma, mb, a);
+    case EPI_RESIDUAL: return tc_launch<EPI_RESIDUAL>(c, ma, mb, a);
+    case EPI_SWIGLU: return tc_launch<EPI_SWIGLU>(c, ma, mb, a);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace q3

@@ -108,6 +108,22 @@ struct GemmArgs {
 cudaError_t launch_gemm_simt(const LaunchCtx& c, int dt, int wfmt, const GemmArgs& a);
 int gemm_simt_tile_m();
 
+// Tensor-core (tcgen05 / TMEM / TMA) bf16 GEMM: out[M, N] = a[M, K] w[N, K]^T
+// with EPI_STORE, EPI_RESIDUAL (out += R(.), in place) or EPI_SWIGLU (w has
+// 2N rows, gate first).  Dense bf16 weights only.
+struct GemmTcArgs {
+  int M, N, K;
+  const void* a;
+  int lda;
+  const void* w;
+  void* out;
+  int ldo;
+  int epilogue;
+  int* err;
+};
+bool gemm_tc_supported(int M, int N, int K, int epilogue);
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a);
+
 // Attention over the cache.  Work: query blocks (rows of one sequence at
 // consecutive positions) x key chunks x kv heads; each item writes a partial
 // (max, sum, unnormalised output) and the last item of a (query block, kv
@@ -137,11 +153,8 @@ struct AttnArgs {
   void* out;           // dt [T, H * D]
   int grid_x;          // persistent grid width
 };
-cudaError_t launch_attention_decode(const LaunchCtx& c, int dt, const AttnArgs& a);
 cudaError_t launch_attention_prefill(const LaunchCtx& c, int dt, const AttnArgs& a);
-// chunk sizes and query-vector limits each attention kernel is built for
-int attn_decode_chunk();
-int attn_decode_nq_max();
+// chunk size and query-vector limit the prefill attention kernel is built for
 int attn_prefill_chunk();
 int attn_prefill_nq_max();
 
@@ -222,6 +235,8 @@ struct Gemv2Args {
   double* sumsq_out;
   int stages;
   int* err;
+  const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
+  size_t pf_bytes;
 };
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a);
 // Ring slots per warp that fit, and the dynamic shared memory they need (0 = does not fit).
@@ -254,6 +269,8 @@ struct AttnDecArgs {
   void* out;
   int grid_x;
   int* err;
+  const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
+  size_t pf_bytes;
 };
 cudaError_t launch_attn_decode2(const LaunchCtx& c, int dt, const AttnDecArgs& a);
 int attn_decode2_chunk(int dt);

@@ -74,7 +74,7 @@ struct qwen3_handle {
   std::vector<int32_t> lengths;
   std::string err;
   // options
-  bool use_graphs = true, profile = false, pdl = true;
+  bool use_graphs = true, profile = false, pdl = true, use_tc = true, l2_prefetch = true;
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
       cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err;
@@ -426,6 +426,8 @@ qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value) {
     case QWEN3_OPT_CUDA_GRAPHS: h->use_graphs = value != 0; return QWEN3_OK;
     case QWEN3_OPT_PROFILE: h->profile = value != 0; return QWEN3_OK;
     case QWEN3_OPT_PDL: h->pdl = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_TENSOR_CORES: h->use_tc = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_L2_PREFETCH: h->l2_prefetch = value != 0; return QWEN3_OK;
   }
   return fail(h, QWEN3_E_ARG, "unknown option");
 }
@@ -729,7 +731,8 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
 }
 
 // Attention of layer l for the plan's kernel.
-cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l, const Bufs& B) {
+cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l, const Bufs& B,
+                              const void* pf = nullptr, size_t pf_bytes = 0) {
   const qwen3_config& c = h->cfg;
   const qwen3_layer_weights& W = h->layers[l];
   const int dt = h->dt, KV = c.n_kv_heads, D = c.head_dim;
@@ -749,7 +752,8 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
     a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity; a.scale = scale; a.qblocks = qbs;
     a.items = items; a.n_items = n_items; a.part_o = B.part_o; a.part_ml = B.part_ml; a.nq_max = P.nq_max;
     a.counters = B.counters; a.out = B.attn; a.err = B.err;
-    a.grid_x = std::max(1, (h->num_sms * 2 + KV - 1) / KV);
+    a.grid_x = std::max(1, (h->num_sms + KV - 1) / KV);
+    a.pf = pf; a.pf_bytes = pf_bytes;
     return launch(L, "attn_decode", [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
   QkRopeArgs r{};
@@ -780,6 +784,11 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
   void* hres = B.hA;
   auto slot = [&](int s) { return B.sumsq + (size_t)s * T; };
   auto wfmt_of = [&](const qwen3_linear& lin) { return lin.scale ? wf : W_DT; };
+  // bytes of a linear's weight matrix (the codes for int8), for L2 prefetch
+  auto lin_bytes = [&](const qwen3_linear& lin, int rows, int K) {
+    return (size_t)rows * K * (lin.scale ? 1 : h->esz);
+  };
+  const bool pf_on = h->l2_prefetch;
   cudaError_t e;
   for (int l = 0; l < NL; ++l) {
     const qwen3_layer_weights& W = h->layers[l];
@@ -797,18 +806,20 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       e = launch(L, "gemv_qkv", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.qkv), g); });
       if (e != cudaSuccess) return e;
     }
-    e = enqueue_attention(h, L, P, l, B);
+    const bool moe = is_moe_layer(h, l);
+    e = enqueue_attention(h, L, P, l, B, pf_on ? W.o.w : nullptr, lin_bytes(W.o, hid, H * D));
     if (e != cudaSuccess) return e;
     {
       Gemv2Args g{};
       g.T = T; g.K = H * D; g.N = hid; g.w = W.o.w; g.scale = W.o.scale; g.bias = W.o.bias; g.group = c.group_size;
       g.prologue = PRO_X; g.x = B.attn; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
       g.sumsq_out = slot(2 * l + 1); g.err = B.err;
+      if (pf_on && !moe) { g.pf = W.gate_up.w; g.pf_bytes = lin_bytes(W.gate_up, 2 * I, hid); }
       g.stages = gemv2_plan(dt, wfmt_of(W.o), T, H * D, c.group_size, false, nullptr);
       e = launch(L, "gemv_o", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.o), g); });
       if (e != cudaSuccess) return e;
     }
-    if (is_moe_layer(h, l)) {
+    if (moe) {
       NormApplyArgs n{};
       n.h = hres; n.sumsq = slot(2 * l + 1); n.gain = W.post_norm; n.out = B.y; n.T = T; n.hidden = hid;
       n.eps = c.rms_eps;
@@ -823,6 +834,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.T = T; g.K = hid; g.N = I; g.w = W.gate_up.w; g.scale = W.gate_up.scale; g.bias = W.gate_up.bias;
       g.group = c.group_size; g.prologue = PRO_SUMSQ; g.h = hres; g.gain = W.post_norm; g.eps = c.rms_eps;
       g.sumsq_in = slot(2 * l + 1); g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I; g.err = B.err;
+      if (pf_on) { g.pf = W.down.w; g.pf_bytes = lin_bytes(W.down, hid, I); }
       g.stages = gemv2_plan(dt, wfmt_of(W.gate_up), T, hid, c.group_size, true, nullptr);
       e = launch(L, "gemv_gate_up", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.gate_up), g); });
       if (e != cudaSuccess) return e;
@@ -832,6 +844,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.T = T; g.K = I; g.N = hid; g.w = W.down.w; g.scale = W.down.scale; g.bias = W.down.bias;
       g.group = c.group_size; g.prologue = PRO_X; g.x = B.m; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
       g.sumsq_out = slot(2 * l + 2); g.err = B.err;
+      if (pf_on && l + 1 < NL) { g.pf = h->layers[l + 1].qkv.w; g.pf_bytes = lin_bytes(h->layers[l + 1].qkv, qkv_rows, hid); }
       g.stages = gemv2_plan(dt, wfmt_of(W.down), T, I, c.group_size, false, nullptr);
       e = launch(L, "gemv_down", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.down), g); });
       if (e != cudaSuccess) return e;
@@ -841,6 +854,20 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
   n.h = hres; n.sumsq = slot(2 * NL); n.gain = h->final_norm; n.out = out; n.T = T; n.hidden = hid;
   n.eps = c.rms_eps;
   return launch(L, "norm_apply", [&] { return launch_norm_apply(L.ctx, dt, n); });
+}
+
+// A prefill linear: the tcgen05 GEMM for dense bf16 weights on shapes its
+// tile takes, the CUDA-core GEMM otherwise (fp32, int8, ragged N).
+cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const char* tc_name, const char* simt_name, int wfmt,
+                        const GemmArgs& g, const Bufs& B) {
+  if (h->use_tc && h->dt == DT_BF16 && wfmt == W_DT && !g.a_rows && !g.c_rows && !g.tile_start &&
+      gemm_tc_supported(g.M, g.N, g.K, g.epilogue)) {
+    GemmTcArgs t{};
+    t.M = g.M; t.N = g.N; t.K = g.K; t.a = g.a; t.lda = g.lda; t.w = g.w; t.out = g.out; t.ldo = g.ldo;
+    t.epilogue = g.epilogue; t.err = B.err;
+    return launch(L, tc_name, [&] { return launch_gemm_tc(L.ctx, t); });
+  }
+  return launch(L, simt_name, [&] { return launch_gemm_simt(L.ctx, h->dt, wfmt, g); });
 }
 
 // Prefill plan (T > 4): add+RMSNorm kernels, tiled GEMMs, ping-pong residual.
@@ -864,14 +891,14 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
     GemmArgs g{};
     g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
     g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
-    e = launch(L, "gemm_qkv", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.qkv), g); });
+    e = linear_gemm(h, L, "gemm_tc_qkv", "gemm_qkv", wfmt_of(W.qkv), g, B);
     if (e != cudaSuccess) return e;
     e = enqueue_attention(h, L, P, l, B);
     if (e != cudaSuccess) return e;
     GemmArgs go{};
     go.M = T; go.N = hid; go.K = H * D; go.a = B.attn; go.lda = H * D; go.w = W.o.w; go.scale = W.o.scale;
     go.bias = W.o.bias; go.group = c.group_size; go.epilogue = EPI_RESIDUAL; go.out = h_cur; go.ldo = hid;
-    e = launch(L, "gemm_o", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.o), go); });
+    e = linear_gemm(h, L, "gemm_tc_o", "gemm_o", wfmt_of(W.o), go, B);
     if (e != cudaSuccess) return e;
     NormArgs n2{};
     n2.h_in = h_cur; n2.pend = nullptr; n2.h_out = h_cur; n2.y = B.y; n2.gain = W.post_norm; n2.rows = T;
@@ -885,12 +912,12 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
       GemmArgs gu{};
       gu.M = T; gu.N = I; gu.K = hid; gu.a = B.y; gu.lda = hid; gu.w = W.gate_up.w; gu.scale = W.gate_up.scale;
       gu.bias = W.gate_up.bias; gu.group = c.group_size; gu.epilogue = EPI_SWIGLU; gu.out = B.m; gu.ldo = I;
-      e = launch(L, "gemm_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.gate_up), gu); });
+      e = linear_gemm(h, L, "gemm_tc_gate_up", "gemm_gate_up", wfmt_of(W.gate_up), gu, B);
       if (e != cudaSuccess) return e;
       GemmArgs d{};
       d.M = T; d.N = hid; d.K = I; d.a = B.m; d.lda = I; d.w = W.down.w; d.scale = W.down.scale;
       d.bias = W.down.bias; d.group = c.group_size; d.epilogue = EPI_STORE; d.out = B.pend; d.ldo = hid;
-      e = launch(L, "gemm_down", [&] { return launch_gemm_simt(L.ctx, dt, wfmt_of(W.down), d); });
+      e = linear_gemm(h, L, "gemm_tc_down", "gemm_down", wfmt_of(W.down), d, B);
       if (e != cudaSuccess) return e;
     }
     have_pend = true;

@@ -53,6 +53,29 @@ def test_fp32_d128_strict(cuda_ok, n_prefill):
     _prefill_decode(I.with_sizes(SMALL_D128, dtype="fp32"), n_prefill, 3, seed=1300 + n_prefill)
 
 
+TC_CFG = I.with_sizes(SMALL_D128, name="tc_d128", intermediate=1024, capacity=400)
+
+
+@pytest.mark.parametrize("T", [130, 256])
+def test_tensor_core_gemm_prefill(cuda_ok, T):
+    """Prefill with every linear on the tcgen05 GEMM (T=130 leaves a ragged
+    2-row tile): within the bound of the oracle, and within the same bound of
+    the CUDA-core GEMM path run on the same inputs."""
+    w = I.make_weights(TC_CFG, seed=1350 + T)
+    wd = to_device(w)
+    x = I.make_rows(TC_CFG, T, seed=1351).cuda()
+    p = Parity(TC_CFG, weights=w, device_weights=wd)
+    tc, _ = p.step(x)
+    p.check()
+    simt = Q.Qwen3Stack(TC_CFG, wd)
+    Q.qwen3_set_option(simt.h, Q.QWEN3_OPT_TENSOR_CORES, 0)
+    ref_simt = simt.forward(x)
+    assert rel_err(tc, ref_simt) <= p.bound()
+    assert Q.qwen3_device_error(p.stack.h) == 0
+    simt.close()
+    p.close()
+
+
 def test_chunked_prefill_matches_one_pass(cuda_ok):
     """One 96-row prefill, four 24-row chunks and 96 single rows: each against the
     oracle, and the chunked GPU run against the one-pass GPU run."""
