@@ -7,17 +7,21 @@
 // Split-K ("flash-decoding"): the keys of each query block (rows of one
 // sequence, x G query heads of kv head j) are cut into chunks of SUBS
 // sub-chunks of CK keys.  A work item is one (query block, chunk, kv head);
-// a persistent grid walks the item list.  Each block streams the sub-chunks
-// of its items, in order, through a 3-stage shared-memory ring filled by TMA
-// bulk copies (the first ones issued before griddepcontrol.wait, so the KV
-// stream overlaps the qkv projection), and keeps an online softmax (running
-// max m, sum l, output o) over an item's sub-chunks.  Keys appended in this
-// call are computed from the qkv row (RMSNorm + RoPE) and written over their
-// slots once the sub-chunk has landed; the item that owns the row also stores
-// them to the cache.  Each item stores its partial (m, l, o); the last item
-// of a (query block, kv head) -- found with an atomic counter, no waiting --
-// merges them: M = max m_c, out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c,
-// rounded once to the model dtype.
+// a persistent grid walks the item list.
+//
+// Warp-specialised block: one producer warp streams the sub-chunks of the
+// block's items, in order, into a 3-stage shared-memory ring with TMA bulk
+// copies (full / empty mbarriers).  It reads only cached positions, which no
+// kernel in flight writes, so it starts at launch without waiting for the qkv
+// projection.  Sixteen consumer warps normalise and rotate the queries, keep
+// an online softmax (running max m, sum l, output o) over an item's
+// sub-chunks -- P.V split over 512/D key groups, merged once per item -- and
+// compute the keys appended in this call from the qkv row, writing them over
+// their slots once the sub-chunk has landed (the item owning the row also
+// stores them to the cache).  Each item stores its partial (m, l, o); the last
+// item of a (query block, kv head) -- found with an atomic counter, no
+// waiting -- merges them: M = max m_c, out = sum_c e^(m_c - M) o_c /
+// sum_c e^(m_c - M) l_c, rounded once to the model dtype.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -27,8 +31,9 @@ namespace q3 {
 
 namespace {
 
-constexpr int AD_THREADS = 128;
-constexpr int AD_WARPS = AD_THREADS / 32;
+constexpr int AD_CWARPS = 16;                    // consumer warps
+constexpr int AD_CTHREADS = AD_CWARPS * 32;      // 512
+constexpr int AD_THREADS = AD_CTHREADS + 32;     // + producer warp
 constexpr int AD_NQ = 16;
 constexpr int AD_STAGES = 3;
 constexpr int AD_SUBS = 4;  // sub-chunks per item
@@ -38,18 +43,25 @@ template <typename Dt> struct ADT {
 };
 
 template <typename Dt, int D> struct ADLayout {
+  static constexpr int KG = AD_CTHREADS / D;  // key groups in P.V
   static constexpr size_t TILE = (size_t)ADT<Dt>::CK * D * sizeof(Dt);
   static constexpr size_t STAGE = 2 * TILE;
-  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                  // [NQ][D] fp32 queries
-  static constexpr size_t OFF_SC = OFF_QS + (size_t)AD_NQ * D * 4;     // [NQ][CK] scores / p
-  static constexpr size_t OFF_RUN = OFF_SC + (size_t)AD_NQ * ADT<Dt>::CK * 4;  // [NQ] m, l, alpha
-  static constexpr size_t OFF_RED = OFF_RUN + (size_t)AD_NQ * 4 * 4;  // merge: [WARPS][NQ][D] fp32
-  static constexpr size_t OFF_BAR = OFF_RED + (size_t)AD_WARPS * AD_NQ * D * 4;
-  static constexpr size_t TOTAL = OFF_BAR + AD_STAGES * 8 + 16;
+  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                          // [NQ][D] fp32 queries
+  static constexpr size_t OFF_SC = OFF_QS + (size_t)AD_NQ * D * 4;             // [NQ][CK] scores / p
+  static constexpr size_t OFF_RUN = OFF_SC + (size_t)AD_NQ * ADT<Dt>::CK * 4;  // [NQ][4] m, l, alpha
+  static constexpr size_t OFF_RED = OFF_RUN + (size_t)AD_NQ * 4 * 4;           // [KG][NQ][D] fp32 (32 KB)
+  static constexpr size_t RED_FLOATS = (size_t)KG * AD_NQ * D;
+  static constexpr size_t OFF_BAR = OFF_RED + RED_FLOATS * 4;
+  static constexpr size_t TOTAL = OFF_BAR + 2 * AD_STAGES * 8 + 16;
 };
+
+// Named barrier over the consumer warps only.
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(AD_CTHREADS) : "memory"); }
 
 // Per-head RMSNorm + RoPE of one raw q or k head (warp-wide: lane holds
 // elements lane*DPL .. +DPL) at position pos, rounded to the model dtype.
+// RMS statistics in double.  RoPE: for bf16 both products are exact in fp32
+// and fmaf rounds their difference once; for fp32 they are formed in double.
 template <typename Dt, int D>
 __device__ __forceinline__ void norm_rope_head(float* x, const Dt* gain, const float* cos_t, const float* sin_t,
                                                int pos, float eps) {
@@ -69,22 +81,25 @@ __device__ __forceinline__ void norm_rope_head(float* x, const Dt* gain, const f
 #pragma unroll
   for (int e = 0; e < DPL; ++e) {
     const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
-    const double xc = (double)x[e] * (double)cs[e], ps = (double)partner * (double)sn[e];
-    o[e] = rd_d<Dt>(first ? xc - ps : xc + ps);
+    if (sizeof(Dt) == 2) {
+      const float ps = partner * sn[e];  // exact: 8-bit x 8-bit significands
+      o[e] = rd<Dt>(first ? fmaf(x[e], cs[e], -ps) : fmaf(x[e], cs[e], ps));
+    } else {
+      const double xc = (double)x[e] * (double)cs[e], ps = (double)partner * (double)sn[e];
+      o[e] = rd_d<Dt>(first ? xc - ps : xc + ps);
+    }
   }
 #pragma unroll
   for (int e = 0; e < DPL; ++e) x[e] = o[e];
 }
 
-// Keys of item `it`: [key0, key0 + nkeys).
+// Keys of item `it`: [key0, key0 + nkeys) in nsub sub-chunks.
 struct ItemKeys {
   int key0, nkeys, nsub;
 };
 template <typename Dt>
-__device__ __forceinline__ ItemKeys item_keys(const AttnDecArgs& a, int it) {
+__device__ __forceinline__ ItemKeys item_keys(const AttnItem& item, const AttnQBlock& qb) {
   constexpr int CK = ADT<Dt>::CK;
-  const AttnItem item = a.items[it];
-  const AttnQBlock qb = a.qblocks[item.qb];
   ItemKeys r;
   r.key0 = item.chunk * CK * AD_SUBS;
   r.nkeys = min(CK * AD_SUBS, qb.pos0 + qb.nrows - r.key0);
@@ -93,10 +108,11 @@ __device__ __forceinline__ ItemKeys item_keys(const AttnDecArgs& a, int it) {
 }
 
 template <typename Dt, int D>
-__global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) {
+__global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs a) {
   extern __shared__ __align__(128) uint8_t ad_smem[];
   using LY = ADLayout<Dt, D>;
   constexpr int CK = ADT<Dt>::CK;
+  constexpr int KG = LY::KG;
   constexpr int EPV = 16 / sizeof(Dt);  // elements per 16-byte vector
   constexpr int LPK = D / EPV;          // lanes per key in the score loop
   constexpr int KPW = 32 / LPK;         // keys per warp step
@@ -105,70 +121,76 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) 
   float* sc = reinterpret_cast<float*>(ad_smem + LY::OFF_SC);
   float* run = reinterpret_cast<float*>(ad_smem + LY::OFF_RUN);  // [i*4]: m, l, alpha
   float* red = reinterpret_cast<float*>(ad_smem + LY::OFF_RED);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
-  __shared__ int s_flag;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
+  uint64_t* empty = full + AD_STAGES;
+  __shared__ int s_flag, s_fail;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.y;
   const int G = a.H / a.KV;
   const int qkv_ld = (a.H + 2 * a.KV) * D;
   const int n_items = *a.n_items;
-  const Dt* qkv = static_cast<const Dt*>(a.qkv);
-  const Dt* kc = static_cast<const Dt*>(a.kc);
-  const Dt* vc = static_cast<const Dt*>(a.vc);
   auto tiles = [&](int s) { return ad_smem + (size_t)s * LY::STAGE; };
 
-  // Producer cursor (thread 0 only): next (local item, sub-chunk) to load.
-  int p_k = 0, p_sub = 0, p_g = 0;
-  auto produce = [&]() {  // issue the next sub-chunk of this block's item sequence, if any
-    while (true) {
-      const int it = blockIdx.x + p_k * gridDim.x;
-      if (it >= n_items) return;
-      const ItemKeys ik = item_keys<Dt>(a, it);
-      if (p_sub >= ik.nsub) { ++p_k; p_sub = 0; continue; }
-      const AttnQBlock qb = a.qblocks[a.items[it].qb];
-      const int k0 = ik.key0 + p_sub * CK;
-      const int nk = min(CK, ik.key0 + ik.nkeys - k0);
-      const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
-      const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
-      const int s = p_g % AD_STAGES;
-      mbar_expect_tx(&bars[s], 2 * bytes);
-      tma_load_1d(tiles(s), kc + off, bytes, &bars[s]);
-      tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &bars[s]);
-      ++p_sub;
-      ++p_g;
-      return;
-    }
-  };
-
-  // The cached keys do not depend on the previous kernel: start the copies.
   if (tid == 0) {
-    for (int s = 0; s < AD_STAGES; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < AD_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
     mbar_fence_init();
-    for (int s = 0; s < AD_STAGES; ++s) produce();
-  }
-  // ... and ask L2 for the next kernel's operand (its share of it).
-  if (tid == 32 && a.pf && a.pf_bytes) {
-    const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
-    const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
-    for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
-      prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
+    s_fail = 0;
   }
   __syncthreads();
+
+  if (warp == AD_CWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      // L2 prefetch of this block's share of the next kernel's operand
+      if (a.pf && a.pf_bytes) {
+        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+        const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
+        for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
+          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
+      }
+      const Dt* kc = static_cast<const Dt*>(a.kc);
+      const Dt* vc = static_cast<const Dt*>(a.vc);
+      int g = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const AttnItem item = a.items[it];
+        const AttnQBlock qb = a.qblocks[item.qb];
+        const ItemKeys ik = item_keys<Dt>(item, qb);
+        for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
+          const int s = g % AD_STAGES;
+          if (g >= AD_STAGES && !mbar_wait(&empty[s], (uint32_t)((g / AD_STAGES - 1) & 1), a.err, 2)) {
+            s_fail = 1;
+            return;
+          }
+          const int k0 = ik.key0 + sub * CK;
+          const int nk = min(CK, ik.key0 + ik.nkeys - k0);
+          const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
+          const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
+          mbar_expect_tx(&full[s], 2 * bytes);
+          tma_load_1d(tiles(s), kc + off, bytes, &full[s]);
+          tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
   pdl_wait();
   pdl_launch();
-
-  int g = 0;  // consumer position in the block's sub-chunk sequence
-  bool failed = false;
-  for (int k = 0; !failed; ++k) {
-    const int it = blockIdx.x + k * gridDim.x;
-    if (it >= n_items) break;
+  const Dt* qkv = static_cast<const Dt*>(a.qkv);
+  const int kg = tid / D, dcol = tid % D;  // P.V key group and head element of this thread
+  int g = 0;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const AttnItem item = a.items[it];
     const AttnQBlock qb = a.qblocks[item.qb];
-    const ItemKeys ik = item_keys<Dt>(a, it);
+    const ItemKeys ik = item_keys<Dt>(item, qb);
     const int nq = qb.nrows * G;
 
-    // queries: RMSNorm + RoPE of this block's q heads of kv group j
-    for (int i = warp; i < nq; i += AD_WARPS) {
+    // queries: RMSNorm + RoPE of this block's q heads of kv group j (warp per query)
+    for (int i = warp; i < nq; i += AD_CWARPS) {
       const int row = qb.row0 + i / G, hh = j * G + i % G;
       float x[DPL];
       const Dt* src = qkv + (size_t)row * qkv_ld + (size_t)hh * D + lane * DPL;
@@ -186,17 +208,18 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) 
 #pragma unroll
     for (int i = 0; i < AD_NQ; ++i) o[i] = 0.f;
 
+    bool failed = false;
     for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
       const int s = g % AD_STAGES;
       const int key0 = ik.key0 + sub * CK;
       const int nk = min(CK, ik.key0 + ik.nkeys - key0);
       Dt* Kt = reinterpret_cast<Dt*>(tiles(s));
       Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE);
-      const bool landed = mbar_wait(&bars[s], (uint32_t)((g / AD_STAGES) & 1), a.err, 2);
-      if (__syncthreads_or(!landed)) { failed = true; break; }
-      // keys appended by this call that fall in the sub-chunk: computed here
+      const bool landed = mbar_wait(&full[s], (uint32_t)((g / AD_STAGES) & 1), a.err, 2);
+      if (!landed) s_fail = 1;
+      // keys appended by this call that fall in the sub-chunk: computed here (warp per key)
       const int n0 = max(key0, qb.seg_pos0), n1 = min(key0 + nk, qb.seg_pos0 + qb.seg_n);
-      for (int u = n0 + warp; u < n1; u += AD_WARPS) {
+      for (int u = n0 + warp; u < n1 && landed; u += AD_CWARPS) {
         const int row = qb.seg_row0 + (u - qb.seg_pos0);
         float x[DPL], v[DPL];
         const Dt* ksrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + j) * D + lane * DPL;
@@ -216,11 +239,12 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) 
           }
         }
       }
-      __syncthreads();
+      csync();
+      if (s_fail) { failed = true; break; }
       // scores: LPK lanes per key, KPW keys per warp step
       {
         const int sub_l = lane % LPK;
-        for (int ub = warp * KPW; ub < nk; ub += AD_WARPS * KPW) {
+        for (int ub = warp * KPW; ub < nk; ub += AD_CWARPS * KPW) {
           const int u = ub + lane / LPK;
           float kv[EPV];
           if (u < nk) {
@@ -231,9 +255,13 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) 
           }
           for (int i = 0; i < nq; ++i) {
             const float* qp = qs + i * D + sub_l * EPV;
-            float d = 0.f;
+            float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) d = fmaf(qp[e], kv[e], d);
+            for (int e = 0; e < EPV; e += 2) {
+              d0 = fmaf(qp[e], kv[e], d0);
+              d1 = fmaf(qp[e + 1], kv[e + 1], d1);
+            }
+            float d = d0 + d1;
 #pragma unroll
             for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
             if (sub_l == 0 && u < nk)
@@ -241,9 +269,9 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) 
           }
         }
       }
-      __syncthreads();
+      csync();
       // online softmax update per query (warp per query)
-      for (int i = warp; i < nq; i += AD_WARPS) {
+      for (int i = warp; i < nq; i += AD_CWARPS) {
         float mc = -CUDART_INF_F;
         for (int u = lane; u < nk; u += 32) mc = fmaxf(mc, sc[i * CK + u]);
         mc = warp_max(mc);
@@ -264,106 +292,102 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_kernel(AttnDecArgs a) 
           run[i * 4 + 2] = alpha;
         }
       }
-      __syncthreads();
-      if (tid < D) {
+      csync();
+      // P.V: thread (key group kg, element dcol) over keys kg, kg + KG, ...
+#pragma unroll
+      for (int i = 0; i < AD_NQ; ++i)
+        if (i < nq) o[i] *= run[i * 4 + 2];
+      for (int u = kg; u < nk; u += KG) {
+        const float v = to_f(Vt[(size_t)u * D + dcol]);
 #pragma unroll
         for (int i = 0; i < AD_NQ; ++i)
-          if (i < nq) o[i] *= run[i * 4 + 2];
-        int u = 0;
-        for (; u + 4 <= nk; u += 4) {
-          const float v0 = to_f(Vt[(size_t)u * D + tid]), v1 = to_f(Vt[(size_t)(u + 1) * D + tid]);
-          const float v2 = to_f(Vt[(size_t)(u + 2) * D + tid]), v3 = to_f(Vt[(size_t)(u + 3) * D + tid]);
-#pragma unroll
-          for (int i = 0; i < AD_NQ; ++i)
-            if (i < nq) {
-              const float4 p = *reinterpret_cast<const float4*>(sc + i * CK + u);
-              o[i] = fmaf(p.x, v0, fmaf(p.y, v1, fmaf(p.z, v2, fmaf(p.w, v3, o[i]))));
-            }
-        }
-        for (; u < nk; ++u) {
-          const float v = to_f(Vt[(size_t)u * D + tid]);
-#pragma unroll
-          for (int i = 0; i < AD_NQ; ++i)
-            if (i < nq) o[i] = fmaf(sc[i * CK + u], v, o[i]);
-        }
+          if (i < nq) o[i] = fmaf(sc[i * CK + u], v, o[i]);
       }
-      // release the stage; refill it with the next sub-chunk of the sequence
-      fence_proxy_async();
-      __syncthreads();
-      if (tid == 0) produce();
+      // release the stage to the producer
+      csync();
+      if (tid == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
     }
     if (failed) break;
 
-    // partial of this item
-    const size_t part0 = ((size_t)(qb.part_base + item.chunk) * a.KV + j) * a.nq_max;
-    if (tid < D) {
+    // merge the key groups, then store this item's partial
 #pragma unroll
-      for (int i = 0; i < AD_NQ; ++i)
-        if (i < nq) a.part_o[(part0 + i) * D + tid] = o[i];
+    for (int i = 0; i < AD_NQ; ++i)
+      if (i < nq) red[(kg * AD_NQ + i) * D + dcol] = o[i];
+    csync();
+    const size_t part0 = ((size_t)(qb.part_base + item.chunk) * a.KV + j) * a.nq_max;
+    for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
+      const int i = idx / D, d = idx % D;
+      float v = 0.f;
+#pragma unroll
+      for (int q = 0; q < KG; ++q) v += red[(q * AD_NQ + i) * D + d];
+      a.part_o[(part0 + i) * D + d] = v;
     }
     if (tid < nq) {
       a.part_ml[(part0 + tid) * 2] = run[tid * 4];
       a.part_ml[(part0 + tid) * 2 + 1] = run[tid * 4 + 1];
     }
     __threadfence();
-    __syncthreads();
+    csync();
     if (tid == 0) {
       const int prev = atomicAdd(a.counters + (size_t)item.qb * a.KV + j, 1);
       s_flag = (prev == qb.n_chunks - 1);
     }
-    __syncthreads();
+    csync();
     if (s_flag) {
       __threadfence();
       const int nc = qb.n_chunks;
       const size_t pbase = (size_t)qb.part_base * a.KV + j;  // partial of chunk c: (pbase + c * KV) * nq_max
+      const bool staged = (size_t)nc * nq <= LY::RED_FLOATS;
+      float* fs = red;  // [c][i]: chunk maxima, then their weights e^(m_c - M_i)
+      if (staged) {
+        for (int idx = tid; idx < nc * nq; idx += AD_CTHREADS) {
+          const int c = idx / nq, i = idx % nq;
+          fs[idx] = __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
+        }
+        csync();
+      }
       // per-query max and normaliser (warp per query, lanes over chunks)
-      for (int i = warp; i < nq; i += AD_WARPS) {
+      for (int i = warp; i < nq; i += AD_CWARPS) {
+        auto mval = [&](int c) {
+          return staged ? fs[c * nq + i] : __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
+        };
         float M = -CUDART_INF_F;
-        for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2));
+        for (int c = lane; c < nc; c += 32) M = fmaxf(M, mval(c));
         M = warp_max(M);
         float Lsum = 0.f;
         for (int c = lane; c < nc; c += 32) {
-          const size_t p = ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2;
-          const float m = __ldcg(a.part_ml + p);
-          if (m != -CUDART_INF_F) Lsum = fmaf(__ldcg(a.part_ml + p + 1), expf(m - M), Lsum);
+          const float m = mval(c);
+          const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+          Lsum = fmaf(__ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2 + 1), f, Lsum);
+          if (staged) fs[c * nq + i] = f;
         }
         Lsum = warp_sum(Lsum);
         if (lane == 0) { run[i * 4] = M; run[i * 4 + 1] = Lsum; }
       }
-      __syncthreads();
-      // weighted chunk sums: warp w takes chunks w, w + 4, ...; fixed-order sum over warps
-      for (int i = 0; i < nq; ++i) {
-        float acc[DPL];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-        const float M = run[i * 4];
-#pragma unroll 4
-        for (int c = warp; c < nc; c += AD_WARPS) {
-          const size_t p = (pbase + (size_t)c * a.KV) * a.nq_max + i;
-          const float m = __ldcg(a.part_ml + p * 2);
-          const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[e] = fmaf(__ldcg(a.part_o + p * D + lane * DPL + e), f, acc[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) red[(warp * AD_NQ + i) * D + lane * DPL + e] = acc[e];
-      }
-      __syncthreads();
-      for (int idx = tid; idx < nq * D; idx += AD_THREADS) {
+      csync();
+      // out[i][d] = sum_c f[c][i] o_c[i][d] / L_i, one thread per output element
+      for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
         const int i = idx / D, d = idx % D;
+        const float M = run[i * 4];
         float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < AD_WARPS; ++w) v += red[(w * AD_NQ + i) * D + d];
+#pragma unroll 4
+        for (int c = 0; c < nc; ++c) {
+          const size_t p = (pbase + (size_t)c * a.KV) * a.nq_max + i;
+          float f;
+          if (staged) {
+            f = fs[c * nq + i];
+          } else {
+            const float m = __ldcg(a.part_ml + p * 2);
+            f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+          }
+          v = fmaf(__ldcg(a.part_o + p * D + d), f, v);
+        }
         const int row = qb.row0 + i / G, head = j * G + i % G;
         static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / run[i * 4 + 1]);
       }
       if (tid == 0) a.counters[(size_t)item.qb * a.KV + j] = 0;
-      __syncthreads();
     }
-  }
-  if (failed && tid == 0) {
-    // give the copies still in flight a bounded chance to land before exiting
-    for (int q = g + 1; q < p_g; ++q) mbar_wait(&bars[q % AD_STAGES], (uint32_t)((q / AD_STAGES) & 1), a.err, 2);
+    csync();
   }
 }
 

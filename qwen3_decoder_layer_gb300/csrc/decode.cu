@@ -1,15 +1,19 @@
-// Decode-path kernels (T <= 4 rows per call) of the Qwen3 stack forward
-// (maya2_mlx/backbone.py, Backbone.forward), built so that each step's HBM
-// stream starts before the step it depends on has finished:
+// Decode-path linears (T <= 4 rows per call) of the Qwen3 stack forward
+// (maya2_mlx/backbone.py, Backbone.forward: `Q.mm(y, L["qkv"])`,
+// `Q.mm(a, L["o"])` with the residual add, `Q.mm(y2, L["gu"])` with the fp32
+// SiLU * up, `Q.mm(act * u, L["down"])` with the residual add), and the final
+// RMSNorm.
 //
-//  * gemv2: the linears.  Every warp owns a strided set of weight rows (gate
-//    and up rows together for SiLU * up) and streams them through its own
-//    ring of shared-memory slots filled by TMA bulk copies.  The first copies
-//    are issued before griddepcontrol.wait, i.e. while the previous kernel is
-//    still running under programmatic dependent launch.  The residual
+//  * gemv2: every warp owns a strided set of weight rows (gate and up rows
+//    together for SiLU * up) and streams them through its own ring of
+//    shared-memory slots filled by TMA bulk copies.  The first copies are
+//    issued before griddepcontrol.wait, i.e. while the previous kernel is
+//    still running under programmatic dependent launch, and one thread also
+//    asks L2 for the next linear's weights.  The normalised input rows sit in
+//    shared memory as fp32; each row's dot product runs as independent
+//    accumulator chains (one per unrolled 16-byte vector).  The residual
 //    epilogue (o_proj, down_proj) updates h in place and accumulates the sum
 //    of squares of the new rows, so the following RMSNorm needs no reduction.
-//  * attention: see attn_decode.cu.
 //  * norm_apply: the final RMSNorm from the precomputed sum of squares.
 #include <math_constants.h>
 
@@ -22,23 +26,20 @@ namespace {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// ============================================================ gemv2
-constexpr int G2_WARPS = 8;
-constexpr int G2_THREADS = G2_WARPS * 32;
-constexpr int G2_UNROLL = 4;
+constexpr int G2_MAX_WARPS = 16;
 constexpr size_t G2_SMEM_LIMIT = 220 * 1024;
 
 struct G2Layout {
   size_t x_bytes, row_bytes, unit_bytes, ring_bytes, total;
 };
 
-__host__ __device__ inline G2Layout g2_layout(int wbytes, int T, int K, bool pair, int stages) {
+__host__ __device__ inline G2Layout g2_layout(int wbytes, int T, int K, bool pair, int stages, int nwarps) {
   G2Layout L;
   L.x_bytes = align_up((size_t)T * K * 4, 128);
   L.row_bytes = (size_t)K * wbytes;
   L.unit_bytes = align_up((pair ? 2 : 1) * L.row_bytes, 128);
-  L.ring_bytes = (size_t)G2_WARPS * stages * L.unit_bytes;
-  L.total = L.x_bytes + L.ring_bytes + (size_t)G2_WARPS * stages * 8 + G2_WARPS * 4 * 8;
+  L.ring_bytes = (size_t)nwarps * stages * L.unit_bytes;
+  L.total = L.x_bytes + L.ring_bytes + (size_t)nwarps * stages * 8 + G2_MAX_WARPS * 4 * 8;
   return L;
 }
 
@@ -141,20 +142,22 @@ __device__ __forceinline__ void prefetch_share(const void* p, size_t bytes) {
 }
 
 template <typename Dt, int WF, int NT, int EPI>
-__global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
+__global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a) {
   extern __shared__ __align__(128) uint8_t g2_smem[];
   using W = G2W<Dt, WF>;
   constexpr bool PAIR = (EPI == EPI_SWIGLU);
+  constexpr int U = (NT * (PAIR ? 2 : 1) * W::EPV > 32) ? 2 : 4;  // 16-byte vectors in flight per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
   const int S = a.stages;
-  const G2Layout L = g2_layout(W::BYTES, NT, a.K, PAIR, S);
+  const G2Layout L = g2_layout(W::BYTES, NT, a.K, PAIR, S, nwarps);
   float* xs = reinterpret_cast<float*>(g2_smem);
   uint8_t* ring = g2_smem + L.x_bytes + (size_t)warp * S * L.unit_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(g2_smem + L.x_bytes + L.ring_bytes) + warp * S;
-  double* red = reinterpret_cast<double*>(g2_smem + L.x_bytes + L.ring_bytes + (size_t)G2_WARPS * S * 8);
+  double* red = reinterpret_cast<double*>(g2_smem + L.x_bytes + L.ring_bytes + (size_t)nwarps * S * 8);
   __shared__ double red_norm[32];
 
-  const int gw = blockIdx.x * G2_WARPS + warp, nw = gridDim.x * G2_WARPS;
+  const int gw = blockIdx.x * nwarps + warp, nw = gridDim.x * nwarps;
   const char* wb = static_cast<const char*>(a.w);
   const uint32_t unit_tx = (uint32_t)((PAIR ? 2 : 1) * L.row_bytes);
 
@@ -193,13 +196,15 @@ __global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
     const int s = k % S;
     if (!mbar_wait(&bars[s], (uint32_t)((k / S) & 1), a.err, 1)) { ok = false; break; }
     const uint8_t* slot = ring + (size_t)s * L.unit_bytes;
-    float acc[NT], acc2[NT];
+    float acc[NT][U], acc2[NT][U];  // independent chains, one per unrolled vector
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = acc2[t] = 0.f;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * G2_UNROLL) {
-      uint4 q0[G2_UNROLL], q1[G2_UNROLL];
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int i = 0; i < G2_UNROLL; ++i) {
+      for (int i = 0; i < U; ++i) acc[t][i] = acc2[t][i] = 0.f;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+      uint4 q0[U], q1[U];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
         const int v = v0 + 32 * i;
         if (v < nvec) {
           q0[i] = *reinterpret_cast<const uint4*>(slot + (size_t)v * 16);
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
         }
       }
 #pragma unroll
-      for (int i = 0; i < G2_UNROLL; ++i) {
+      for (int i = 0; i < U; ++i) {
         const int v = v0 + 32 * i;
         if (v >= nvec) break;
         const int k0 = v * W::EPV;
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
         for (int t = 0; t < NT; ++t) {
           const float* xp = xs + (size_t)t * a.K + k0;
 #pragma unroll
-          for (int e = 0; e < W::EPV; ++e) acc[t] = fmaf(w0[e], xp[e], acc[t]);
+          for (int e = 0; e < W::EPV; ++e) acc[t][i] = fmaf(w0[e], xp[e], acc[t][i]);
         }
         if (PAIR) {
           float w1[W::EPV];
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
           for (int t = 0; t < NT; ++t) {
             const float* xp = xs + (size_t)t * a.K + k0;
 #pragma unroll
-            for (int e = 0; e < W::EPV; ++e) acc2[t] = fmaf(w1[e], xp[e], acc2[t]);
+            for (int e = 0; e < W::EPV; ++e) acc2[t][i] = fmaf(w1[e], xp[e], acc2[t][i]);
           }
         }
       }
@@ -240,16 +245,20 @@ __global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
         issue(un, s);
       }
     }
+    float r[NT], r2[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      acc[t] = warp_sum(acc[t]);
-      if (PAIR) acc2[t] = warp_sum(acc2[t]);
+      float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < U; ++i) { s1 += acc[t][i]; s2 += acc2[t][i]; }
+      r[t] = warp_sum(s1);
+      r2[t] = PAIR ? warp_sum(s2) : 0.f;
     }
     if (lane < NT) {
-      float v = acc[0], v2 = acc2[0];
+      float v = r[0], v2 = r2[0];
 #pragma unroll
       for (int t = 1; t < NT; ++t)
-        if (lane == t) { v = acc[t]; v2 = acc2[t]; }
+        if (lane == t) { v = r[t]; v2 = r2[t]; }
       const size_t o = (size_t)lane * a.ldo + u;
       if (EPI == EPI_STORE) {
         static_cast<Dt*>(a.out)[o] = from_f<Dt>(v);
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(G2_THREADS, 1) gemv2_kernel(Gemv2Args a) {
     __syncthreads();
     if (threadIdx.x < NT) {
       double s = 0.0;
-      for (int w = 0; w < G2_WARPS; ++w) s += red[w * 4 + threadIdx.x];
+      for (int w = 0; w < nwarps; ++w) s += red[w * 4 + threadIdx.x];
       atomicAdd(a.sumsq_out + threadIdx.x, s);
     }
   }
@@ -291,10 +300,10 @@ cudaError_t g2_launch(const LaunchCtx& c, const Gemv2Args& a) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const G2Layout L = g2_layout(WF == W_U8 ? 1 : (int)sizeof(Dt), NT, a.K, EPI == EPI_SWIGLU, a.stages);
-  int grid = (a.N + G2_WARPS - 1) / G2_WARPS;
+  const G2Layout L = g2_layout(WF == W_U8 ? 1 : (int)sizeof(Dt), NT, a.K, EPI == EPI_SWIGLU, a.stages, a.nwarps);
+  int grid = (a.N + a.nwarps - 1) / a.nwarps;
   if (grid > c.num_sms) grid = c.num_sms;
-  return launch_k(kern, dim3(grid), dim3(G2_THREADS), L.total, c, a);
+  return launch_k(kern, dim3(grid), dim3(a.nwarps * 32), L.total, c, a);
 }
 
 template <typename Dt, int WF, int EPI>
@@ -322,6 +331,7 @@ cudaError_t g2_epi(const LaunchCtx& c, const Gemv2Args& a) {
 // ============================================================ norm_apply
 template <typename Dt>
 __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
+  constexpr int V = Vec16<Dt>::N;
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
@@ -329,26 +339,35 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
   const Dt* h = static_cast<const Dt*>(a.h) + (size_t)t * a.hidden;
   const Dt* g = static_cast<const Dt*>(a.gain);
   Dt* out = static_cast<Dt*>(a.out) + (size_t)t * a.hidden;
-  for (int k = threadIdx.x; k < a.hidden; k += blockDim.x) out[k] = from_f<Dt>(rms_apply<Dt>(to_f(h[k]), rs, to_f(g[k])));
+  for (int k = threadIdx.x * V; k < a.hidden; k += blockDim.x * V) {
+    float hv[V], gv[V], o[V];
+    Vec16<Dt>::unpack(ld16(h + k), hv);
+    Vec16<Dt>::unpack(ld16(g + k), gv);
+#pragma unroll
+    for (int e = 0; e < V; ++e) o[e] = rms_apply<Dt>(hv[e], rs, gv[e]);
+    *reinterpret_cast<uint4*>(out + k) = Vec16<Dt>::pack(o);
+  }
 }
 
 }  // namespace
 
-int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, size_t* smem) {
+int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps) {
   (void)group;
   const int wbytes = wfmt == W_U8 ? 1 : (dt == DT_BF16 ? 2 : 4);
-  for (int s = 4; s >= 1; --s) {
-    const G2Layout L = g2_layout(wbytes, T, K, pair, s);
-    if (L.total <= G2_SMEM_LIMIT) {
-      if (smem) *smem = L.total;
-      return s;
+  for (int nw = G2_MAX_WARPS; nw >= 4; nw /= 2)
+    for (int s = 4; s >= (nw == 4 ? 1 : 2); --s) {
+      const G2Layout L = g2_layout(wbytes, T, K, pair, s, nw);
+      if (L.total <= G2_SMEM_LIMIT) {
+        if (nwarps) *nwarps = nw;
+        return s;
+      }
     }
-  }
-  return 0;
+  if (nwarps) *nwarps = 4;
+  return g2_layout(wbytes, T, K, pair, 1, 4).total <= G2_SMEM_LIMIT ? 1 : 0;
 }
 
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a) {
-  if (a.T < 1 || a.T > 4 || a.stages < 1) return cudaErrorInvalidValue;
+  if (a.T < 1 || a.T > 4 || a.stages < 1 || a.nwarps < 1 || a.nwarps > G2_MAX_WARPS) return cudaErrorInvalidValue;
   if (dt == DT_BF16) return wfmt == W_U8 ? g2_epi<bf16, W_U8>(c, a) : g2_epi<bf16, W_DT>(c, a);
   return wfmt == W_U8 ? g2_epi<float, W_U8>(c, a) : g2_epi<float, W_DT>(c, a);
 }

@@ -233,14 +233,16 @@ struct Gemv2Args {
   void* out;
   int ldo;
   double* sumsq_out;
-  int stages;
+  int stages;          // ring slots per warp
+  int nwarps;          // warps per block
   int* err;
   const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
   size_t pf_bytes;
 };
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a);
-// Ring slots per warp that fit, and the dynamic shared memory they need (0 = does not fit).
-int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, size_t* smem);
+// Ring slots per warp (return value, 0 = does not fit) and warps per block
+// (*nwarps) for a linear of K inputs at T rows.
+int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps);
 
 // Decode attention with the q/k RMSNorm, RoPE and cache append fused in:
 // items as in AttnArgs; K/V chunks stream into a shared-memory ring by TMA;

@@ -802,7 +802,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       } else {
         g.prologue = PRO_SUMSQ; g.sumsq_in = slot(2 * l);
       }
-      g.stages = gemv2_plan(dt, wfmt_of(W.qkv), T, hid, c.group_size, false, nullptr);
+      g.stages = gemv2_plan(dt, wfmt_of(W.qkv), T, hid, c.group_size, false, &g.nwarps);
       e = launch(L, "gemv_qkv", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.qkv), g); });
       if (e != cudaSuccess) return e;
     }
@@ -815,7 +815,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.prologue = PRO_X; g.x = B.attn; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
       g.sumsq_out = slot(2 * l + 1); g.err = B.err;
       if (pf_on && !moe) { g.pf = W.gate_up.w; g.pf_bytes = lin_bytes(W.gate_up, 2 * I, hid); }
-      g.stages = gemv2_plan(dt, wfmt_of(W.o), T, H * D, c.group_size, false, nullptr);
+      g.stages = gemv2_plan(dt, wfmt_of(W.o), T, H * D, c.group_size, false, &g.nwarps);
       e = launch(L, "gemv_o", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.o), g); });
       if (e != cudaSuccess) return e;
     }
@@ -835,7 +835,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.group = c.group_size; g.prologue = PRO_SUMSQ; g.h = hres; g.gain = W.post_norm; g.eps = c.rms_eps;
       g.sumsq_in = slot(2 * l + 1); g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I; g.err = B.err;
       if (pf_on) { g.pf = W.down.w; g.pf_bytes = lin_bytes(W.down, hid, I); }
-      g.stages = gemv2_plan(dt, wfmt_of(W.gate_up), T, hid, c.group_size, true, nullptr);
+      g.stages = gemv2_plan(dt, wfmt_of(W.gate_up), T, hid, c.group_size, true, &g.nwarps);
       e = launch(L, "gemv_gate_up", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.gate_up), g); });
       if (e != cudaSuccess) return e;
     }
@@ -845,7 +845,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.group = c.group_size; g.prologue = PRO_X; g.x = B.m; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
       g.sumsq_out = slot(2 * l + 2); g.err = B.err;
       if (pf_on && l + 1 < NL) { g.pf = h->layers[l + 1].qkv.w; g.pf_bytes = lin_bytes(h->layers[l + 1].qkv, qkv_rows, hid); }
-      g.stages = gemv2_plan(dt, wfmt_of(W.down), T, I, c.group_size, false, nullptr);
+      g.stages = gemv2_plan(dt, wfmt_of(W.down), T, I, c.group_size, false, &g.nwarps);
       e = launch(L, "gemv_down", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.down), g); });
       if (e != cudaSuccess) return e;
     }
