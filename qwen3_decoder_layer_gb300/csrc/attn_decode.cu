@@ -60,20 +60,21 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(A
 
 // Per-head RMSNorm + RoPE of one raw q or k head (warp-wide: lane holds
 // elements lane*DPL .. +DPL) at position pos, rounded to the model dtype.
-// RMS statistics in double.  RoPE: for bf16 both products are exact in fp32
-// and fmaf rounds their difference once; for fp32 they are formed in double.
+// RMS statistics in compensated fp32 pairs.  RoPE: for bf16 both products
+// are exact in fp32 and fmaf rounds their difference once; for fp32 they are
+// formed in double.
 template <typename Dt, int D>
 __device__ __forceinline__ void norm_rope_head(float* x, const Dt* gain, const float* cos_t, const float* sin_t,
                                                int pos, float eps) {
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
-  double ss = 0.0;
+  F2 ss = {0.f, 0.f};
 #pragma unroll
-  for (int e = 0; e < DPL; ++e) ss = fma((double)x[e], (double)x[e], ss);
-  ss = warp_sum_d(ss);
-  const double rs = rms_scale(ss, D, eps);
+  for (int e = 0; e < DPL; ++e) f2_add_sq(ss, x[e]);
+  ss = f2_warp_sum(ss);
+  const F2 rs = rms_scale2(ss, D, eps);
 #pragma unroll
-  for (int e = 0; e < DPL; ++e) x[e] = rms_apply<Dt>(x[e], rs, to_f(gain[lane * DPL + e]));
+  for (int e = 0; e < DPL; ++e) x[e] = rms_apply2<Dt>(x[e], rs, to_f(gain[lane * DPL + e]));
   const float* cs = cos_t + (size_t)pos * D + lane * DPL;
   const float* sn = sin_t + (size_t)pos * D + lane * DPL;
   const bool first = lane < 16;

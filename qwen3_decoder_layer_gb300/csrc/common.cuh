@@ -166,34 +166,114 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return warp_sum(t);
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+// ---------------------------------------------------------------- double-float
+// fp32 pairs (hi + lo) with error-free transformations: FP64 throughput on this
+// part is a small fraction of FP32, so the RMSNorm statistics, scale and
+// normalised product are carried in pairs of floats instead of doubles, with
+// the same effect (no rounding decision differs from exact arithmetic except
+// where the exact value is within ~2^-40 relative of a tie).
+struct F2 {
+  float hi, lo;
+};
+// s + e == a + b exactly (Knuth's two-sum; additions only, so no contraction).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e += a.lo + b.lo;
+  F2 r;
+  r.hi = s + e;
+  r.lo = e - (r.hi - s);
+  return r;
+}
+// Add v*v (formed exactly with an fma for the low part) to an accumulator.
+__device__ __forceinline__ void f2_add_sq(F2& acc, float v) {
+  const float p = v * v;
+  const float pe = fmaf(v, v, -p);
+  float s, e;
+  two_sum(acc.hi, p, s, e);
+  acc.hi = s;
+  acc.lo += e + pe;
+}
+__device__ __forceinline__ F2 f2_warp_sum(F2 a) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  for (int o = 16; o > 0; o >>= 1) {
+    F2 b;
+    b.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
+    b.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
+    a = f2_add(a, b);
+  }
+  return a;
 }
-
-// Sum of doubles over the block; `red` must hold 32 doubles.
-__device__ __forceinline__ double block_sum_d(double v, double* red) {
+// Sum over the block; `red` must hold 64 floats.  All threads get the result.
+__device__ __forceinline__ F2 f2_block_sum(F2 v, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  v = warp_sum_d(v);
+  v = f2_warp_sum(v);
   __syncthreads();
-  if (lane == 0) red[warp] = v;
+  if (lane == 0) { red[2 * warp] = v.hi; red[2 * warp + 1] = v.lo; }
   __syncthreads();
-  double t = (lane < nw) ? red[lane] : 0.0;
-  return warp_sum_d(t);
+  F2 t;
+  t.hi = lane < nw ? red[2 * lane] : 0.f;
+  t.lo = lane < nw ? red[2 * lane + 1] : 0.f;
+  return f2_warp_sum(t);
+}
+__device__ __forceinline__ F2 f2_from_double(double d) {
+  F2 r;
+  r.hi = (float)d;
+  r.lo = (float)(d - (double)r.hi);
+  return r;
 }
 
-// RMSNorm scale 1/sqrt(mean + eps) from a sum of squares, in double.
-__device__ __forceinline__ double rms_scale(double sumsq, int n, float eps) {
-  return 1.0 / sqrt(sumsq / (double)n + (double)eps);
+// RMSNorm scale 1/sqrt(sumsq/n + eps) as a float pair: rsqrtf, then one Newton
+// step evaluated with error-free products (relative error ~1e-13).
+__device__ __forceinline__ F2 rms_scale2(F2 ss, int n, float eps) {
+  const float fn = (float)n;
+  F2 m;
+  m.hi = ss.hi / fn;
+  m.lo = (fmaf(-m.hi, fn, ss.hi) + ss.lo) / fn;  // residual of the division
+  {
+    float s, e;
+    two_sum(m.hi, eps, s, e);
+    e += m.lo;
+    m.hi = s + e;
+    m.lo = e - (m.hi - s);
+  }
+  const float y = rsqrtf(m.hi);
+  const float t = y * y, te = fmaf(y, y, -t);           // y^2 = t + te exactly
+  const float u = m.hi * t, ue = fmaf(m.hi, t, -u);    // m.hi * t = u + ue exactly
+  // 1 - m y^2, with u within a few ulps of 1 so 1 - u is exact
+  const float r = ((1.0f - u) - ue) - (m.hi * te + m.lo * t);
+  F2 out;
+  const float c = 0.5f * y * r;
+  out.hi = y + c;
+  out.lo = c - (out.hi - y);
+  return out;
 }
 
-// Qwen3 RMSNorm output element with its two roundings: R(R(h * rs) * g).
-// h * rs is formed in double and rounded once; R(.) * g is exact in fp32
-// for bf16 operands and rounded once.
+// R(h * rs) to the model dtype from the float pair rs: the fp32 product p
+// with its exact residual decides, only when p lands exactly on a rounding
+// tie of the model dtype, which way the exact product lies.
+template <typename Dt> __device__ __forceinline__ float mul_round(float h, F2 rs);
+template <> __device__ __forceinline__ float mul_round<float>(float h, F2 rs) { return fmaf(h, rs.hi, h * rs.lo); }
+template <> __device__ __forceinline__ float mul_round<__nv_bfloat16>(float h, F2 rs) {
+  const float p = h * rs.hi;
+  const uint32_t b = __float_as_uint(p);
+  if ((b & 0xffffu) != 0x8000u) return rd<__nv_bfloat16>(p);
+  const float res = fmaf(h, rs.hi, -p) + h * rs.lo;  // exact product - p (to fp32 accuracy)
+  if (res == 0.f) return rd<__nv_bfloat16>(p);
+  // p is halfway between two bf16 values: the residual's sign picks the side
+  const uint32_t lo = b & 0xffff0000u;  // toward zero
+  const float down = __uint_as_float(lo), up = __uint_as_float(lo + 0x10000u);  // up = away from zero
+  return ((res > 0.f) == (p > 0.f)) ? up : down;
+}
+// Qwen3 RMSNorm element with its two roundings: R(R(h * rs) * g).
 template <typename Dt>
-__device__ __forceinline__ float rms_apply(float h, double rs, float g) {
-  return rd<Dt>(rd_d<Dt>((double)h * rs) * g);
+__device__ __forceinline__ float rms_apply2(float h, F2 rs, float g) {
+  return rd<Dt>(mul_round<Dt>(h, rs) * g);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }

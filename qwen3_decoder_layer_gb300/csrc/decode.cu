@@ -69,9 +69,14 @@ template <typename Dt> struct G2W<Dt, W_U8> {
 // Stage the T input rows as fp32 in shared memory (16-byte vector loads),
 // applying the prologue.
 template <typename Dt>
-__device__ void g2_stage_x(const Gemv2Args& a, float* xs, double* red) {
+__device__ void g2_stage_x(const Gemv2Args& a, float* xs, float* red) {
   constexpr int V = Vec16<Dt>::N;
   const int K = a.K;
+  __shared__ F2 s_rs[4];
+  if (a.prologue == PRO_SUMSQ) {  // one thread turns each row's double sum into the scale
+    if (threadIdx.x < a.T) s_rs[threadIdx.x] = rms_scale2(f2_from_double(a.sumsq_in[threadIdx.x]), K, a.eps);
+    __syncthreads();
+  }
   for (int t = 0; t < a.T; ++t) {
     float* xt = xs + (size_t)t * K;
     if (a.prologue == PRO_X) {
@@ -83,7 +88,7 @@ __device__ void g2_stage_x(const Gemv2Args& a, float* xs, double* red) {
         for (int e = 0; e < V; ++e) xt[k + e] = v[e];
       }
     } else if (a.prologue == PRO_SUMSQ) {
-      const double rs = rms_scale(a.sumsq_in[t], K, a.eps);
+      const F2 rs = s_rs[t];
       const Dt* h = static_cast<const Dt*>(a.h) + (size_t)t * K;
       const Dt* g = static_cast<const Dt*>(a.gain);
       for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
@@ -91,13 +96,13 @@ __device__ void g2_stage_x(const Gemv2Args& a, float* xs, double* red) {
         Vec16<Dt>::unpack(ld16(h + k), hv);
         Vec16<Dt>::unpack(ld16(g + k), gv);
 #pragma unroll
-        for (int e = 0; e < V; ++e) xt[k + e] = rms_apply<Dt>(hv[e], rs, gv[e]);
+        for (int e = 0; e < V; ++e) xt[k + e] = rms_apply2<Dt>(hv[e], rs, gv[e]);
       }
     } else {  // PRO_FULL
       const Dt* x = static_cast<const Dt*>(a.x) + (size_t)t * K;
       const Dt* pe = a.pend ? static_cast<const Dt*>(a.pend) + (size_t)t * K : nullptr;
       Dt* ho = blockIdx.x == 0 ? static_cast<Dt*>(a.h) + (size_t)t * K : nullptr;
-      double ss = 0.0;
+      F2 ss = {0.f, 0.f};
       for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
         float v[V];
         Vec16<Dt>::unpack(ld16(x + k), v);
@@ -111,17 +116,17 @@ __device__ void g2_stage_x(const Gemv2Args& a, float* xs, double* red) {
 #pragma unroll
         for (int e = 0; e < V; ++e) {
           xt[k + e] = v[e];
-          ss = fma((double)v[e], (double)v[e], ss);
+          f2_add_sq(ss, v[e]);
         }
       }
-      ss = block_sum_d(ss, red);
-      const double rs = rms_scale(ss, K, a.eps);
+      ss = f2_block_sum(ss, red);
+      const F2 rs = rms_scale2(ss, K, a.eps);
       const Dt* g = static_cast<const Dt*>(a.gain);
       for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
         float gv[V];
         Vec16<Dt>::unpack(ld16(g + k), gv);
 #pragma unroll
-        for (int e = 0; e < V; ++e) xt[k + e] = rms_apply<Dt>(xt[k + e], rs, gv[e]);
+        for (int e = 0; e < V; ++e) xt[k + e] = rms_apply2<Dt>(xt[k + e], rs, gv[e]);
       }
     }
   }
@@ -154,8 +159,8 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
   float* xs = reinterpret_cast<float*>(g2_smem);
   uint8_t* ring = g2_smem + L.x_bytes + (size_t)warp * S * L.unit_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(g2_smem + L.x_bytes + L.ring_bytes) + warp * S;
-  double* red = reinterpret_cast<double*>(g2_smem + L.x_bytes + L.ring_bytes + (size_t)nwarps * S * 8);
-  __shared__ double red_norm[32];
+  float* red = reinterpret_cast<float*>(g2_smem + L.x_bytes + L.ring_bytes + (size_t)nwarps * S * 8);
+  __shared__ float red_norm[64];
 
   const int gw = blockIdx.x * nwarps + warp, nw = gridDim.x * nwarps;
   const char* wb = static_cast<const char*>(a.w);
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
   __syncthreads();
 
   const int nvec = a.K / W::EPV;
-  double ssq = 0.0;  // lane t: squares of updated rows of x-row t (residual epilogue)
+  F2 ssq = {0.f, 0.f};  // lane t: squares of updated elements of row t (residual epilogue)
   bool ok = true;
   int k = 0;
   for (;; ++k) {
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
         Dt* p = static_cast<Dt*>(a.out) + o;
         const float hn = rd<Dt>(to_f(*p) + rd<Dt>(v));
         *p = from_f<Dt>(hn);
-        ssq = fma((double)hn, (double)hn, ssq);
+        f2_add_sq(ssq, hn);
       } else {  // SwiGLU: act = R(silu(R(g))) in fp32, out = R(act * R(u))
         const float g = rd<Dt>(v), up = rd<Dt>(v2);
         static_cast<Dt*>(a.out)[o] = from_f<Dt>(rd<Dt>(silu_f(g)) * up);
@@ -281,12 +286,12 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
       if (gw + j * nw < a.N) mbar_wait(&bars[j % S], (uint32_t)((j / S) & 1), a.err, 1);
   }
   if (EPI == EPI_RESIDUAL) {
-    if (lane < NT) red[warp * 4 + lane] = ssq;
+    if (lane < NT) { red[(warp * 4 + lane) * 2] = ssq.hi; red[(warp * 4 + lane) * 2 + 1] = ssq.lo; }
     __syncthreads();
     if (threadIdx.x < NT) {
-      double s = 0.0;
-      for (int w = 0; w < nwarps; ++w) s += red[w * 4 + threadIdx.x];
-      atomicAdd(a.sumsq_out + threadIdx.x, s);
+      F2 s = {0.f, 0.f};
+      for (int w = 0; w < nwarps; ++w) s = f2_add(s, F2{red[(w * 4 + threadIdx.x) * 2], red[(w * 4 + threadIdx.x) * 2 + 1]});
+      atomicAdd(a.sumsq_out + threadIdx.x, (double)s.hi + (double)s.lo);
     }
   }
 }
@@ -335,7 +340,10 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
-  const double rs = rms_scale(a.sumsq[t], a.hidden, a.eps);
+  __shared__ F2 s_rs;
+  if (threadIdx.x == 0) s_rs = rms_scale2(f2_from_double(a.sumsq[t]), a.hidden, a.eps);
+  __syncthreads();
+  const F2 rs = s_rs;
   const Dt* h = static_cast<const Dt*>(a.h) + (size_t)t * a.hidden;
   const Dt* g = static_cast<const Dt*>(a.gain);
   Dt* out = static_cast<Dt*>(a.out) + (size_t)t * a.hidden;
@@ -344,7 +352,7 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
     Vec16<Dt>::unpack(ld16(h + k), hv);
     Vec16<Dt>::unpack(ld16(g + k), gv);
 #pragma unroll
-    for (int e = 0; e < V; ++e) o[e] = rms_apply<Dt>(hv[e], rs, gv[e]);
+    for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hv[e], rs, gv[e]);
     *reinterpret_cast<uint4*>(out + k) = Vec16<Dt>::pack(o);
   }
 }

@@ -4,13 +4,12 @@
 // @mlx-bun/inference qwen3-moe.ts Qwen3UnsortedExperts for the gathered
 // expert projections).
 //
-// At T <= 4 rows the linears are bound by reading the weights once from HBM,
-// so each warp streams whole weight rows with 16-byte non-allocating loads
-// while the (normalised) input rows sit in shared memory as fp32.  Before
-// waiting on the producer kernel, every block asks L2 to prefetch its weight
-// rows, so with programmatic dependent launch the weight stream overlaps the
-// tail of the previous kernel.  Optional prologues fuse the residual add and
-// RMSNorm; epilogues fuse rounding, the residual add (o_proj) and SiLU * up.
+// Used for the MoE router logits and the gathered (unsorted) expert
+// projections of few rows: each warp streams whole weight rows with 16-byte
+// non-allocating loads while the input rows sit in shared memory as fp32.
+// Before waiting on the producer kernel, every block asks L2 to prefetch its
+// weight rows (shared-weight mode).  Epilogues fuse rounding, fp32 output,
+// the residual add and SiLU * up.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -47,39 +46,26 @@ template <typename Dt> struct WTraits<Dt, W_U8> {
   }
 };
 
-// Stage the input rows as fp32 in shared memory, applying the prologue.
+// Stage the input rows as fp32 in shared memory (16-byte vector loads).
 template <typename Dt>
-__device__ void stage_x(const GemvArgs& a, float* xs, double* red) {
+__device__ void stage_x(const GemvArgs& a, float* xs) {
+  constexpr int V = Vec16<Dt>::N;
   const int K = a.K;
   for (int t = 0; t < a.x_rows; ++t) {
     float* xt = xs + (size_t)t * K;
-    if (a.prologue == 0) {
-      const Dt* x = static_cast<const Dt*>(a.x) + (size_t)t * K;
-      for (int k = threadIdx.x; k < K; k += blockDim.x) xt[k] = to_f(x[k]);
-      continue;
+    const Dt* x = static_cast<const Dt*>(a.x) + (size_t)t * K;
+    for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
+      float v[V];
+      Vec16<Dt>::unpack(ld16(x + k), v);
+#pragma unroll
+      for (int e = 0; e < V; ++e) xt[k + e] = v[e];
     }
-    const Dt* hi = static_cast<const Dt*>(a.h_in) + (size_t)t * K;
-    const Dt* pe = (a.prologue == 2 && a.pend) ? static_cast<const Dt*>(a.pend) + (size_t)t * K : nullptr;
-    Dt* ho = (a.prologue == 2 && blockIdx.x == 0) ? static_cast<Dt*>(a.h_out) + (size_t)t * K : nullptr;
-    double ss = 0.0;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-      float h = to_f(hi[k]);
-      if (pe) h = rd<Dt>(h + to_f(pe[k]));
-      if (ho) ho[k] = from_f<Dt>(h);
-      xt[k] = h;
-      ss = fma((double)h, (double)h, ss);
-    }
-    ss = block_sum_d(ss, red);
-    const double rs = rms_scale(ss, K, a.eps);
-    const Dt* g = static_cast<const Dt*>(a.gain);
-    for (int k = threadIdx.x; k < K; k += blockDim.x) xt[k] = rms_apply<Dt>(xt[k], rs, to_f(g[k]));
   }
 }
 
 template <typename Dt, int WF, int NT, int EPI>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
   extern __shared__ float xs[];
-  __shared__ double red[32];
   using W = WTraits<Dt, WF>;
   constexpr bool PAIR = (EPI == EPI_SWIGLU);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -98,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
   }
   pdl_wait();
   pdl_launch();
-  stage_x<Dt>(a, xs, red);
+  stage_x<Dt>(a, xs);
   __syncthreads();
 
   const int nvec = a.K / W::EPV;

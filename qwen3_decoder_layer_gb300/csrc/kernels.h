@@ -65,15 +65,7 @@ struct GemvArgs {
   long long w_stride;
   int slot_div;
   int x_rows;          // rows of x staged in shared memory
-  // input: prologue 0: x given (dt [x_rows, K]); 1: x = RMSNorm(h_in); 2: h_out = R(h_in + pend)
-  // (h_in alone when pend is NULL), x = RMSNorm(h_out); block 0 writes h_out, which must not alias h_in.
-  int prologue;
-  const void* x;
-  const void* h_in;
-  const void* pend;
-  void* h_out;
-  const void* gain;
-  float eps;
+  const void* x;       // dt [x_rows, K]
   int epilogue;        // Epi
   void* out;
   int ldo;

@@ -104,7 +104,7 @@ __global__ void moe_scatter_kernel(MoeScatterArgs a) {
 
 template <typename Dt>
 __global__ void moe_combine_kernel(MoeCombineArgs a) {
-  __shared__ double red[32];
+  __shared__ float red[64];
   pdl_wait();
   pdl_launch();
   const int t = blockIdx.x;
@@ -112,7 +112,7 @@ __global__ void moe_combine_kernel(MoeCombineArgs a) {
   const float* w = a.w + (size_t)t * a.k;
   Dt* out = a.out ? static_cast<Dt*>(a.out) + (size_t)t * a.hidden : nullptr;
   Dt* h = a.h ? static_cast<Dt*>(a.h) + (size_t)t * a.hidden : nullptr;
-  double ss = 0.0;
+  F2 ss = {0.f, 0.f};
   for (int n = threadIdx.x; n < a.hidden; n += blockDim.x) {
     float acc = 0.f;
     for (int i = 0; i < a.k; ++i) acc = fmaf(w[i], to_f(z[(size_t)i * a.hidden + n]), acc);
@@ -120,14 +120,14 @@ __global__ void moe_combine_kernel(MoeCombineArgs a) {
     if (h) {
       const float hn = rd<Dt>(to_f(h[n]) + pend);
       h[n] = from_f<Dt>(hn);
-      ss = fma((double)hn, (double)hn, ss);
+      f2_add_sq(ss, hn);
     } else {
       out[n] = from_f<Dt>(pend);
     }
   }
   if (h) {
-    ss = block_sum_d(ss, red);
-    if (threadIdx.x == 0) a.sumsq_out[t] = ss;
+    ss = f2_block_sum(ss, red);
+    if (threadIdx.x == 0) a.sumsq_out[t] = (double)ss.hi + (double)ss.lo;
   }
 }
 

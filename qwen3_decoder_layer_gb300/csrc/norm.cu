@@ -9,7 +9,7 @@ namespace q3 {
 // Backbone's "one rounding" add and Qwen3's "two roundings" RMSNorm.
 template <typename Dt>
 __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
-  __shared__ double red[32];
+  __shared__ float red[64];
   pdl_wait();
   pdl_launch();
   const int row = blockIdx.x;
@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
   const Dt* pe = a.pend ? static_cast<const Dt*>(a.pend) + (size_t)row * a.hidden : nullptr;
   Dt* ho = static_cast<Dt*>(a.h_out) + (size_t)row * a.hidden;
   constexpr int V = Vec16<Dt>::N;
-  double ss = 0.0;
+  F2 ss = {0.f, 0.f};
   for (int i = threadIdx.x * V; i < a.hidden; i += blockDim.x * V) {
     float h[V];
     Vec16<Dt>::unpack(ld16(hi + i), h);
@@ -29,11 +29,11 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
     }
     if (pe || ho != hi) *reinterpret_cast<uint4*>(ho + i) = Vec16<Dt>::pack(h);
 #pragma unroll
-    for (int e = 0; e < V; ++e) ss = fma((double)h[e], (double)h[e], ss);
+    for (int e = 0; e < V; ++e) f2_add_sq(ss, h[e]);
   }
-  ss = block_sum_d(ss, red);
+  ss = f2_block_sum(ss, red);
   if (!a.y) return;
-  const double rs = rms_scale(ss, a.hidden, a.eps);
+  const F2 rs = rms_scale2(ss, a.hidden, a.eps);
   const Dt* g = static_cast<const Dt*>(a.gain);
   Dt* y = static_cast<Dt*>(a.y) + (size_t)row * a.hidden;
   for (int i = threadIdx.x * V; i < a.hidden; i += blockDim.x * V) {
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
     Vec16<Dt>::unpack(ld16(ho + i), h);  // own writes of this thread: visible
     Vec16<Dt>::unpack(ld16(g + i), gg);
 #pragma unroll
-    for (int e = 0; e < V; ++e) o[e] = rms_apply<Dt>(h[e], rs, gg[e]);
+    for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(h[e], rs, gg[e]);
     *reinterpret_cast<uint4*>(y + i) = Vec16<Dt>::pack(o);
   }
 }
@@ -78,15 +78,16 @@ __global__ void __launch_bounds__(256) qk_rope_cache_kernel(QkRopeArgs a) {
   }
   const bool is_q = hh < a.H;
   const Dt* gain = static_cast<const Dt*>(is_q ? a.q_gain : a.k_gain) + lane * EPL;
-  double ss = 0.0;
+  F2 ss = {0.f, 0.f};
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) ss = fma((double)x[e], (double)x[e], ss);
-  ss = warp_sum_d(ss);
-  const double rs = rms_scale(ss, D, a.eps);
+  for (int e = 0; e < EPL; ++e) f2_add_sq(ss, x[e]);
+  ss = f2_warp_sum(ss);
+  const F2 rs = rms_scale2(ss, D, a.eps);
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) x[e] = rms_apply<Dt>(x[e], rs, to_f(gain[e]));
+  for (int e = 0; e < EPL; ++e) x[e] = rms_apply2<Dt>(x[e], rs, to_f(gain[e]));
   // RoPE: o1 = y1*c - y2*s (first half), o2 = y2*c + y1*s (second half), one
-  // rounding.  The products are formed and differenced in double.
+  // rounding.  bf16: both products are exact in fp32 and fmaf rounds their
+  // difference once; fp32: formed and differenced in double.
   const float* cs = a.cos_t + (size_t)pos * D + lane * EPL;
   const float* sn = a.sin_t + (size_t)pos * D + lane * EPL;
   const bool first = lane < 16;
@@ -94,8 +95,13 @@ __global__ void __launch_bounds__(256) qk_rope_cache_kernel(QkRopeArgs a) {
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
     const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
-    const double xc = (double)x[e] * (double)cs[e], ps = (double)partner * (double)sn[e];
-    o[e] = rd_d<Dt>(first ? xc - ps : xc + ps);
+    if (sizeof(Dt) == 2) {
+      const float ps = partner * sn[e];  // exact: 8-bit x 8-bit significands
+      o[e] = rd<Dt>(first ? fmaf(x[e], cs[e], -ps) : fmaf(x[e], cs[e], ps));
+    } else {
+      const double xc = (double)x[e] * (double)cs[e], ps = (double)partner * (double)sn[e];
+      o[e] = rd_d<Dt>(first ? xc - ps : xc + ps);
+    }
   }
   Dt* dst;
   if (is_q) {

@@ -667,7 +667,7 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
   // router logits, fp32, not rounded
   if (T <= 4) {
     GemvArgs g{};
-    g.T = T; g.K = hid; g.N = E; g.w = W.router; g.x_rows = T; g.prologue = 0; g.x = y;
+    g.T = T; g.K = hid; g.N = E; g.w = W.router; g.x_rows = T; g.x = y;
     g.epilogue = EPI_STORE_F32; g.out = B.logits; g.ldo = E;
     e = launch(L, "gemv_router", [&] { return launch_gemv(L.ctx, dt, W_DT, g); });
   } else {
@@ -688,13 +688,13 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
   if (unsorted) {
     GemvArgs g{};
     g.T = slots; g.K = hid; g.N = mI; g.w = W.exp_gate_up; g.slot_expert = idx;
-    g.w_stride = (long long)2 * mI * hid; g.slot_div = k; g.x_rows = T; g.prologue = 0; g.x = y;
+    g.w_stride = (long long)2 * mI * hid; g.slot_div = k; g.x_rows = T; g.x = y;
     g.epilogue = EPI_SWIGLU; g.out = B.mexp; g.ldo = mI;
     e = launch(L, "gemv_expert_gate_up", [&] { return launch_gemv(L.ctx, dt, W_DT, g); });
     if (e != cudaSuccess) return e;
     GemvArgs d{};
     d.T = slots; d.K = mI; d.N = hid; d.w = W.exp_down; d.slot_expert = idx; d.w_stride = (long long)hid * mI;
-    d.slot_div = 1; d.x_rows = slots; d.prologue = 0; d.x = B.mexp; d.epilogue = EPI_STORE; d.out = B.zexp;
+    d.slot_div = 1; d.x_rows = slots; d.x = B.mexp; d.epilogue = EPI_STORE; d.out = B.zexp;
     d.ldo = hid;
     e = launch(L, "gemv_expert_down", [&] { return launch_gemv(L.ctx, dt, W_DT, d); });
     if (e != cudaSuccess) return e;
