@@ -216,8 +216,10 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
       const int nk = min(CK, ik.key0 + ik.nkeys - key0);
       Dt* Kt = reinterpret_cast<Dt*>(tiles(s));
       Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE);
-      const bool landed = mbar_wait(&full[s], (uint32_t)((g / AD_STAGES) & 1), a.err, 2);
-      if (!landed) s_fail = 1;
+      // one thread waits for the sub-chunk; the others park on the named barrier
+      if (tid == 0 && !mbar_wait(&full[s], (uint32_t)((g / AD_STAGES) & 1), a.err, 2)) s_fail = 1;
+      csync();
+      const bool landed = !s_fail;
       // keys appended by this call that fall in the sub-chunk: computed here (warp per key)
       const int n0 = max(key0, qb.seg_pos0), n1 = min(key0 + nk, qb.seg_pos0 + qb.seg_n);
       for (int u = n0 + warp; u < n1 && landed; u += AD_CWARPS) {

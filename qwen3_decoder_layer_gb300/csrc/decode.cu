@@ -199,7 +199,11 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
     const int u = gw + k * nw;
     if (u >= a.N) break;
     const int s = k % S;
-    if (!mbar_wait(&bars[s], (uint32_t)((k / S) & 1), a.err, 1)) { ok = false; break; }
+    // lane 0 waits for the row; the other lanes wait at the warp barrier
+    int landed = 1;
+    if (lane == 0) landed = mbar_wait(&bars[s], (uint32_t)((k / S) & 1), a.err, 1);
+    __syncwarp();  // orders lane 0's acquire of the copy before the other lanes' reads
+    if (!__shfl_sync(0xffffffffu, landed, 0)) { ok = false; break; }
     const uint8_t* slot = ring + (size_t)s * L.unit_bytes;
     float acc[NT][U], acc2[NT][U];  // independent chains, one per unrolled vector
 #pragma unroll

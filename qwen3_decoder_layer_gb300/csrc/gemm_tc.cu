@@ -157,7 +157,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (ok) mma_commit(accum);
     }
   } else {  // epilogue: warp q reads TMEM lanes 32q .. 32q + 31 = tile rows
-    ok = __all_sync(0xffffffffu, mbar_wait(accum, 0, a.err, 5));
+    int okl = 1;  // lane 0 waits for the accumulator; the other lanes wait at the warp barrier
+    if (lane == 0) okl = mbar_wait(accum, 0, a.err, 5);
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
     tc_fence_after();
     const int row = m0 + warp * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
