@@ -10,18 +10,20 @@
 // a persistent grid walks the item list.
 //
 // Warp-specialised block: one producer warp streams the sub-chunks of the
-// block's items, in order, into a 3-stage shared-memory ring with TMA bulk
-// copies (full / empty mbarriers).  It reads only cached positions, which no
-// kernel in flight writes, so it starts at launch without waiting for the qkv
-// projection.  Sixteen consumer warps normalise and rotate the queries, keep
-// an online softmax (running max m, sum l, output o) over an item's
-// sub-chunks -- P.V split over 512/D key groups, merged once per item -- and
-// compute the keys appended in this call from the qkv row, writing them over
-// their slots once the sub-chunk has landed (the item owning the row also
-// stores them to the cache).  Each item stores its partial (m, l, o); the last
-// item of a (query block, kv head) -- found with an atomic counter, no
-// waiting -- merges them: M = max m_c, out = sum_c e^(m_c - M) o_c /
-// sum_c e^(m_c - M) l_c, rounded once to the model dtype.
+// block's items, in order, into a shared-memory ring with TMA bulk copies
+// (full / empty mbarriers).  It reads only cached positions, which no kernel
+// in flight writes, so it starts at launch without waiting for the qkv
+// projection.  Sixteen consumer warps normalise and rotate the NQ query
+// vectors of the item (NQ, a template parameter, bounds rows x G), keep an
+// online softmax (running max m, sum l, output o) over the item's
+// sub-chunks -- P.V split into 512/D contiguous key ranges, merged once per
+// item -- and compute the keys appended in this call from the qkv row,
+// writing them over their slots once the sub-chunk has landed (the item
+// owning the row also stores them to the cache).  Each item stores its
+// partial (m, l, o); the last item of a (query block, kv head) -- found with
+// an atomic counter, no waiting -- merges them: M = max m_c,
+// out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c, rounded once to the
+// model dtype.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -34,7 +36,7 @@ namespace {
 constexpr int AD_CWARPS = 16;                    // consumer warps
 constexpr int AD_CTHREADS = AD_CWARPS * 32;      // 512
 constexpr int AD_THREADS = AD_CTHREADS + 32;     // + producer warp
-constexpr int AD_NQ = 16;
+constexpr int AD_NQ_MAX = 16;
 constexpr int AD_STAGES = 3;
 constexpr int AD_SUBS = 4;  // sub-chunks per item
 
@@ -42,21 +44,27 @@ template <typename Dt> struct ADT {
   static constexpr int CK = sizeof(Dt) == 2 ? 64 : 32;  // 16 KB per K or V sub-chunk at head_dim 128
 };
 
-template <typename Dt, int D> struct ADLayout {
-  static constexpr int KG = AD_CTHREADS / D;  // key groups in P.V
-  static constexpr size_t TILE = (size_t)ADT<Dt>::CK * D * sizeof(Dt);
+template <typename Dt, int D, int NQ> struct ADLayout {
+  static constexpr int CK = ADT<Dt>::CK;
+  static constexpr int KG = AD_CTHREADS / D;  // P.V key ranges
+  static constexpr int KPG = CK / KG;         // keys per range
+  static constexpr size_t TILE = (size_t)CK * D * sizeof(Dt);
   static constexpr size_t STAGE = 2 * TILE;
-  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                          // [NQ][D] fp32 queries
-  static constexpr size_t OFF_SC = OFF_QS + (size_t)AD_NQ * D * 4;             // [NQ][CK] scores / p
-  static constexpr size_t OFF_RUN = OFF_SC + (size_t)AD_NQ * ADT<Dt>::CK * 4;  // [NQ][4] m, l, alpha
-  static constexpr size_t OFF_RED = OFF_RUN + (size_t)AD_NQ * 4 * 4;           // [KG][NQ][D] fp32 (32 KB)
-  static constexpr size_t RED_FLOATS = (size_t)KG * AD_NQ * D;
+  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                    // [NQ][D] fp32 queries
+  static constexpr size_t OFF_SC = OFF_QS + (size_t)NQ * D * 4;          // [NQ][CK] scores / p
+  static constexpr size_t OFF_RUN = OFF_SC + (size_t)NQ * CK * 4;        // [NQ][4] m, l, alpha
+  static constexpr size_t OFF_GAIN = OFF_RUN + (size_t)NQ * 4 * 4;       // q gain, k gain [2][D]
+  static constexpr size_t OFF_RED = OFF_GAIN + (size_t)2 * D * 4;        // [KG][NQ][D] fp32
+  static constexpr size_t RED_FLOATS = (size_t)KG * NQ * D;
   static constexpr size_t OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr size_t TOTAL = OFF_BAR + 2 * AD_STAGES * 8 + 16;
 };
 
 // Named barrier over the consumer warps only.
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(AD_CTHREADS) : "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // Per-head RMSNorm + RoPE of one raw q or k head (warp-wide: lane holds
 // elements lane*DPL .. +DPL) at position pos, rounded to the model dtype.
@@ -64,19 +72,23 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(A
 // are exact in fp32 and fmaf rounds their difference once; for fp32 they are
 // formed in double.
 template <typename Dt, int D>
-__device__ __forceinline__ void norm_rope_head(float* x, const Dt* gain, const float* cos_t, const float* sin_t,
+__device__ __forceinline__ void norm_rope_head(float* x, const float* gain, const float* cos_t, const float* sin_t,
                                                int pos, float eps) {
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
+  float cs[DPL], sn[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) {
+    cs[e] = cos_t[(size_t)pos * D + lane * DPL + e];
+    sn[e] = sin_t[(size_t)pos * D + lane * DPL + e];
+  }
   F2 ss = {0.f, 0.f};
 #pragma unroll
   for (int e = 0; e < DPL; ++e) f2_add_sq(ss, x[e]);
   ss = f2_warp_sum(ss);
   const F2 rs = rms_scale2(ss, D, eps);
 #pragma unroll
-  for (int e = 0; e < DPL; ++e) x[e] = rms_apply2<Dt>(x[e], rs, to_f(gain[lane * DPL + e]));
-  const float* cs = cos_t + (size_t)pos * D + lane * DPL;
-  const float* sn = sin_t + (size_t)pos * D + lane * DPL;
+  for (int e = 0; e < DPL; ++e) x[e] = rms_apply2<Dt>(x[e], rs, gain[lane * DPL + e]);
   const bool first = lane < 16;
   float o[DPL];
 #pragma unroll
@@ -86,15 +98,15 @@ __device__ __forceinline__ void norm_rope_head(float* x, const Dt* gain, const f
       const float ps = partner * sn[e];  // exact: 8-bit x 8-bit significands
       o[e] = rd<Dt>(first ? fmaf(x[e], cs[e], -ps) : fmaf(x[e], cs[e], ps));
     } else {
-      const double xc = (double)x[e] * (double)cs[e], ps = (double)partner * (double)sn[e];
-      o[e] = rd_d<Dt>(first ? xc - ps : xc + ps);
+      const double xc = (double)x[e] * (double)cs[e], pd = (double)partner * (double)sn[e];
+      o[e] = rd_d<Dt>(first ? xc - pd : xc + pd);
     }
   }
 #pragma unroll
   for (int e = 0; e < DPL; ++e) x[e] = o[e];
 }
 
-// Keys of item `it`: [key0, key0 + nkeys) in nsub sub-chunks.
+// Keys of an item: [key0, key0 + nkeys) in nsub sub-chunks.
 struct ItemKeys {
   int key0, nkeys, nsub;
 };
@@ -108,12 +120,13 @@ __device__ __forceinline__ ItemKeys item_keys(const AttnItem& item, const AttnQB
   return r;
 }
 
-template <typename Dt, int D>
+template <typename Dt, int D, int NQ>
 __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs a) {
   extern __shared__ __align__(128) uint8_t ad_smem[];
-  using LY = ADLayout<Dt, D>;
-  constexpr int CK = ADT<Dt>::CK;
+  using LY = ADLayout<Dt, D, NQ>;
+  constexpr int CK = LY::CK;
   constexpr int KG = LY::KG;
+  constexpr int KPG = LY::KPG;
   constexpr int EPV = 16 / sizeof(Dt);  // elements per 16-byte vector
   constexpr int LPK = D / EPV;          // lanes per key in the score loop
   constexpr int KPW = 32 / LPK;         // keys per warp step
@@ -121,6 +134,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   float* qs = reinterpret_cast<float*>(ad_smem + LY::OFF_QS);
   float* sc = reinterpret_cast<float*>(ad_smem + LY::OFF_SC);
   float* run = reinterpret_cast<float*>(ad_smem + LY::OFF_RUN);  // [i*4]: m, l, alpha
+  float* gq = reinterpret_cast<float*>(ad_smem + LY::OFF_GAIN);
+  float* gk = gq + D;
   float* red = reinterpret_cast<float*>(ad_smem + LY::OFF_RED);
   uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
   uint64_t* empty = full + AD_STAGES;
@@ -145,13 +160,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   if (warp == AD_CWARPS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // L2 prefetch of this block's share of the next kernel's operand
-      if (a.pf && a.pf_bytes) {
-        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
-        const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
-        for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
-          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
-      }
       const Dt* kc = static_cast<const Dt*>(a.kc);
       const Dt* vc = static_cast<const Dt*>(a.vc);
       int g = 0;
@@ -174,42 +182,59 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
         }
       }
+      // L2 prefetch of this block's share of the next kernel's operand
+      if (a.pf && a.pf_bytes) {
+        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+        const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
+        for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
+          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
+      }
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  // gains do not depend on the previous kernel
+  for (int d = tid; d < D; d += AD_CTHREADS) {
+    gq[d] = to_f(static_cast<const Dt*>(a.q_gain)[d]);
+    gk[d] = to_f(static_cast<const Dt*>(a.k_gain)[d]);
+  }
   pdl_wait();
   pdl_launch();
+  csync();
   const Dt* qkv = static_cast<const Dt*>(a.qkv);
-  const int kg = tid / D, dcol = tid % D;  // P.V key group and head element of this thread
+  const int kg = tid / D, dcol = tid % D;  // P.V key range and head element of this thread
   int g = 0;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const AttnItem item = a.items[it];
     const AttnQBlock qb = a.qblocks[item.qb];
     const ItemKeys ik = item_keys<Dt>(item, qb);
-    const int nq = qb.nrows * G;
+    const int nq = qb.nrows * G;  // <= NQ
 
     // queries: RMSNorm + RoPE of this block's q heads of kv group j (warp per query)
-    for (int i = warp; i < nq; i += AD_CWARPS) {
-      const int row = qb.row0 + i / G, hh = j * G + i % G;
+    for (int i = warp; i < NQ; i += AD_CWARPS) {
       float x[DPL];
-      const Dt* src = qkv + (size_t)row * qkv_ld + (size_t)hh * D + lane * DPL;
+      if (i < nq) {
+        const int row = qb.row0 + i / G, hh = j * G + i % G;
+        const Dt* src = qkv + (size_t)row * qkv_ld + (size_t)hh * D + lane * DPL;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) x[e] = to_f(src[e]);
-      norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.q_gain), a.cos_t, a.sin_t, qb.pos0 + i / G, a.eps);
+        for (int e = 0; e < DPL; ++e) x[e] = to_f(src[e]);
+        norm_rope_head<Dt, D>(x, gq, a.cos_t, a.sin_t, qb.pos0 + i / G, a.eps);
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) x[e] = 0.f;
+      }
 #pragma unroll
       for (int e = 0; e < DPL; ++e) qs[i * D + lane * DPL + e] = x[e];
+      if (lane == 0) {
+        run[i * 4] = -CUDART_INF_F;
+        run[i * 4 + 1] = 0.f;
+      }
     }
-    if (tid < nq) {
-      run[tid * 4] = -CUDART_INF_F;
-      run[tid * 4 + 1] = 0.f;
-    }
-    float o[AD_NQ];
+    float o[NQ];
 #pragma unroll
-    for (int i = 0; i < AD_NQ; ++i) o[i] = 0.f;
+    for (int i = 0; i < NQ; ++i) o[i] = 0.f;
 
-    bool failed = false;
     for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
       const int s = g % AD_STAGES;
       const int key0 = ik.key0 + sub * CK;
@@ -217,37 +242,40 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
       Dt* Kt = reinterpret_cast<Dt*>(tiles(s));
       Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE);
       // one thread waits for the sub-chunk; the others park on the named barrier
+      // (this barrier also ends the previous sub-chunk's P.V)
       if (tid == 0 && !mbar_wait(&full[s], (uint32_t)((g / AD_STAGES) & 1), a.err, 2)) s_fail = 1;
       csync();
-      const bool landed = !s_fail;
+      if (s_fail) break;
+      if (tid == 0 && sub > 0) mbar_arrive(&empty[(g - 1) % AD_STAGES]);  // previous stage is free
       // keys appended by this call that fall in the sub-chunk: computed here (warp per key)
       const int n0 = max(key0, qb.seg_pos0), n1 = min(key0 + nk, qb.seg_pos0 + qb.seg_n);
-      for (int u = n0 + warp; u < n1 && landed; u += AD_CWARPS) {
-        const int row = qb.seg_row0 + (u - qb.seg_pos0);
-        float x[DPL], v[DPL];
-        const Dt* ksrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + j) * D + lane * DPL;
-        const Dt* vsrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + a.KV + j) * D + lane * DPL;
+      if (n0 < n1) {
+        for (int u = n0 + warp; u < n1; u += AD_CWARPS) {
+          const int row = qb.seg_row0 + (u - qb.seg_pos0);
+          float x[DPL], v[DPL];
+          const Dt* ksrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + j) * D + lane * DPL;
+          const Dt* vsrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + a.KV + j) * D + lane * DPL;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) { x[e] = to_f(ksrc[e]); v[e] = to_f(vsrc[e]); }
-        norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.k_gain), a.cos_t, a.sin_t, u, a.eps);
-        const bool owner = row >= qb.row0 && row < qb.row0 + qb.nrows;
-        const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
+          for (int e = 0; e < DPL; ++e) { x[e] = to_f(ksrc[e]); v[e] = to_f(vsrc[e]); }
+          norm_rope_head<Dt, D>(x, gk, a.cos_t, a.sin_t, u, a.eps);
+          const bool owner = row >= qb.row0 && row < qb.row0 + qb.nrows;
+          const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) {
-          Kt[(u - key0) * D + lane * DPL + e] = from_f<Dt>(x[e]);
-          Vt[(u - key0) * D + lane * DPL + e] = from_f<Dt>(v[e]);
-          if (owner) {
-            static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
-            static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
+          for (int e = 0; e < DPL; ++e) {
+            Kt[(u - key0) * D + lane * DPL + e] = from_f<Dt>(x[e]);
+            Vt[(u - key0) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+            if (owner) {
+              static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
+              static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
+            }
           }
         }
+        csync();
       }
-      csync();
-      if (s_fail) { failed = true; break; }
       // scores: LPK lanes per key, KPW keys per warp step
       {
         const int sub_l = lane % LPK;
-        for (int ub = warp * KPW; ub < nk; ub += AD_CWARPS * KPW) {
+        for (int ub = warp * KPW; ub < CK; ub += AD_CWARPS * KPW) {
           const int u = ub + lane / LPK;
           float kv[EPV];
           if (u < nk) {
@@ -256,32 +284,36 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
 #pragma unroll
             for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
           }
-          for (int i = 0; i < nq; ++i) {
-            const float* qp = qs + i * D + sub_l * EPV;
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            const float4* qp = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV);
             float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPV; e += 2) {
-              d0 = fmaf(qp[e], kv[e], d0);
-              d1 = fmaf(qp[e + 1], kv[e + 1], d1);
+            for (int e = 0; e < EPV / 4; ++e) {
+              const float4 q4 = qp[e];
+              d0 = fmaf(q4.x, kv[4 * e], d0);
+              d1 = fmaf(q4.y, kv[4 * e + 1], d1);
+              d0 = fmaf(q4.z, kv[4 * e + 2], d0);
+              d1 = fmaf(q4.w, kv[4 * e + 3], d1);
             }
             float d = d0 + d1;
 #pragma unroll
             for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            if (sub_l == 0 && u < nk)
-              sc[i * CK + u] = (key0 + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
+            if (sub_l == 0)
+              sc[i * CK + u] = (u < nk && i < nq && key0 + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
           }
         }
       }
       csync();
-      // online softmax update per query (warp per query)
-      for (int i = warp; i < nq; i += AD_CWARPS) {
+      // online softmax update per query (warp per query); p = 0 past nk
+      for (int i = warp; i < NQ; i += AD_CWARPS) {
         float mc = -CUDART_INF_F;
-        for (int u = lane; u < nk; u += 32) mc = fmaxf(mc, sc[i * CK + u]);
+        for (int u = lane; u < CK; u += 32) mc = fmaxf(mc, sc[i * CK + u]);
         mc = warp_max(mc);
         const float m_old = run[i * 4];
         const float m_new = fmaxf(m_old, mc);
         float l = 0.f;
-        for (int u = lane; u < nk; u += 32) {
+        for (int u = lane; u < CK; u += 32) {
           const float x = sc[i * CK + u];
           const float p = (x == -CUDART_INF_F) ? 0.f : expf(x - m_new);
           sc[i * CK + u] = p;
@@ -296,33 +328,44 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
         }
       }
       csync();
-      // P.V: thread (key group kg, element dcol) over keys kg, kg + KG, ...
+      // P.V: thread (range kg, element dcol) over keys kg*KPG .. +KPG
 #pragma unroll
-      for (int i = 0; i < AD_NQ; ++i)
-        if (i < nq) o[i] *= run[i * 4 + 2];
-      for (int u = kg; u < nk; u += KG) {
-        const float v = to_f(Vt[(size_t)u * D + dcol]);
+      for (int i = 0; i < NQ; ++i) o[i] *= run[i * 4 + 2];
+      const int kb = kg * KPG;
+      if (kb + KPG <= nk) {
 #pragma unroll
-        for (int i = 0; i < AD_NQ; ++i)
-          if (i < nq) o[i] = fmaf(sc[i * CK + u], v, o[i]);
+        for (int u4 = 0; u4 < KPG; u4 += 4) {
+          const int u = kb + u4;
+          const float v0 = to_f(Vt[(size_t)u * D + dcol]), v1 = to_f(Vt[(size_t)(u + 1) * D + dcol]);
+          const float v2 = to_f(Vt[(size_t)(u + 2) * D + dcol]), v3 = to_f(Vt[(size_t)(u + 3) * D + dcol]);
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            const float4 p = *reinterpret_cast<const float4*>(sc + i * CK + u);
+            o[i] = fmaf(p.x, v0, fmaf(p.y, v1, fmaf(p.z, v2, fmaf(p.w, v3, o[i]))));
+          }
+        }
+      } else {
+        for (int u = kb; u < min(kb + KPG, nk); ++u) {
+          const float v = to_f(Vt[(size_t)u * D + dcol]);
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) o[i] = fmaf(sc[i * CK + u], v, o[i]);
+        }
       }
-      // release the stage to the producer
-      csync();
-      if (tid == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
     }
-    if (failed) break;
+    csync();  // the item's last P.V is done: its stage is free
+    if (s_fail) break;
+    if (tid == 0) mbar_arrive(&empty[(g - 1) % AD_STAGES]);
 
-    // merge the key groups, then store this item's partial
+    // merge the key ranges, then store this item's partial
 #pragma unroll
-    for (int i = 0; i < AD_NQ; ++i)
-      if (i < nq) red[(kg * AD_NQ + i) * D + dcol] = o[i];
+    for (int i = 0; i < NQ; ++i) red[(kg * NQ + i) * D + dcol] = o[i];
     csync();
     const size_t part0 = ((size_t)(qb.part_base + item.chunk) * a.KV + j) * a.nq_max;
     for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
       const int i = idx / D, d = idx % D;
       float v = 0.f;
 #pragma unroll
-      for (int q = 0; q < KG; ++q) v += red[(q * AD_NQ + i) * D + d];
+      for (int q = 0; q < KG; ++q) v += red[(q * NQ + i) * D + d];
       a.part_o[(part0 + i) * D + d] = v;
     }
     if (tid < nq) {
@@ -394,27 +437,37 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   }
 }
 
-template <typename Dt, int D>
+template <typename Dt, int D, int NQ>
 cudaError_t ad_launch(const LaunchCtx& c, const AttnDecArgs& a) {
-  auto kern = attn_decode_kernel<Dt, D>;
+  auto kern = attn_decode_kernel<Dt, D, NQ>;
+  using LY = ADLayout<Dt, D, NQ>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)ADLayout<Dt, D>::TOTAL);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::TOTAL);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_k(kern, dim3(a.grid_x, a.KV), dim3(AD_THREADS), ADLayout<Dt, D>::TOTAL, c, a);
+  return launch_k(kern, dim3(a.grid_x, a.KV), dim3(AD_THREADS), LY::TOTAL, c, a);
+}
+
+template <typename Dt, int D>
+cudaError_t ad_nq(const LaunchCtx& c, const AttnDecArgs& a) {
+  if (a.nq <= 1) return ad_launch<Dt, D, 1>(c, a);
+  if (a.nq <= 2) return ad_launch<Dt, D, 2>(c, a);
+  if (a.nq <= 4) return ad_launch<Dt, D, 4>(c, a);
+  if (a.nq <= 8) return ad_launch<Dt, D, 8>(c, a);
+  return ad_launch<Dt, D, 16>(c, a);
 }
 
 }  // namespace
 
 int attn_decode2_chunk(int dt) { return (dt == DT_BF16 ? ADT<bf16>::CK : ADT<float>::CK) * AD_SUBS; }
-int attn_decode2_nq_max() { return AD_NQ; }
+int attn_decode2_nq_max() { return AD_NQ_MAX; }
 
 cudaError_t launch_attn_decode2(const LaunchCtx& c, int dt, const AttnDecArgs& a) {
-  if (a.D == 128) return dt == DT_BF16 ? ad_launch<bf16, 128>(c, a) : ad_launch<float, 128>(c, a);
-  if (a.D == 64) return dt == DT_BF16 ? ad_launch<bf16, 64>(c, a) : ad_launch<float, 64>(c, a);
+  if (a.nq < 1 || a.nq > AD_NQ_MAX) return cudaErrorInvalidValue;
+  if (a.D == 128) return dt == DT_BF16 ? ad_nq<bf16, 128>(c, a) : ad_nq<float, 128>(c, a);
+  if (a.D == 64) return dt == DT_BF16 ? ad_nq<bf16, 64>(c, a) : ad_nq<float, 64>(c, a);
   return cudaErrorInvalidValue;
 }
 

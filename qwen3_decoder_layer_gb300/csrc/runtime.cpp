@@ -491,6 +491,7 @@ struct Plan {
   int rows_per_block = 1;
   int chunk = 64;
   int nq_max = 16;
+  int max_nq = 1;              // largest rows x G of any query block
   int n_qblocks = 0, n_items = 0, n_parts = 0;
   std::vector<int32_t> blob;   // row_seq[T] row_pos[T] n_items qblocks items
   size_t off_rowseq = 0, off_rowpos = 0, off_nitems = 0, off_qb = 0, off_items = 0;
@@ -537,6 +538,7 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
   for (auto& g : segs) {
     for (int r = 0; r < g.n; r += P.rows_per_block) {
       const int nr = std::min(P.rows_per_block, g.n - r);
+      P.max_nq = std::max(P.max_nq, nr * G);
       const int last_pos = g.pos0 + r + nr - 1;
       const int nch = (last_pos + 1 + P.chunk - 1) / P.chunk;
       qb.insert(qb.end(), {g.seq, g.row0 + r, nr, g.pos0 + r, nch, parts, g.row0, g.pos0, g.n, 0});
@@ -753,6 +755,7 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
     a.items = items; a.n_items = n_items; a.part_o = B.part_o; a.part_ml = B.part_ml; a.nq_max = P.nq_max;
     a.counters = B.counters; a.out = B.attn; a.err = B.err;
     a.grid_x = std::max(1, (h->num_sms + KV - 1) / KV);
+    a.nq = P.max_nq;
     a.pf = pf; a.pf_bytes = pf_bytes;
     return launch(L, "attn_decode", [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
@@ -956,7 +959,7 @@ extern "C" qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T,
   const bool graph = h->use_graphs && !h->profile && P.gemv;
   cudaError_t e;
   if (graph) {
-    const GraphKey key{T, P.attn, x, out};
+    const GraphKey key{T, P.attn * 64 + P.max_nq, x, out};
     if (h->graphs.size() > 32) {  // callers cycling through buffers: start over
       for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
       h->graphs.clear();
