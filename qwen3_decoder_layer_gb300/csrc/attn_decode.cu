@@ -9,19 +9,19 @@
 // sub-chunks of CK keys.  A work item is one (query block, chunk, kv head);
 // a persistent grid walks the item list.
 //
-// Warp-specialised block: one producer warp streams the sub-chunks of the
-// block's items, in order, into a shared-memory ring with TMA bulk copies
-// (full / empty mbarriers).  It reads only cached positions, which no kernel
-// in flight writes, so it starts at launch without waiting for the qkv
-// projection.  Sixteen consumer warps normalise and rotate the NQ query
-// vectors of the item (NQ, a template parameter, bounds rows x G), keep an
-// online softmax (running max m, sum l, output o) over the item's
-// sub-chunks -- P.V split into 512/D contiguous key ranges, merged once per
-// item -- and compute the keys appended in this call from the qkv row,
-// writing them over their slots once the sub-chunk has landed (the item
-// owning the row also stores them to the cache).  Each item stores its
-// partial (m, l, o); the last item of a (query block, kv head) -- found with
-// an atomic counter, no waiting -- merges them: M = max m_c,
+// Warp-specialised block.  One producer warp streams the sub-chunks of the
+// block's items, in order, into a 4-stage shared-memory ring (one item) with
+// TMA bulk copies (full / empty mbarriers).  It reads only cached positions,
+// which no kernel in flight writes, so it starts at launch without waiting
+// for the qkv projection.  Sixteen consumer warps: warps 0..NQ-1 first
+// normalise and rotate the NQ query vectors of the item; then every warp
+// takes its own CK/4 keys of one sub-chunk and runs them end to end -- keys
+// appended in this call computed from the qkv row (and stored to the cache
+// by the item owning the row), scores, a warp-local softmax, P.V -- with no
+// block barrier, producing a warp partial (m, l, o).  A block barrier, one
+// merge of the 16 partials, and the item's partial (m, l, o) goes to global
+// memory.  The last item of a (query block, kv head) -- found with an atomic
+// counter, no waiting -- merges the chunks: M = max m_c,
 // out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c, rounded once to the
 // model dtype.
 #include <math_constants.h>
@@ -36,9 +36,10 @@ namespace {
 constexpr int AD_CWARPS = 16;                    // consumer warps
 constexpr int AD_CTHREADS = AD_CWARPS * 32;      // 512
 constexpr int AD_THREADS = AD_CTHREADS + 32;     // + producer warp
-constexpr int AD_NQ_MAX = 16;
-constexpr int AD_STAGES = 3;
-constexpr int AD_SUBS = 4;  // sub-chunks per item
+constexpr int AD_NQ_MAX = 8;
+constexpr int AD_SUBS = 4;                       // sub-chunks per item
+constexpr int AD_STAGES = AD_SUBS;               // the ring holds one item
+constexpr int AD_WPS = AD_CWARPS / AD_SUBS;      // warps per sub-chunk
 
 template <typename Dt> struct ADT {
   static constexpr int CK = sizeof(Dt) == 2 ? 64 : 32;  // 16 KB per K or V sub-chunk at head_dim 128
@@ -46,17 +47,17 @@ template <typename Dt> struct ADT {
 
 template <typename Dt, int D, int NQ> struct ADLayout {
   static constexpr int CK = ADT<Dt>::CK;
-  static constexpr int KG = AD_CTHREADS / D;  // P.V key ranges
-  static constexpr int KPG = CK / KG;         // keys per range
+  static constexpr int KW = CK / AD_WPS;  // keys per warp
   static constexpr size_t TILE = (size_t)CK * D * sizeof(Dt);
   static constexpr size_t STAGE = 2 * TILE;
-  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                    // [NQ][D] fp32 queries
-  static constexpr size_t OFF_SC = OFF_QS + (size_t)NQ * D * 4;          // [NQ][CK] scores / p
-  static constexpr size_t OFF_RUN = OFF_SC + (size_t)NQ * CK * 4;        // [NQ][4] m, l, alpha
-  static constexpr size_t OFF_GAIN = OFF_RUN + (size_t)NQ * 4 * 4;       // q gain, k gain [2][D]
-  static constexpr size_t OFF_RED = OFF_GAIN + (size_t)2 * D * 4;        // [KG][NQ][D] fp32
-  static constexpr size_t RED_FLOATS = (size_t)KG * NQ * D;
-  static constexpr size_t OFF_BAR = OFF_RED + RED_FLOATS * 4;
+  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                             // [NQ][D] queries
+  static constexpr size_t OFF_PS = OFF_QS + (size_t)NQ * D * 4;                   // [warp][NQ][KW] scores / p
+  static constexpr int WPITCH = D + 4;                                            // o[D], m, l, pad
+  static constexpr size_t OFF_WP = OFF_PS + (size_t)AD_CWARPS * NQ * KW * 4;      // [warp][NQ][WPITCH] partials
+  static constexpr size_t WP_FLOATS = (size_t)AD_CWARPS * NQ * WPITCH;
+  static constexpr int MPITCH = AD_CWARPS + 2;                                    // weights of the warps, M, L
+  static constexpr size_t OFF_MRG = OFF_WP + WP_FLOATS * 4;                       // [NQ][MPITCH] merge scratch
+  static constexpr size_t OFF_BAR = (OFF_MRG + (size_t)NQ * MPITCH * 4 + 15) & ~size_t(15);
   static constexpr size_t TOTAL = OFF_BAR + 2 * AD_STAGES * 8 + 16;
 };
 
@@ -72,15 +73,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // are exact in fp32 and fmaf rounds their difference once; for fp32 they are
 // formed in double.
 template <typename Dt, int D>
-__device__ __forceinline__ void norm_rope_head(float* x, const float* gain, const float* cos_t, const float* sin_t,
+__device__ __forceinline__ void norm_rope_head(float* x, const Dt* gain, const float* cos_t, const float* sin_t,
                                                int pos, float eps) {
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
-  float cs[DPL], sn[DPL];
+  float cs[DPL], sn[DPL], gg[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) {
     cs[e] = cos_t[(size_t)pos * D + lane * DPL + e];
     sn[e] = sin_t[(size_t)pos * D + lane * DPL + e];
+    gg[e] = to_f(gain[lane * DPL + e]);
   }
   F2 ss = {0.f, 0.f};
 #pragma unroll
@@ -88,7 +90,7 @@ __device__ __forceinline__ void norm_rope_head(float* x, const float* gain, cons
   ss = f2_warp_sum(ss);
   const F2 rs = rms_scale2(ss, D, eps);
 #pragma unroll
-  for (int e = 0; e < DPL; ++e) x[e] = rms_apply2<Dt>(x[e], rs, gain[lane * DPL + e]);
+  for (int e = 0; e < DPL; ++e) x[e] = rms_apply2<Dt>(x[e], rs, gg[e]);
   const bool first = lane < 16;
   float o[DPL];
 #pragma unroll
@@ -104,6 +106,39 @@ __device__ __forceinline__ void norm_rope_head(float* x, const float* gain, cons
   }
 #pragma unroll
   for (int e = 0; e < DPL; ++e) x[e] = o[e];
+}
+
+// DPL consecutive elements at p (one aligned vector load) as floats.
+template <typename Dt, int DPL>
+__device__ __forceinline__ void load_lane_vec(const Dt* p, float* v) {
+  constexpr int BYTES = DPL * (int)sizeof(Dt);
+  static_assert(BYTES == 4 || BYTES == 8 || BYTES == 16, "lane vector");
+  constexpr int NW = BYTES / 4;
+  uint32_t w[NW];
+  if (NW == 4) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    w[0] = r.x; w[NW > 1 ? 1 : 0] = r.y; w[NW > 2 ? 2 : 0] = r.z; w[NW > 3 ? 3 : 0] = r.w;
+  } else if (NW == 2) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    w[0] = r.x; w[NW > 1 ? 1 : 0] = r.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+#pragma unroll
+  for (int e = 0; e < DPL; ++e)
+    v[e] = sizeof(Dt) == 2 ? __uint_as_float((e & 1) ? (w[e / 2] & 0xffff0000u) : (w[e / 2] << 16))
+                           : __uint_as_float(w[e]);
+}
+template <int DPL>
+__device__ __forceinline__ void store_lane_vec(float* p, const float* v) {
+  if (DPL == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[DPL > 1 ? 1 : 0], v[DPL > 2 ? 2 : 0], v[DPL > 3 ? 3 : 0]);
+  } else if (DPL == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[DPL > 1 ? 1 : 0]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) p[e] = v[e];
+  }
 }
 
 // Keys of an item: [key0, key0 + nkeys) in nsub sub-chunks.
@@ -125,18 +160,17 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   extern __shared__ __align__(128) uint8_t ad_smem[];
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
-  constexpr int KG = LY::KG;
-  constexpr int KPG = LY::KPG;
+  constexpr int KW = LY::KW;            // keys per warp
   constexpr int EPV = 16 / sizeof(Dt);  // elements per 16-byte vector
   constexpr int LPK = D / EPV;          // lanes per key in the score loop
-  constexpr int KPW = 32 / LPK;         // keys per warp step
+  constexpr int KPS = 32 / LPK;         // keys per score step
   constexpr int DPL = D / 32;           // head elements per lane
+  constexpr int WP = LY::WPITCH;
+  constexpr int MP = LY::MPITCH;
   float* qs = reinterpret_cast<float*>(ad_smem + LY::OFF_QS);
-  float* sc = reinterpret_cast<float*>(ad_smem + LY::OFF_SC);
-  float* run = reinterpret_cast<float*>(ad_smem + LY::OFF_RUN);  // [i*4]: m, l, alpha
-  float* gq = reinterpret_cast<float*>(ad_smem + LY::OFF_GAIN);
-  float* gk = gq + D;
-  float* red = reinterpret_cast<float*>(ad_smem + LY::OFF_RED);
+  float* ps_all = reinterpret_cast<float*>(ad_smem + LY::OFF_PS);
+  float* wp = reinterpret_cast<float*>(ad_smem + LY::OFF_WP);
+  float* mrg = reinterpret_cast<float*>(ad_smem + LY::OFF_MRG);
   uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
   uint64_t* empty = full + AD_STAGES;
   __shared__ int s_flag, s_fail;
@@ -150,7 +184,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   if (tid == 0) {
     for (int s = 0; s < AD_STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], AD_WPS);
     }
     mbar_fence_init();
     s_fail = 0;
@@ -194,17 +228,13 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   }
 
   // -------------------------------------------------------------- consumers
-  // gains do not depend on the previous kernel
-  for (int d = tid; d < D; d += AD_CTHREADS) {
-    gq[d] = to_f(static_cast<const Dt*>(a.q_gain)[d]);
-    gk[d] = to_f(static_cast<const Dt*>(a.k_gain)[d]);
-  }
   pdl_wait();
   pdl_launch();
-  csync();
   const Dt* qkv = static_cast<const Dt*>(a.qkv);
-  const int kg = tid / D, dcol = tid % D;  // P.V key range and head element of this thread
-  int g = 0;
+  float* ps = ps_all + (size_t)warp * NQ * KW;  // this warp's scores / probabilities
+  const int wsub = warp / AD_WPS;               // sub-chunk of this warp
+  const int wk0 = (warp % AD_WPS) * KW;         // its first key inside the sub-chunk
+  int g = 0;                                    // block-wide sub-chunk sequence position
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const AttnItem item = a.items[it];
     const AttnQBlock qb = a.qblocks[item.qb];
@@ -212,71 +242,73 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
     const int nq = qb.nrows * G;  // <= NQ
 
     // queries: RMSNorm + RoPE of this block's q heads of kv group j (warp per query)
-    for (int i = warp; i < NQ; i += AD_CWARPS) {
+    if (warp < NQ) {
+      const int i = warp;
       float x[DPL];
       if (i < nq) {
         const int row = qb.row0 + i / G, hh = j * G + i % G;
         const Dt* src = qkv + (size_t)row * qkv_ld + (size_t)hh * D + lane * DPL;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) x[e] = to_f(src[e]);
-        norm_rope_head<Dt, D>(x, gq, a.cos_t, a.sin_t, qb.pos0 + i / G, a.eps);
+        norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.q_gain), a.cos_t, a.sin_t, qb.pos0 + i / G, a.eps);
       } else {
 #pragma unroll
         for (int e = 0; e < DPL; ++e) x[e] = 0.f;
       }
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) qs[i * D + lane * DPL + e] = x[e];
-      if (lane == 0) {
-        run[i * 4] = -CUDART_INF_F;
-        run[i * 4 + 1] = 0.f;
-      }
+      store_lane_vec<DPL>(qs + i * D + lane * DPL, x);
     }
-    float o[NQ];
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) o[i] = 0.f;
+    csync();
 
-    for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
-      const int s = g % AD_STAGES;
-      const int key0 = ik.key0 + sub * CK;
-      const int nk = min(CK, ik.key0 + ik.nkeys - key0);
-      Dt* Kt = reinterpret_cast<Dt*>(tiles(s));
-      Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE);
-      // one thread waits for the sub-chunk; the others park on the named barrier
-      // (this barrier also ends the previous sub-chunk's P.V)
-      if (tid == 0 && !mbar_wait(&full[s], (uint32_t)((g / AD_STAGES) & 1), a.err, 2)) s_fail = 1;
-      csync();
-      if (s_fail) break;
-      if (tid == 0 && sub > 0) mbar_arrive(&empty[(g - 1) % AD_STAGES]);  // previous stage is free
-      // keys appended by this call that fall in the sub-chunk: computed here (warp per key)
-      const int n0 = max(key0, qb.seg_pos0), n1 = min(key0 + nk, qb.seg_pos0 + qb.seg_n);
-      if (n0 < n1) {
-        for (int u = n0 + warp; u < n1; u += AD_CWARPS) {
+    // ---- this warp's keys, end to end
+    float m_w[NQ], l_w[NQ], o_w[NQ][DPL];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      m_w[i] = -CUDART_INF_F;
+      l_w[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
+    }
+    if (wsub < ik.nsub) {
+      const int s = (g + wsub) % AD_STAGES;
+      const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
+      const int nk = min(KW, ik.key0 + ik.nkeys - key0 - wk0);  // this warp's keys (may be <= 0)
+      Dt* Kt = reinterpret_cast<Dt*>(tiles(s)) + (size_t)wk0 * D;
+      Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE) + (size_t)wk0 * D;
+      int landed = 1;
+      if (lane == 0) landed = mbar_wait(&full[s], (uint32_t)(((g + wsub) / AD_STAGES) & 1), a.err, 2);
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, landed, 0)) {
+        s_fail = 1;
+      } else if (nk > 0) {
+        const int kb = key0 + wk0;  // absolute position of this warp's first key
+        // keys appended by this call among this warp's keys
+        const int n0 = max(kb, qb.seg_pos0), n1 = min(kb + nk, qb.seg_pos0 + qb.seg_n);
+        for (int u = n0; u < n1; ++u) {
           const int row = qb.seg_row0 + (u - qb.seg_pos0);
           float x[DPL], v[DPL];
           const Dt* ksrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + j) * D + lane * DPL;
           const Dt* vsrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + a.KV + j) * D + lane * DPL;
 #pragma unroll
           for (int e = 0; e < DPL; ++e) { x[e] = to_f(ksrc[e]); v[e] = to_f(vsrc[e]); }
-          norm_rope_head<Dt, D>(x, gk, a.cos_t, a.sin_t, u, a.eps);
+          norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.k_gain), a.cos_t, a.sin_t, u, a.eps);
           const bool owner = row >= qb.row0 && row < qb.row0 + qb.nrows;
           const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
 #pragma unroll
           for (int e = 0; e < DPL; ++e) {
-            Kt[(u - key0) * D + lane * DPL + e] = from_f<Dt>(x[e]);
-            Vt[(u - key0) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+            Kt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(x[e]);
+            Vt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(v[e]);
             if (owner) {
               static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
               static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
             }
           }
         }
-        csync();
-      }
-      // scores: LPK lanes per key, KPW keys per warp step
-      {
-        const int sub_l = lane % LPK;
-        for (int ub = warp * KPW; ub < CK; ub += AD_CWARPS * KPW) {
-          const int u = ub + lane / LPK;
+        __syncwarp();
+        // scores: LPK lanes per key, KPS keys per step
+        const int sub_l = lane % LPK, kq = lane / LPK;
+#pragma unroll
+        for (int st = 0; st < KW / KPS; ++st) {
+          const int u = st * KPS + kq;
           float kv[EPV];
           if (u < nk) {
             Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
@@ -300,77 +332,72 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
 #pragma unroll
             for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
             if (sub_l == 0)
-              sc[i * CK + u] = (u < nk && i < nq && key0 + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
+              ps[i * KW + u] = (u < nk && i < nq && kb + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
           }
         }
-      }
-      csync();
-      // online softmax update per query (warp per query); p = 0 past nk
-      for (int i = warp; i < NQ; i += AD_CWARPS) {
-        float mc = -CUDART_INF_F;
-        for (int u = lane; u < CK; u += 32) mc = fmaxf(mc, sc[i * CK + u]);
-        mc = warp_max(mc);
-        const float m_old = run[i * 4];
-        const float m_new = fmaxf(m_old, mc);
-        float l = 0.f;
-        for (int u = lane; u < CK; u += 32) {
-          const float x = sc[i * CK + u];
-          const float p = (x == -CUDART_INF_F) ? 0.f : expf(x - m_new);
-          sc[i * CK + u] = p;
-          l += p;
-        }
-        l = warp_sum(l);
-        if (lane == 0) {
-          const float alpha = (m_old == -CUDART_INF_F) ? 0.f : expf(m_old - m_new);
-          run[i * 4] = m_new;
-          run[i * 4 + 1] = run[i * 4 + 1] * alpha + l;
-          run[i * 4 + 2] = alpha;
-        }
-      }
-      csync();
-      // P.V: thread (range kg, element dcol) over keys kg*KPG .. +KPG
+        __syncwarp();
+        // warp-local softmax over the warp's keys (lanes over keys)
 #pragma unroll
-      for (int i = 0; i < NQ; ++i) o[i] *= run[i * 4 + 2];
-      const int kb = kg * KPG;
-      if (kb + KPG <= nk) {
-#pragma unroll
-        for (int u4 = 0; u4 < KPG; u4 += 4) {
-          const int u = kb + u4;
-          const float v0 = to_f(Vt[(size_t)u * D + dcol]), v1 = to_f(Vt[(size_t)(u + 1) * D + dcol]);
-          const float v2 = to_f(Vt[(size_t)(u + 2) * D + dcol]), v3 = to_f(Vt[(size_t)(u + 3) * D + dcol]);
+        for (int i = 0; i < NQ; ++i) {
+          const float sv = lane < KW ? ps[i * KW + lane] : -CUDART_INF_F;
+          const float m = warp_max(sv);
+          const float p = (sv == -CUDART_INF_F) ? 0.f : expf(sv - m);
+          const float l = warp_sum(p);
+          if (lane < KW) ps[i * KW + lane] = p;
+          m_w[i] = m;
+          l_w[i] = l;
+        }
+        __syncwarp();
+        // P.V: lane holds head elements lane*DPL .. +DPL
+#pragma unroll 4
+        for (int u = 0; u < nk; ++u) {
+          float v[DPL];
+          load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
 #pragma unroll
           for (int i = 0; i < NQ; ++i) {
-            const float4 p = *reinterpret_cast<const float4*>(sc + i * CK + u);
-            o[i] = fmaf(p.x, v0, fmaf(p.y, v1, fmaf(p.z, v2, fmaf(p.w, v3, o[i]))));
+            const float p = ps[i * KW + u];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o_w[i][e] = fmaf(p, v[e], o_w[i][e]);
           }
         }
-      } else {
-        for (int u = kb; u < min(kb + KPG, nk); ++u) {
-          const float v = to_f(Vt[(size_t)u * D + dcol]);
+      }
+      // this warp is done with its part of the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // warp partial -> shared memory
+    float* mine = wp + (size_t)warp * NQ * WP;
 #pragma unroll
-          for (int i = 0; i < NQ; ++i) o[i] = fmaf(sc[i * CK + u], v, o[i]);
-        }
+    for (int i = 0; i < NQ; ++i) {
+      store_lane_vec<DPL>(mine + i * WP + lane * DPL, o_w[i]);
+      if (lane == 0) { mine[i * WP + D] = m_w[i]; mine[i * WP + D + 1] = l_w[i]; }
+    }
+    g += ik.nsub;
+    csync();
+    if (s_fail) break;
+
+    // merge the 16 warp partials into this item's partial; warp i: lanes over
+    // the warp partials of query i
+    const size_t part0 = ((size_t)(qb.part_base + item.chunk) * a.KV + j) * a.nq_max;
+    if (warp < nq) {
+      const int i = warp;
+      const float m = lane < AD_CWARPS ? wp[((size_t)lane * NQ + i) * WP + D] : -CUDART_INF_F;
+      const float M = warp_max(m);
+      const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+      const float L = warp_sum(lane < AD_CWARPS ? f * wp[((size_t)lane * NQ + i) * WP + D + 1] : 0.f);
+      if (lane < AD_CWARPS) mrg[i * MP + lane] = f;
+      if (lane == 0) {
+        a.part_ml[(part0 + i) * 2] = M;
+        a.part_ml[(part0 + i) * 2 + 1] = L;
       }
     }
-    csync();  // the item's last P.V is done: its stage is free
-    if (s_fail) break;
-    if (tid == 0) mbar_arrive(&empty[(g - 1) % AD_STAGES]);
-
-    // merge the key ranges, then store this item's partial
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) red[(kg * NQ + i) * D + dcol] = o[i];
     csync();
-    const size_t part0 = ((size_t)(qb.part_base + item.chunk) * a.KV + j) * a.nq_max;
     for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
       const int i = idx / D, d = idx % D;
       float v = 0.f;
 #pragma unroll
-      for (int q = 0; q < KG; ++q) v += red[(q * NQ + i) * D + d];
+      for (int w = 0; w < AD_CWARPS; ++w) v = fmaf(wp[((size_t)w * NQ + i) * WP + d], mrg[i * MP + w], v);
       a.part_o[(part0 + i) * D + d] = v;
-    }
-    if (tid < nq) {
-      a.part_ml[(part0 + tid) * 2] = run[tid * 4];
-      a.part_ml[(part0 + tid) * 2 + 1] = run[tid * 4 + 1];
     }
     __threadfence();
     csync();
@@ -383,8 +410,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
       __threadfence();
       const int nc = qb.n_chunks;
       const size_t pbase = (size_t)qb.part_base * a.KV + j;  // partial of chunk c: (pbase + c * KV) * nq_max
-      const bool staged = (size_t)nc * nq <= LY::RED_FLOATS;
-      float* fs = red;  // [c][i]: chunk maxima, then their weights e^(m_c - M_i)
+      const bool staged = (size_t)nc * nq <= LY::WP_FLOATS;
+      float* fs = wp;  // [c][i]: chunk maxima, then their weights e^(m_c - M_i)
       if (staged) {
         for (int idx = tid; idx < nc * nq; idx += AD_CTHREADS) {
           const int c = idx / nq, i = idx % nq;
@@ -408,13 +435,13 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           if (staged) fs[c * nq + i] = f;
         }
         Lsum = warp_sum(Lsum);
-        if (lane == 0) { run[i * 4] = M; run[i * 4 + 1] = Lsum; }
+        if (lane == 0) { mrg[i * MP + AD_CWARPS] = M; mrg[i * MP + AD_CWARPS + 1] = Lsum; }
       }
       csync();
       // out[i][d] = sum_c f[c][i] o_c[i][d] / L_i, one thread per output element
       for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
         const int i = idx / D, d = idx % D;
-        const float M = run[i * 4];
+        const float M = mrg[i * MP + AD_CWARPS];
         float v = 0.f;
 #pragma unroll 4
         for (int c = 0; c < nc; ++c) {
@@ -429,7 +456,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           v = fmaf(__ldcg(a.part_o + p * D + d), f, v);
         }
         const int row = qb.row0 + i / G, head = j * G + i % G;
-        static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / run[i * 4 + 1]);
+        static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / mrg[i * MP + AD_CWARPS + 1]);
       }
       if (tid == 0) a.counters[(size_t)item.qb * a.KV + j] = 0;
     }
@@ -455,8 +482,7 @@ cudaError_t ad_nq(const LaunchCtx& c, const AttnDecArgs& a) {
   if (a.nq <= 1) return ad_launch<Dt, D, 1>(c, a);
   if (a.nq <= 2) return ad_launch<Dt, D, 2>(c, a);
   if (a.nq <= 4) return ad_launch<Dt, D, 4>(c, a);
-  if (a.nq <= 8) return ad_launch<Dt, D, 8>(c, a);
-  return ad_launch<Dt, D, 16>(c, a);
+  return ad_launch<Dt, D, 8>(c, a);
 }
 
 }  // namespace

@@ -10,8 +10,9 @@
 //    issued before griddepcontrol.wait, i.e. while the previous kernel is
 //    still running under programmatic dependent launch, and one thread also
 //    asks L2 for the next linear's weights.  The normalised input rows sit in
-//    shared memory as fp32; each row's dot product runs as independent
-//    accumulator chains (one per unrolled 16-byte vector).  The residual
+//    shared memory in the model dtype, so each lane reads its x vector as
+//    contiguous 16-byte loads free of bank conflicts; each row's dot product
+//    runs as independent accumulator chains (one per unrolled 16-byte vector).  The residual
 //    epilogue (o_proj, down_proj) updates h in place and accumulates the sum
 //    of squares of the new rows, so the following RMSNorm needs no reduction.
 //  * norm_apply: the final RMSNorm from the precomputed sum of squares.
@@ -33,9 +34,10 @@ struct G2Layout {
   size_t x_bytes, row_bytes, unit_bytes, ring_bytes, total;
 };
 
-__host__ __device__ inline G2Layout g2_layout(int wbytes, int T, int K, bool pair, int stages, int nwarps) {
+__host__ __device__ inline G2Layout g2_layout(int wbytes, int xbytes, int T, int K, bool pair, int stages,
+                                              int nwarps) {
   G2Layout L;
-  L.x_bytes = align_up((size_t)T * K * 4, 128);
+  L.x_bytes = align_up((size_t)T * K * xbytes, 128);
   L.row_bytes = (size_t)K * wbytes;
   L.unit_bytes = align_up((pair ? 2 : 1) * L.row_bytes, 128);
   L.ring_bytes = (size_t)nwarps * stages * L.unit_bytes;
@@ -66,39 +68,66 @@ template <typename Dt> struct G2W<Dt, W_U8> {
   }
 };
 
-// Stage the T input rows as fp32 in shared memory (16-byte vector loads),
-// applying the prologue.
+// Stage the T input rows in shared memory in the model dtype (16-byte vector
+// loads), applying the prologue.  Every staged value is already a model-dtype
+// value (x, R(x + pend), or the RMSNorm output), so nothing is lost.
 template <typename Dt>
-__device__ void g2_stage_x(const Gemv2Args& a, float* xs, float* red) {
+__device__ void g2_stage_x(const Gemv2Args& a, Dt* xs, float* red) {
   constexpr int V = Vec16<Dt>::N;
+  constexpr int MAXC = 4;  // 16-byte chunks per thread kept in registers
   const int K = a.K;
+  const int nch = a.T * K / V;
   __shared__ F2 s_rs[4];
-  if (a.prologue == PRO_SUMSQ) {  // one thread turns each row's double sum into the scale
+  if (a.prologue == PRO_X) {
+    const Dt* x = static_cast<const Dt*>(a.x);
+    for (int c = threadIdx.x; c < nch; c += blockDim.x)
+      *reinterpret_cast<uint4*>(xs + (size_t)c * V) = ld16(x + (size_t)c * V);
+  } else if (a.prologue == PRO_SUMSQ && nch <= MAXC * (int)blockDim.x) {
+    // h and the gain are fetched while one thread per row turns its double
+    // sum of squares into the scale
+    uint4 hv[MAXC], gv[MAXC];
+    const Dt* h = static_cast<const Dt*>(a.h);
+    const Dt* g = static_cast<const Dt*>(a.gain);
+#pragma unroll
+    for (int q = 0; q < MAXC; ++q) {
+      const int c = threadIdx.x + q * blockDim.x;
+      if (c < nch) {
+        hv[q] = ld16(h + (size_t)c * V);
+        gv[q] = ld16(g + (size_t)((c * V) % K));
+      }
+    }
     if (threadIdx.x < a.T) s_rs[threadIdx.x] = rms_scale2(f2_from_double(a.sumsq_in[threadIdx.x]), K, a.eps);
     __syncthreads();
-  }
-  for (int t = 0; t < a.T; ++t) {
-    float* xt = xs + (size_t)t * K;
-    if (a.prologue == PRO_X) {
-      const Dt* x = static_cast<const Dt*>(a.x) + (size_t)t * K;
-      for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
-        float v[V];
-        Vec16<Dt>::unpack(ld16(x + k), v);
 #pragma unroll
-        for (int e = 0; e < V; ++e) xt[k + e] = v[e];
-      }
-    } else if (a.prologue == PRO_SUMSQ) {
-      const F2 rs = s_rs[t];
-      const Dt* h = static_cast<const Dt*>(a.h) + (size_t)t * K;
-      const Dt* g = static_cast<const Dt*>(a.gain);
-      for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
-        float hv[V], gv[V];
-        Vec16<Dt>::unpack(ld16(h + k), hv);
-        Vec16<Dt>::unpack(ld16(g + k), gv);
+    for (int q = 0; q < MAXC; ++q) {
+      const int c = threadIdx.x + q * blockDim.x;
+      if (c < nch) {
+        const F2 rs = s_rs[c * V / K];
+        float hf[V], gf[V], o[V];
+        Vec16<Dt>::unpack(hv[q], hf);
+        Vec16<Dt>::unpack(gv[q], gf);
 #pragma unroll
-        for (int e = 0; e < V; ++e) xt[k + e] = rms_apply2<Dt>(hv[e], rs, gv[e]);
+        for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hf[e], rs, gf[e]);
+        *reinterpret_cast<uint4*>(xs + (size_t)c * V) = Vec16<Dt>::pack(o);
       }
-    } else {  // PRO_FULL
+    }
+  } else if (a.prologue == PRO_SUMSQ) {
+    if (threadIdx.x < a.T) s_rs[threadIdx.x] = rms_scale2(f2_from_double(a.sumsq_in[threadIdx.x]), K, a.eps);
+    __syncthreads();
+    const Dt* h = static_cast<const Dt*>(a.h);
+    const Dt* g = static_cast<const Dt*>(a.gain);
+    for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+      const F2 rs = s_rs[c * V / K];
+      float hf[V], gf[V], o[V];
+      Vec16<Dt>::unpack(ld16(h + (size_t)c * V), hf);
+      Vec16<Dt>::unpack(ld16(g + (size_t)((c * V) % K)), gf);
+#pragma unroll
+      for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hf[e], rs, gf[e]);
+      *reinterpret_cast<uint4*>(xs + (size_t)c * V) = Vec16<Dt>::pack(o);
+    }
+  } else {  // PRO_FULL
+    for (int t = 0; t < a.T; ++t) {
+      Dt* xt = xs + (size_t)t * K;
       const Dt* x = static_cast<const Dt*>(a.x) + (size_t)t * K;
       const Dt* pe = a.pend ? static_cast<const Dt*>(a.pend) + (size_t)t * K : nullptr;
       Dt* ho = blockIdx.x == 0 ? static_cast<Dt*>(a.h) + (size_t)t * K : nullptr;
@@ -112,21 +141,22 @@ __device__ void g2_stage_x(const Gemv2Args& a, float* xs, float* red) {
 #pragma unroll
           for (int e = 0; e < V; ++e) v[e] = rd<Dt>(v[e] + p[e]);
         }
-        if (ho) *reinterpret_cast<uint4*>(ho + k) = Vec16<Dt>::pack(v);
+        const uint4 pv = Vec16<Dt>::pack(v);
+        if (ho) *reinterpret_cast<uint4*>(ho + k) = pv;
+        *reinterpret_cast<uint4*>(xt + k) = pv;
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          xt[k + e] = v[e];
-          f2_add_sq(ss, v[e]);
-        }
+        for (int e = 0; e < V; ++e) f2_add_sq(ss, v[e]);
       }
       ss = f2_block_sum(ss, red);
       const F2 rs = rms_scale2(ss, K, a.eps);
       const Dt* g = static_cast<const Dt*>(a.gain);
       for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
-        float gv[V];
+        float gv[V], hv[V], o[V];
         Vec16<Dt>::unpack(ld16(g + k), gv);
+        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(xt + k), hv);  // this thread's own stores
 #pragma unroll
-        for (int e = 0; e < V; ++e) xt[k + e] = rms_apply2<Dt>(xt[k + e], rs, gv[e]);
+        for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hv[e], rs, gv[e]);
+        *reinterpret_cast<uint4*>(xt + k) = Vec16<Dt>::pack(o);
       }
     }
   }
@@ -152,11 +182,12 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
   using W = G2W<Dt, WF>;
   constexpr bool PAIR = (EPI == EPI_SWIGLU);
   constexpr int U = (NT * (PAIR ? 2 : 1) * W::EPV > 32) ? 2 : 4;  // 16-byte vectors in flight per lane
+  constexpr int XV = Vec16<Dt>::N;                                 // x elements per 16-byte vector
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int S = a.stages;
-  const G2Layout L = g2_layout(W::BYTES, NT, a.K, PAIR, S, nwarps);
-  float* xs = reinterpret_cast<float*>(g2_smem);
+  const G2Layout L = g2_layout(W::BYTES, sizeof(Dt), NT, a.K, PAIR, S, nwarps);
+  Dt* xs = reinterpret_cast<Dt*>(g2_smem);
   uint8_t* ring = g2_smem + L.x_bytes + (size_t)warp * S * L.unit_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(g2_smem + L.x_bytes + L.ring_bytes) + warp * S;
   float* red = reinterpret_cast<float*>(g2_smem + L.x_bytes + L.ring_bytes + (size_t)nwarps * S * 8);
@@ -225,22 +256,21 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
         const int v = v0 + 32 * i;
         if (v >= nvec) break;
         const int k0 = v * W::EPV;
-        float w0[W::EPV];
+        float w0[W::EPV], w1[W::EPV];
         W::get(q0[i], w0, a, (size_t)u, k0);
+        if (PAIR) W::get(q1[i], w1, a, (size_t)u + a.N, k0);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const float* xp = xs + (size_t)t * a.K + k0;
+          // this lane's x elements k0 .. k0 + EPV: contiguous 16-byte vectors
+          float xv[W::EPV];
 #pragma unroll
-          for (int e = 0; e < W::EPV; ++e) acc[t][i] = fmaf(w0[e], xp[e], acc[t][i]);
-        }
-        if (PAIR) {
-          float w1[W::EPV];
-          W::get(q1[i], w1, a, (size_t)u + a.N, k0);
+          for (int q = 0; q < W::EPV / XV; ++q)
+            Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)t * a.K + k0 + q * XV), xv + q * XV);
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const float* xp = xs + (size_t)t * a.K + k0;
+          for (int e = 0; e < W::EPV; ++e) acc[t][i] = fmaf(w0[e], xv[e], acc[t][i]);
+          if (PAIR) {
 #pragma unroll
-            for (int e = 0; e < W::EPV; ++e) acc2[t][i] = fmaf(w1[e], xp[e], acc2[t][i]);
+            for (int e = 0; e < W::EPV; ++e) acc2[t][i] = fmaf(w1[e], xv[e], acc2[t][i]);
           }
         }
       }
@@ -309,7 +339,8 @@ cudaError_t g2_launch(const LaunchCtx& c, const Gemv2Args& a) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const G2Layout L = g2_layout(WF == W_U8 ? 1 : (int)sizeof(Dt), NT, a.K, EPI == EPI_SWIGLU, a.stages, a.nwarps);
+  const G2Layout L = g2_layout(WF == W_U8 ? 1 : (int)sizeof(Dt), (int)sizeof(Dt), NT, a.K, EPI == EPI_SWIGLU,
+                               a.stages, a.nwarps);
   int grid = (a.N + a.nwarps - 1) / a.nwarps;
   if (grid > c.num_sms) grid = c.num_sms;
   return launch_k(kern, dim3(grid), dim3(a.nwarps * 32), L.total, c, a);
@@ -366,16 +397,17 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
 int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps) {
   (void)group;
   const int wbytes = wfmt == W_U8 ? 1 : (dt == DT_BF16 ? 2 : 4);
+  const int xbytes = dt == DT_BF16 ? 2 : 4;
   for (int nw = G2_MAX_WARPS; nw >= 4; nw /= 2)
     for (int s = 4; s >= (nw == 4 ? 1 : 2); --s) {
-      const G2Layout L = g2_layout(wbytes, T, K, pair, s, nw);
+      const G2Layout L = g2_layout(wbytes, xbytes, T, K, pair, s, nw);
       if (L.total <= G2_SMEM_LIMIT) {
         if (nwarps) *nwarps = nw;
         return s;
       }
     }
   if (nwarps) *nwarps = 4;
-  return g2_layout(wbytes, T, K, pair, 1, 4).total <= G2_SMEM_LIMIT ? 1 : 0;
+  return g2_layout(wbytes, xbytes, T, K, pair, 1, 4).total <= G2_SMEM_LIMIT ? 1 : 0;
 }
 
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a) {

@@ -262,7 +262,7 @@ struct AttnDecArgs {
   int* counters;
   void* out;
   int grid_x;
-  int nq;              // largest query-vector count (rows x G) of any query block, <= 16
+  int nq;              // largest query-vector count (rows x G) of any query block, <= attn_decode2_nq_max()
   int* err;
   const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
   size_t pf_bytes;

@@ -529,7 +529,8 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
   P.gemv = T <= 4;
   int max_rows = 0;
   for (auto& g : segs) max_rows = std::max(max_rows, g.n);
-  P.attn = max_rows * G > attn_decode2_nq_max() ? ATTN_PREFILL : ATTN_DECODE;
+  // the decode kernel takes up to 4 rows per sequence, in query blocks of nq_max / G rows
+  P.attn = (max_rows <= 4 && G <= attn_decode2_nq_max()) ? ATTN_DECODE : ATTN_PREFILL;
   P.nq_max = P.attn == ATTN_PREFILL ? attn_prefill_nq_max() : attn_decode2_nq_max();
   P.chunk = P.attn == ATTN_PREFILL ? attn_prefill_chunk() : attn_decode2_chunk(h->dt);
   P.rows_per_block = P.nq_max / G;
