@@ -163,6 +163,42 @@ QWEN3_API qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T, 
 QWEN3_API qwen3_status qwen3_moe_layer(qwen3_handle* h, int32_t layer, const void* y, int32_t T, void* out,
                              int32_t* topk_idx, float* topk_w, void* stream);
 
+/* qwen3_moe_layer for callers that must not allocate.  The paper has no
+ * counterpart: this entry point exists for the library's users.
+ *
+ * qwen3_moe_layer grows the handle's workspace with cudaMalloc when a call
+ * needs more room than any earlier one.  Some callers cannot allow that: a
+ * serving engine that reserves nearly all of the GPU's memory for its own pool
+ * at start-up (a later cudaMalloc may fail), a host program that runs inside
+ * another framework's allocator and must not take memory behind its back, and
+ * latency-bound loops where cudaFree's implicit device-wide synchronisation
+ * would stall every stream.  This variant computes the same result as
+ * qwen3_moe_layer (same arguments, same kernels) with all of its scratch --
+ * router logits, expert histogram and permutation, expert activations and
+ * per-slot expert outputs -- in one fixed 4 MiB array in device memory that
+ * is part of the library: it calls no cudaMalloc, cudaFree or other
+ * allocating routine.  Every GPU that loads the library holds those 4 MiB
+ * until the process exits.
+ *
+ * Limit: the scratch must fit in 4 MiB; for the 128-expert, top-8,
+ * moe_intermediate 768, hidden 2048 bf16 model that is up to 91 rows.  A
+ * larger T returns QWEN3_E_ARG with the row count that fits in
+ * qwen3_last_error, before any work is enqueued.  QWEN3_E_ARG too when the
+ * handle's device is not the current device; QWEN3_E_UNSUPPORTED while
+ * QWEN3_OPT_PROFILE is on (profiling records events).
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture.
+ *
+ * Sharing: every call on a device, from any handle or thread, uses the same
+ * array, which keeps the previous call's contents; each call clears the part
+ * that must start at zero on its own stream.  Calls whose GPU work can overlap
+ * (different streams without an ordering between them) race on the array and
+ * give wrong results: order them on one stream or with events. */
+QWEN3_API qwen3_status qwen3_moe_layer_static(qwen3_handle* h, int32_t layer, const void* y, int32_t T, void* out,
+                                    int32_t* topk_idx, float* topk_w, void* stream);
+
 /* Device pointers of one (sequence, layer) cache slab: K and V, each dt
  * [n_kv_heads][capacity][head_dim], K post-RoPE.  Owned by the library; valid
  * until qwen3_destroy.  Used to pre-fill a cache, then qwen3_set_length. */

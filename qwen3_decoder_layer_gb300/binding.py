@@ -67,6 +67,7 @@ _SIGS = {
     "qwen3_reset": (_I32, [_P, _I32, _P]),
     "qwen3_forward": (_I32, [_P, _P, _I32, _PI32, _PI32, _P, _P]),
     "qwen3_moe_layer": (_I32, [_P, _I32, _P, _I32, _P, _P, _P, _P]),
+    "qwen3_moe_layer_static": (_I32, [_P, _I32, _P, _I32, _P, _P, _P, _P]),
     "qwen3_cache_view": (_I32, [_P, _I32, _I32, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
     "qwen3_set_length": (_I32, [_P, _I32, _I32]),
     "qwen3_get_length": (_I32, [_P, _I32, _PI32]),
@@ -181,6 +182,13 @@ def qwen3_forward(h, x, seq_ids, positions, out, stream=None) -> None:
 def qwen3_moe_layer(h, layer: int, y, out, topk_idx, topk_w, stream=None) -> None:
     _check(h, lib().qwen3_moe_layer(h, layer, _ptr(y), int(y.shape[0]), _ptr(out), _ptr(topk_idx),
                                     _ptr(topk_w), _stream(stream)))
+
+
+def qwen3_moe_layer_static(h, layer: int, y, out, topk_idx, topk_w, stream=None) -> None:
+    """qwen3_moe_layer with its scratch in the library's fixed device array
+    (no allocation; T bounded by that array's size)."""
+    _check(h, lib().qwen3_moe_layer_static(h, layer, _ptr(y), int(y.shape[0]), _ptr(out), _ptr(topk_idx),
+                                           _ptr(topk_w), _stream(stream)))
 
 
 def qwen3_cache_view(h, seq: int, layer: int):

@@ -1043,3 +1043,97 @@ extern "C" qwen3_status qwen3_device_error(qwen3_handle* h, int32_t* code) {
   }
   return QWEN3_OK;
 }
+
+// ======================================================================
+// MoE block on caller-provided scratch (used by qwen3_moe_layer_static)
+// ======================================================================
+namespace {
+
+// Scratch of the MoE block for T rows, carved in 256-byte-aligned pieces.
+// [0, zeroed) holds the expert histogram and the scatter cursors, which the
+// router and the scatter expect at zero.
+struct MoeScratch {
+  size_t counts, cursor, zeroed, row_off, row_cnt, tile_start, logits, sorted_tok, sorted_src, mexp, zexp, total;
+};
+
+MoeScratch moe_scratch_layout(const qwen3_config& c, size_t esz, size_t T) {
+  MoeScratch s{};
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t o = off;
+    off += (n + 255) / 256 * 256;
+    return o;
+  };
+  const size_t E = (size_t)c.num_experts, slots = T * (size_t)c.top_k;
+  s.counts = take(E * 4);
+  s.cursor = take(E * 4);
+  s.zeroed = off;
+  s.row_off = take(E * 4);
+  s.row_cnt = take(E * 4);
+  s.tile_start = take((E + 1) * 4);
+  s.logits = take(T * E * 4);
+  s.sorted_tok = take(slots * 4);
+  s.sorted_src = take(slots * 4);
+  s.mexp = take(slots * (size_t)c.moe_intermediate * esz);
+  s.zexp = take(slots * (size_t)c.hidden * esz);
+  s.total = off;
+  return s;
+}
+
+}  // namespace
+
+namespace q3 {
+
+int handle_device(const qwen3_handle* h) { return h->device; }
+
+qwen3_status report_error(qwen3_handle* h, qwen3_status s, const char* msg) { return fail(h, s, msg); }
+
+// qwen3_moe_layer with every scratch buffer taken from the device region
+// [scratch, scratch + scratch_bytes) instead of the handle's workspace: the
+// call allocates nothing and leaves the workspace as it is.  The region's
+// zero-initialised part is cleared on `stream` before the kernels.
+qwen3_status moe_layer_on_scratch(qwen3_handle* h, int32_t layer, const void* y, int32_t T, void* out,
+                                  int32_t* topk_idx, float* topk_w, void* stream, void* scratch,
+                                  size_t scratch_bytes) {
+  if (!y || !out || !topk_idx || !topk_w || !scratch) return fail(h, QWEN3_E_ARG, "null pointer argument");
+  if (layer < 0 || layer >= h->cfg.num_layers || !is_moe_layer(h, layer))
+    return fail(h, QWEN3_E_ARG, "layer is not a MoE layer");
+  if (T < 1 || T > (1 << 20)) return fail(h, QWEN3_E_ARG, "row count out of range");
+  if (h->profile) return fail(h, QWEN3_E_UNSUPPORTED, "turn QWEN3_OPT_PROFILE off for the static-scratch MoE layer");
+  const MoeScratch S = moe_scratch_layout(h->cfg, h->esz, (size_t)T);
+  if (S.total > scratch_bytes) {
+    int lo = 0, hi = T;  // largest row count that fits
+    while (lo < hi) {
+      const int mid = lo + (hi - lo + 1) / 2;
+      if (moe_scratch_layout(h->cfg, h->esz, (size_t)mid).total <= scratch_bytes) lo = mid; else hi = mid - 1;
+    }
+    char msg[256];
+    std::snprintf(msg, sizeof msg,
+                  "%d rows need %zu bytes of scratch, more than the %zu-byte static scratch; at most %d rows of "
+                  "this model fit per call",
+                  T, S.total, scratch_bytes, lo);
+    return fail(h, QWEN3_E_ARG, msg);
+  }
+  char* base = static_cast<char*>(scratch);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(base, 0, S.zeroed, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "static scratch clear");
+  Bufs B{};
+  B.counts = reinterpret_cast<int*>(base + S.counts);
+  B.cursor = reinterpret_cast<int*>(base + S.cursor);
+  B.row_off = reinterpret_cast<int*>(base + S.row_off);
+  B.row_cnt = reinterpret_cast<int*>(base + S.row_cnt);
+  B.tile_start = reinterpret_cast<int*>(base + S.tile_start);
+  B.logits = reinterpret_cast<float*>(base + S.logits);
+  B.sorted_tok = reinterpret_cast<int*>(base + S.sorted_tok);
+  B.sorted_src = reinterpret_cast<int*>(base + S.sorted_src);
+  B.mexp = base + S.mexp;
+  B.zexp = base + S.zexp;
+  Launcher L{h, {s, h->pdl, h->num_sms}};
+  e = moe_block(h, L, layer, y, T, out, nullptr, nullptr, topk_idx, topk_w, B);
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  h->last_launches = L.count;
+  return QWEN3_OK;
+}
+
+}  // namespace q3
