@@ -7,6 +7,13 @@ append, attention, o_proj + residual, RMSNorm, fused gate|up + SiLU*up, down;
 then the final RMSNorm).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --workload prefill|moe_decode|moe_prefill|batched_int8
+
+The default run is the decode line above.  --workload measures one of the
+other workloads on one GPU (2048-row prefill against the bf16 tensor-core
+peak; the 4-layer 128-expert MoE stack's decode at context 2048 and its
+1024-row prefill, and 32-sequence int8 decode at contexts uniform in
+[1024, 16384], against the HBM peak) and prints one JSON line for it.
 
 Multi-GPU runs are independent replicas (one stack per GPU, no collective on
 the data path); the value is all ranks' tokens over the slowest rank's time.
@@ -374,18 +381,188 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- other workloads
+WORKLOADS = ("decode", "prefill", "moe_decode", "moe_prefill", "batched_int8")
+
+
+def _linear_params(cfg):
+    H, KV, D, hid, I_ = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.hidden, cfg.intermediate
+    attn = (H + 2 * KV) * D * hid + hid * H * D
+    if cfg.num_experts:
+        return attn, hid * cfg.num_experts, 3 * cfg.moe_intermediate * hid
+    return attn, 0, 3 * I_ * hid
+
+
+def run_workload(args):
+    """The other workloads of the scope table, each with its own roofline:
+    prefill (2048 rows, tensor-core bound), MoE decode / prefill (HBM bound),
+    32-sequence int8 decode (HBM bound, KV dominated).  One JSON line each."""
+    import statistics
+
+    import torch
+    from qwen3_decoder_layer_gb300 import binding as Q
+    from qwen3_decoder_layer_gb300 import build as B
+    from qwen3_decoder_layer_gb300 import inputs as I
+
+    B.build()
+    peaks = _peaks()
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    tc = peaks.get("bf16_tflops_sustained") or 1700.0
+    wl, K, W = args.workload, args.steps, args.warmup
+    cfg = {"prefill": I.DENSE_1P7B_PREFILL, "moe_decode": I.MOE_A3B_4LAYER, "moe_prefill": I.MOE_A3B_4LAYER,
+           "batched_int8": I.DENSE_1P7B_INT8_B32}[wl]
+    weights = I.make_weights(cfg, seed=I.SEEDS[cfg.name], device="cuda")
+    stack = Q.Qwen3Stack(cfg, weights)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4242)
+    attn_p, router_p, mlp_p = _linear_params(cfg)
+    kv_pos_bytes = cfg.num_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2  # K and V, bf16, every layer
+
+    def fill(seq, n):
+        for l in range(cfg.num_layers):
+            kc, vc = Q.cache_tensors(stack.h, cfg, seq, l)
+            kc[:, :n].normal_(generator=gen)
+            vc[:, :n].normal_(generator=gen)
+
+    if wl == "prefill" or wl == "moe_prefill":
+        T = 2048 if wl == "prefill" else 1024
+        x = I.make_rows(cfg, T, seed=99, device="cuda")
+        out = torch.empty_like(x)
+        runs = []
+        for i in range(W + K):
+            Q.qwen3_set_length(stack.h, 0, 0)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            Q.qwen3_forward(stack.h, x, [0] * T, list(range(T)), out)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= W:
+                runs.append(e0.elapsed_time(e1))
+        ms = statistics.median(runs)
+        value = T / (ms * 1e-3)
+        unit, steps_desc = "tok/s", f"median of {K} {T}-row prefills from an empty cache"
+        def run_one():
+            Q.qwen3_set_length(stack.h, 0, 0)
+            Q.qwen3_forward(stack.h, x, [0] * T, list(range(T)), out)
+    else:
+        if wl == "moe_decode":
+            ctx = [2048]
+            n_seq = 1
+        else:
+            n_seq = cfg.max_seqs
+            ctx = I.batch_context_lengths(n_seq, 1024, 16384, seed=3600)
+        assert max(ctx) + W + K <= cfg.capacity, "steps + warmup exceed the cache capacity"
+        for s_, n in enumerate(ctx):
+            fill(s_, n)
+        xs = I.make_rows(cfg, n_seq * (W + K), seed=99, device="cuda").view(W + K, n_seq, cfg.hidden)
+        out = torch.empty(n_seq, cfg.hidden, dtype=xs.dtype, device="cuda")
+        seqs = list(range(n_seq))
+
+        def reset_len():
+            for s_, n in enumerate(ctx):
+                Q.qwen3_set_length(stack.h, s_, n)
+
+        def step(i):
+            Q.qwen3_forward(stack.h, xs[i], seqs, [n + i for n in ctx], out)
+        reset_len()
+        for i in range(W):
+            step(i)
+        reset_len()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(K):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / K
+        value = n_seq / (ms * 1e-3)
+        unit, steps_desc = "tok/s", f"{K} decode steps of {n_seq} row(s)"
+
+        def run_one():
+            reset_len()
+            step(0)
+
+    # clocks under load, then per-kernel times (events around every launch)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    clocks.mark("t0")
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        run_one()
+        torch.cuda.synchronize()
+    clocks.mark("t1")
+    clocks.stop()
+    Q.qwen3_set_option(stack.h, Q.QWEN3_OPT_PROFILE, 1)
+    run_one()
+    Q.qwen3_profile_reset(stack.h)
+    run_one()
+    prof = Q.qwen3_profile_read(stack.h)
+    Q.qwen3_set_option(stack.h, Q.QWEN3_OPT_PROFILE, 0)
+    total = sum(v[1] for v in prof.values())
+    kernels = {k: {"launches": v[0], "total_ms": round(v[1], 4), "share": round(v[1] / total, 4)}
+               for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])}
+    line = {"metric": f"{wl} tok/s", "value": value, "unit": unit, "n_gpus": 1, "steps": K, "warmup": W,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16" if cfg.weight_format != "int8" else
+            "bf16 activations, int8 weights", "data": "synthetic (seeded)", "workload": wl,
+            "config": {"workload": f"{cfg.name}: {steps_desc}", "layers": cfg.num_layers},
+            "kernels": kernels, "clocks": clocks.summary()}
+    if wl == "prefill":
+        T = 2048
+        gemm_flop = 2.0 * (attn_p + mlp_p) * cfg.num_layers * T
+        gemm_ms = sum(v[1] for k, v in prof.items() if k.startswith("gemm_")) / 1.0
+        attn_flop = 4.0 * cfg.n_heads * cfg.head_dim * (T * (T + 1) / 2) * cfg.num_layers
+        line["roofline"] = {"bound": "tensor", "kernel": "gemm_tc (all linears)",
+                            "achieved": gemm_flop / (gemm_ms * 1e-3) / 1e12, "peak": tc, "unit": "TFLOP/s",
+                            "frac": gemm_flop / (gemm_ms * 1e-3) / 1e12 / tc,
+                            "peak_source": "measured bf16_tflops_sustained", "traffic": None,
+                            "gemm_flop_per_step": gemm_flop, "gemm_ms_per_step": gemm_ms,
+                            "step_tflops": (gemm_flop + attn_flop) / (ms * 1e-3) / 1e12}
+    elif wl == "moe_prefill":
+        T = 1024
+        flop = 2.0 * T * cfg.num_layers * (attn_p + router_p + cfg.top_k * mlp_p)
+        byts = 2.0 * cfg.num_layers * (attn_p + router_p + cfg.num_experts * mlp_p)
+        line["roofline"] = {"bound": "hbm", "kernel": "whole step", "achieved": byts / (ms * 1e-3) / 1e9,
+                            "peak": hbm, "unit": "GB/s", "frac": byts / (ms * 1e-3) / 1e9 / hbm,
+                            "peak_source": "measured hbm_gbs", "traffic": None, "bytes_per_step": byts,
+                            "tflops": flop / (ms * 1e-3) / 1e12}
+    else:
+        ctx_avg = [n + (K - 1) / 2.0 for n in ctx]
+        if wl == "moe_decode":
+            wbytes = 2.0 * cfg.num_layers * (attn_p + router_p + cfg.top_k * mlp_p)
+        else:
+            params = (attn_p + mlp_p) * cfg.num_layers
+            wbytes = params * 1.0 + params / cfg.group_size * 2 * 2
+        byts = wbytes + kv_pos_bytes * sum(c + 1 for c in ctx_avg)
+        line["roofline"] = {"bound": "hbm", "kernel": "whole step", "achieved": byts / (ms * 1e-3) / 1e9,
+                            "peak": hbm, "unit": "GB/s", "frac": byts / (ms * 1e-3) / 1e9 / hbm,
+                            "peak_source": "measured hbm_gbs", "traffic": None, "bytes_per_step": byts,
+                            "weight_bytes": wbytes}
+    stack.close()
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode", choices=WORKLOADS,
+                    help="decode (default: the headline line) or one of the other scope-table workloads")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = {"decode": 256, "prefill": 10, "moe_decode": 56, "moe_prefill": 10, "batched_int8": 64}[
+            args.workload]
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "decode":
+        run_workload(args)
     else:
         run_gpu(args)
 
