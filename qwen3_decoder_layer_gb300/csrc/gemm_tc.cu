@@ -15,10 +15,8 @@
 // For SiLU * up the B tile is two 128-row boxes: gate rows n0.. and up rows
 // N + n0.., so TMEM columns 0..127 hold g and 128..255 hold u of the same
 // output columns.
-#include <cuda.h>
-
-#include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace q3 {
 
@@ -32,62 +30,10 @@ constexpr size_t TC_B_BYTES = (size_t)TC_BN * TC_BK * 2;   // 32 KB
 constexpr size_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
 constexpr size_t TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 1024 /* align */ + 256 /* barriers */;
 
-// ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile with 128-byte rows,
-// 128-byte swizzle and 8-row groups 1024 bytes apart (the layout TMA writes
-// for a {64, rows} bf16 box with CU_TENSOR_MAP_SWIZZLE_128B).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);       // start address
-  d |= (uint64_t)1 << 16;                         // leading-dimension byte offset (unused for this layout)
-  d |= (uint64_t)(1024 >> 4) << 32;               // stride-dimension byte offset: 8 rows x 128 B
-  d |= (uint64_t)1 << 46;                         // descriptor version
-  d |= (uint64_t)2 << 61;                         // swizzle mode: 128 B
-  return d;
-}
+using namespace tc;
 
 // Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TC_BN >> 3) << 17) |
-                            ((uint32_t)(TC_BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_bf16(TC_BM, TC_BN, false);
 
 template <int EPI>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -114,9 +60,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     mbar_fence_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, TC_TMEM_COLS);
-  tc_fence_before();
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_launch();
@@ -146,7 +92,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int s = kt % TC_STAGES;
         ok = mbar_wait(&full[s], (uint32_t)((kt / TC_STAGES) & 1), a.err, 4);
         if (!ok) break;
-        tc_fence_after();
+        fence_after();
         const uint32_t sa = smem_u32(smem + s * TC_STAGE_BYTES);
         const uint32_t sb = sa + (uint32_t)TC_A_BYTES;
 #pragma unroll
@@ -161,7 +107,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) okl = mbar_wait(accum, 0, a.err, 5);
     __syncwarp();
     ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-    tc_fence_after();
+    fence_after();
     const int row = m0 + warp * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
     if (ok) {
@@ -208,47 +154,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 5) {
-    tc_fence_after();
+    fence_after();
     tmem_dealloc(tmem, TC_TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------- host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    else
-      cudaGetLastError();
-  }
-  return fn;
-}
-
 // 2-D bf16 map over a row-major [rows, cols] matrix with row pitch `ld`
 // elements, box {64 columns, box_rows rows}, 128-byte swizzle, zero fill.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {ld * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {ld * 2};
+  return make_map_bf16(m, base, 2, dims, strides, box_rows);
 }
 
 template <int EPI>

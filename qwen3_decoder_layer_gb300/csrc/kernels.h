@@ -150,6 +150,26 @@ cudaError_t launch_attention_prefill(const LaunchCtx& c, int dt, const AttnArgs&
 int attn_prefill_chunk();
 int attn_prefill_nq_max();
 
+// Tensor-core (tcgen05) causal attention for bf16 prefill: one CTA per
+// (128-row query tile, q head); qblocks are 128-row tiles of one sequence.
+// q: bf16 [T, H * D] after RMSNorm + RoPE; kc / vc: the layer's cache of
+// sequence 0, sequences seq_stride elements apart, [KV][capacity][D] inside.
+struct AttnTcArgs {
+  const AttnQBlock* qblocks;
+  int n_qblocks;
+  int T, H, KV, D, capacity, max_seqs;
+  long long seq_stride;
+  const void* q;
+  const void* kc;
+  const void* vc;
+  void* out;           // bf16 [T, H * D]
+  float scale_log2;    // log2(e) / sqrt(D)
+  int* err;
+};
+bool attn_tc_supported(int D);
+int attn_tc_rows();
+cudaError_t launch_attn_tc(const LaunchCtx& c, const AttnTcArgs& a);
+
 // MoE router: softmax over all experts, top-k by logit (ties to the lower
 // index), optional renormalisation; per-expert counts (atomics) if counts != NULL.
 struct RouterArgs {

@@ -482,7 +482,7 @@ int64_t qwen3_last_launch_count(const qwen3_handle* h) { return h ? h->last_laun
 // ======================================================================
 namespace {
 
-enum AttnKind { ATTN_DECODE = 0, ATTN_PREFILL = 1 };
+enum AttnKind { ATTN_DECODE = 0, ATTN_PREFILL = 1, ATTN_TC = 2 };  // decode kernel; SIMT / tcgen05 prefill
 
 struct Plan {
   int T = 0;
@@ -531,9 +531,11 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
   for (auto& g : segs) max_rows = std::max(max_rows, g.n);
   // the decode kernel takes up to 4 rows per sequence, in query blocks of nq_max / G rows
   P.attn = (max_rows <= 4 && G <= attn_decode2_nq_max()) ? ATTN_DECODE : ATTN_PREFILL;
-  P.nq_max = P.attn == ATTN_PREFILL ? attn_prefill_nq_max() : attn_decode2_nq_max();
-  P.chunk = P.attn == ATTN_PREFILL ? attn_prefill_chunk() : attn_decode2_chunk(h->dt);
-  P.rows_per_block = P.nq_max / G;
+  if (P.attn == ATTN_PREFILL && h->dt == DT_BF16 && h->use_tc && attn_tc_supported(c.head_dim)) P.attn = ATTN_TC;
+  P.nq_max = P.attn == ATTN_DECODE ? attn_decode2_nq_max() : attn_prefill_nq_max();
+  P.chunk = P.attn == ATTN_DECODE ? attn_decode2_chunk(h->dt) : attn_prefill_chunk();
+  // tcgen05 attention: 128-row query tiles, each walking all of its keys (one "chunk")
+  P.rows_per_block = P.attn == ATTN_TC ? attn_tc_rows() : P.nq_max / G;
   std::vector<int32_t> qb, items;
   int parts = 0, nqb = 0;
   for (auto& g : segs) {
@@ -541,7 +543,7 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
       const int nr = std::min(P.rows_per_block, g.n - r);
       P.max_nq = std::max(P.max_nq, nr * G);
       const int last_pos = g.pos0 + r + nr - 1;
-      const int nch = (last_pos + 1 + P.chunk - 1) / P.chunk;
+      const int nch = P.attn == ATTN_TC ? 1 : (last_pos + 1 + P.chunk - 1) / P.chunk;
       qb.insert(qb.end(), {g.seq, g.row0 + r, nr, g.pos0 + r, nch, parts, g.row0, g.pos0, g.n, 0});
       for (int ch = 0; ch < nch; ++ch) items.insert(items.end(), {nqb, ch});
       parts += nch;
@@ -766,6 +768,15 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
   r.cos_t = h->rope_cos; r.sin_t = h->rope_sin; r.row_seq = row_seq; r.row_pos = row_pos; r.eps = c.rms_eps;
   e = launch(L, "qk_rope_cache", [&] { return launch_qk_rope_cache(L.ctx, dt, r); });
   if (e != cudaSuccess) return e;
+  if (P.attn == ATTN_TC) {
+    AttnTcArgs t{};
+    t.qblocks = qbs; t.n_qblocks = P.n_qblocks; t.T = P.T; t.H = c.n_heads; t.KV = KV; t.D = D;
+    t.capacity = c.capacity; t.max_seqs = c.max_seqs; t.seq_stride = (long long)h->seq_stride;
+    t.q = B.q; t.kc = kc; t.vc = vc; t.out = B.attn;
+    t.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    t.err = B.err;
+    return launch(L, "attn_tc", [&] { return launch_attn_tc(L.ctx, t); });
+  }
   AttnArgs a{};
   a.q = B.q; a.kc = kc; a.vc = vc; a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity;
   a.H = c.n_heads; a.KV = KV; a.D = D; a.scale = scale; a.qblocks = qbs; a.items = items; a.n_items = n_items;
