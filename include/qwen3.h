@@ -214,6 +214,7 @@ QWEN3_API qwen3_status qwen3_get_length(const qwen3_handle* h, int32_t seq, int3
 #define QWEN3_OPT_PDL 3           /* 1 (default) = programmatic dependent launch between kernels */
 #define QWEN3_OPT_TENSOR_CORES 4  /* 1 (default) = tcgen05 GEMMs for bf16 prefill linears; 0 = CUDA cores */
 #define QWEN3_OPT_L2_PREFETCH 5   /* 1 (default) = decode kernels prefetch the next linear's weights into L2 */
+#define QWEN3_OPT_FUSED_DECODE 6  /* 1 = dense decode steps run as one persistent cooperative kernel; 0 (default) = five kernels per layer */
 QWEN3_API qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value);
 
 /* Kernel timing collected while QWEN3_OPT_PROFILE is on (synchronises the

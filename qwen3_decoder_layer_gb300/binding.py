@@ -22,6 +22,7 @@ STATUS = {0: "QWEN3_OK", 1: "QWEN3_E_ARG", 2: "QWEN3_E_DTYPE", 3: "QWEN3_E_CAPAC
           8: "QWEN3_E_UNSUPPORTED", 9: "QWEN3_E_DEVICE"}
 QWEN3_OPT_CUDA_GRAPHS, QWEN3_OPT_PROFILE, QWEN3_OPT_PDL, QWEN3_OPT_TENSOR_CORES = 1, 2, 3, 4
 QWEN3_OPT_L2_PREFETCH = 5
+QWEN3_OPT_FUSED_DECODE = 6
 
 
 class Qwen3Error(RuntimeError):

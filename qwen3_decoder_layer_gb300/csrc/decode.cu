@@ -19,6 +19,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "kernels.h"
 
 namespace q3 {
@@ -44,29 +45,6 @@ __host__ __device__ inline G2Layout g2_layout(int wbytes, int xbytes, int T, int
   L.total = L.x_bytes + L.ring_bytes + (size_t)nwarps * stages * 8 + G2_MAX_WARPS * 4 * 8;
   return L;
 }
-
-template <typename Dt, int WF> struct G2W;
-template <typename Dt> struct G2W<Dt, W_DT> {
-  static constexpr int EPV = Vec16<Dt>::N;
-  static constexpr int BYTES = sizeof(Dt);
-  __device__ static __forceinline__ void get(const uint4& r, float* w, const Gemv2Args&, size_t, int) {
-    Vec16<Dt>::unpack(r, w);
-  }
-};
-template <typename Dt> struct G2W<Dt, W_U8> {
-  static constexpr int EPV = 16;
-  static constexpr int BYTES = 1;
-  __device__ static __forceinline__ void get(const uint4& r, float* w, const Gemv2Args& a, size_t row, int k0) {
-    const size_t gi = row * (size_t)(a.K / a.group) + k0 / a.group;
-    const float s = __bfloat162float(static_cast<const bf16*>(a.scale)[gi]);
-    const float b = __bfloat162float(static_cast<const bf16*>(a.bias)[gi]);
-    const uint32_t v[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[4 * i + j] = fmaf(s, (float)((v[i] >> (8 * j)) & 0xffu), b);
-  }
-};
 
 // Stage the T input rows in shared memory in the model dtype (16-byte vector
 // loads), applying the prologue.  Every staged value is already a model-dtype
@@ -179,7 +157,7 @@ __device__ __forceinline__ void prefetch_share(const void* p, size_t bytes) {
 template <typename Dt, int WF, int NT, int EPI>
 __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a) {
   extern __shared__ __align__(128) uint8_t g2_smem[];
-  using W = G2W<Dt, WF>;
+  using W = dec::WRow<Dt, WF>;
   constexpr bool PAIR = (EPI == EPI_SWIGLU);
   constexpr int U = (NT * (PAIR ? 2 : 1) * W::EPV > 32) ? 2 : 4;  // 16-byte vectors in flight per lane
   constexpr int XV = Vec16<Dt>::N;                                 // x elements per 16-byte vector
@@ -257,8 +235,8 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
         if (v >= nvec) break;
         const int k0 = v * W::EPV;
         float w0[W::EPV], w1[W::EPV];
-        W::get(q0[i], w0, a, (size_t)u, k0);
-        if (PAIR) W::get(q1[i], w1, a, (size_t)u + a.N, k0);
+        W::get(q0[i], w0, a.scale, a.bias, a.K, a.group, (size_t)u, k0);
+        if (PAIR) W::get(q1[i], w1, a.scale, a.bias, a.K, a.group, (size_t)u + a.N, k0);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           // this lane's x elements k0 .. k0 + EPV: contiguous 16-byte vectors

@@ -291,6 +291,45 @@ cudaError_t launch_attn_decode2(const LaunchCtx& c, int dt, const AttnDecArgs& a
 int attn_decode2_chunk(int dt);
 int attn_decode2_nq_max();
 
+// Whole decode step (T <= 4 rows, dense layers) in one persistent cooperative
+// kernel: per-layer weight pointers in a device table.
+struct FusedLayer {
+  const void *qkv, *qkv_s, *qkv_b, *o, *o_s, *o_b, *gu, *gu_s, *gu_b, *down, *down_s, *down_b;
+  const void *in_norm, *post_norm, *q_norm, *k_norm;
+};
+struct FusedArgs {
+  const FusedLayer* layers;  // [L] device
+  const void* final_norm;
+  int L, T, hidden, H, KV, D, I, group;
+  float eps, scale;
+  int row_seq[4], row_pos[4];
+  void* kc;                  // cache base: layer 0, sequence 0
+  void* vc;
+  long long layer_stride, seq_stride;
+  int capacity;
+  const float* cos_t;
+  const float* sin_t;
+  const void* x;             // dt [T, hidden] input rows
+  void* h;                   // dt [T, hidden] residual stream
+  void* qkv;                 // dt [T, (H + 2 KV) D]
+  void* attn;                // dt [T, H D]
+  void* mbuf;                // dt [T, I]
+  void* out;                 // dt [T, hidden]
+  double* sumsq;             // [2 L + 1][T]
+  float* part_o;             // [parts][KV][8][D]
+  float* part_ml;            // [parts][KV][8][2]
+  int* counters;             // [4 KV], zero at launch
+  unsigned* sync;            // [2]: grid-barrier counter, abort flag; zero at launch
+  int* err;
+  int slot_bytes, n_slots, u_bytes;  // ring geometry (fused_decode_plan)
+};
+// Fills the ring geometry and the dynamic shared memory size; false if this
+// shape is not supported by the fused kernel.
+bool fused_decode_plan(int dt, int wfmt, FusedArgs& a, size_t* smem);
+cudaError_t launch_fused_decode(const LaunchCtx& c, int dt, int wfmt, const FusedArgs& a, int grid, size_t smem);
+int fused_decode_nq_max();
+int fused_decode_chunk();
+
 // out = RMSNorm(h) * gain with the sum of squares of each row precomputed.
 struct NormApplyArgs {
   const void* h;

@@ -74,10 +74,12 @@ struct qwen3_handle {
   std::vector<int32_t> lengths;
   std::string err;
   // options
-  bool use_graphs = true, profile = false, pdl = true, use_tc = true, l2_prefetch = true;
+  bool use_graphs = true, profile = false, pdl = true, use_tc = true, l2_prefetch = true, fused = false;
+  bool coop = false;         // device supports cooperative launches
+  void* fused_layers = nullptr;  // device FusedLayer table (dense stacks)
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
-      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err;
+      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, fsync;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -305,6 +307,9 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
     return QWEN3_E_DEVICE;
   }
   h->num_sms = prop.multiProcessorCount;
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
+  h->coop = coop != 0;
   const qwen3_config& c = h->cfg;
   h->layer_stride = (size_t)c.n_kv_heads * c.capacity * c.head_dim;
   h->seq_stride = h->layer_stride * c.num_layers;
@@ -339,6 +344,21 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
   cudaMemcpy(h->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
   cudaMemcpy(h->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
   h->lengths.assign(c.max_seqs, 0);
+  if (c.num_experts == 0) {  // per-layer weight table of the fused decode kernel
+    std::vector<FusedLayer> fl(c.num_layers);
+    for (int l = 0; l < c.num_layers; ++l) {
+      const qwen3_layer_weights& w = h->layers[l];
+      fl[l] = FusedLayer{w.qkv.w, w.qkv.scale, w.qkv.bias, w.o.w, w.o.scale, w.o.bias, w.gate_up.w,
+                         w.gate_up.scale, w.gate_up.bias, w.down.w, w.down.scale, w.down.bias,
+                         w.in_norm, w.post_norm, w.q_norm, w.k_norm};
+    }
+    if (cudaMalloc(&h->fused_layers, fl.size() * sizeof(FusedLayer)) != cudaSuccess) {
+      cudaGetLastError();
+      qwen3_destroy(h);
+      return QWEN3_E_OOM;
+    }
+    cudaMemcpy(h->fused_layers, fl.data(), fl.size() * sizeof(FusedLayer), cudaMemcpyHostToDevice);
+  }
   for (int i = 0; i < qwen3_handle::kRing; ++i) cudaEventCreateWithFlags(&h->pinned_ev[i], cudaEventDisableTiming);
   cudaStreamCreateWithFlags(&h->gstream, cudaStreamNonBlocking);
   cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming);
@@ -358,7 +378,8 @@ void qwen3_destroy(qwen3_handle* h) {
   for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
-                    &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err};
+                    &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err,
+                    &h->fsync};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -377,6 +398,7 @@ void qwen3_destroy(qwen3_handle* h) {
   if (h->vcache) cudaFree(h->vcache);
   if (h->rope_cos) cudaFree(h->rope_cos);
   if (h->rope_sin) cudaFree(h->rope_sin);
+  if (h->fused_layers) cudaFree(h->fused_layers);
   delete h;
 }
 
@@ -428,6 +450,7 @@ qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value) {
     case QWEN3_OPT_PDL: h->pdl = value != 0; return QWEN3_OK;
     case QWEN3_OPT_TENSOR_CORES: h->use_tc = value != 0; return QWEN3_OK;
     case QWEN3_OPT_L2_PREFETCH: h->l2_prefetch = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_FUSED_DECODE: h->fused = value != 0; return QWEN3_OK;
   }
   return fail(h, QWEN3_E_ARG, "unknown option");
 }
@@ -596,9 +619,13 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   ENS(mbuf, Tz * std::max(c.intermediate, 64) * e, false);
   ENS(sumsq, Tz * (2 * (size_t)c.num_layers + 1) * sizeof(double), true);
   ENS(dev_err, 64, true);
+  ENS(fsync, (size_t)(2 + 4 * c.n_kv_heads) * 4, true);
   // attention partials: sized for the worst case of this row count when graphs replay it
   size_t parts = (size_t)std::max(P.n_parts, 1);
-  if (P.gemv) parts = std::max(parts, (size_t)std::max(P.n_qblocks, T) * ((c.capacity + P.chunk - 1) / P.chunk));
+  if (P.gemv) {
+    const int ch = std::min(P.chunk, fused_decode_chunk());  // the fused kernel's items may be shorter
+    parts = std::max(parts, (size_t)std::max(P.n_qblocks, T) * ((c.capacity + ch - 1) / ch));
+  }
   ENS(part_o, parts * c.n_kv_heads * P.nq_max * c.head_dim * 4, false);
   ENS(part_ml, parts * c.n_kv_heads * P.nq_max * 2 * 4, false);
   ENS(counters, (size_t)std::max(P.n_qblocks, T) * c.n_kv_heads * 4, true);
@@ -946,6 +973,39 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
   return launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
 }
 
+// The fused decode step (one cooperative kernel for the whole stack) applies
+// to dense stacks at decode row counts when the device and shape allow it.
+bool fused_args(qwen3_handle* h, const Plan& P, const void* x, void* out, FusedArgs& a, size_t* smem) {
+  const qwen3_config& c = h->cfg;
+  if (!h->fused || !h->coop || !h->fused_layers || !P.gemv || P.attn != ATTN_DECODE || c.num_experts != 0)
+    return false;
+  a = FusedArgs{};
+  a.layers = static_cast<const FusedLayer*>(h->fused_layers);
+  a.final_norm = h->final_norm;
+  a.L = c.num_layers; a.T = P.T; a.hidden = c.hidden; a.H = c.n_heads; a.KV = c.n_kv_heads; a.D = c.head_dim;
+  a.I = c.intermediate; a.group = c.group_size; a.eps = c.rms_eps;
+  a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+  for (int t = 0; t < P.T; ++t) {
+    a.row_seq[t] = P.blob[P.off_rowseq + t];
+    a.row_pos[t] = P.blob[P.off_rowpos + t];
+  }
+  a.kc = h->kcache; a.vc = h->vcache;
+  a.layer_stride = (long long)h->layer_stride; a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity;
+  a.cos_t = h->rope_cos; a.sin_t = h->rope_sin;
+  a.x = x; a.out = out;
+  return fused_decode_plan(h->dt, h->wfmt, a, smem);
+}
+
+cudaError_t enqueue_fused(qwen3_handle* h, Launcher& L, FusedArgs& a, size_t smem, const Bufs& B) {
+  a.h = B.hA; a.qkv = B.qkv; a.attn = B.attn; a.mbuf = B.m; a.sumsq = B.sumsq;
+  a.part_o = B.part_o; a.part_ml = B.part_ml; a.err = B.err;
+  a.sync = static_cast<unsigned*>(h->fsync.p);
+  a.counters = static_cast<int*>(h->fsync.p) + 2;
+  cudaError_t e = cudaMemsetAsync(h->fsync.p, 0, h->fsync.bytes, L.ctx.stream);
+  if (e != cudaSuccess) return e;
+  return launch(L, "decode_fused", [&] { return launch_fused_decode(L.ctx, h->dt, h->wfmt, a, h->num_sms, smem); });
+}
+
 cudaError_t enqueue_forward(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
   return P.gemv ? enqueue_decode(h, L, P, x, out, B) : enqueue_prefill(h, L, P, x, out, B);
 }
@@ -964,10 +1024,19 @@ extern "C" qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T,
   st = ensure_workspace(h, P, T);
   if (st != QWEN3_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = upload_plan(h, P, s);
-  if (st != QWEN3_OK) return st;
   Bufs B = bufs_of(h);
   Launcher L{h, {s, h->pdl && !h->profile, h->num_sms}};
+  FusedArgs fa;
+  size_t fsmem = 0;
+  if (fused_args(h, P, x, out, fa, &fsmem)) {  // one kernel for the step; the rows travel as launch arguments
+    cudaError_t e = enqueue_fused(h, L, fa, fsmem, B);
+    if (e != cudaSuccess) return cuda_fail(h, e, "fused decode launch");
+    h->last_launches = L.count;
+    for (int t = 0; t < T; ++t) h->lengths[seq_ids[t]] = positions[t] + 1;
+    return QWEN3_OK;
+  }
+  st = upload_plan(h, P, s);
+  if (st != QWEN3_OK) return st;
   const bool graph = h->use_graphs && !h->profile && P.gemv;
   cudaError_t e;
   if (graph) {

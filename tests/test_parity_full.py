@@ -34,12 +34,14 @@ def _gpu_weights(cfg, seed):
     return wd, to_device(wd, "cpu")
 
 
-@pytest.mark.parametrize("dtype,steps", [("bf16", 4), ("fp32", 2)])
-def test_dense_1p7b_decode(cuda_ok, dtype, steps):
-    """28 layers, cache prefilled to 4096 positions with N(0,1) K/V, decode steps."""
+@pytest.mark.parametrize("dtype,steps,fused", [("bf16", 4, 0), ("fp32", 2, 0), ("bf16", 2, 1)])
+def test_dense_1p7b_decode(cuda_ok, dtype, steps, fused):
+    """28 layers, cache prefilled to 4096 positions with N(0,1) K/V, decode steps
+    (fused = 1: the whole step as one persistent cooperative kernel)."""
     cfg = I.with_sizes(I.DENSE_1P7B_DECODE, dtype=dtype)
     wd, w = _gpu_weights(cfg, I.SEEDS["dense_1p7b_decode"])
     p = Parity(cfg, weights=w, device_weights=wd)
+    Q.qwen3_set_option(p.stack.h, Q.QWEN3_OPT_FUSED_DECODE, fused)
     p.fill_cache(0, 4096, seed=3000)
     for s in range(steps):
         p.step(I.make_rows(cfg, 1, seed=3001 + s, device="cuda"))
