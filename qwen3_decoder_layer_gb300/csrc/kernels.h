@@ -100,6 +100,30 @@ struct GemmArgs {
 cudaError_t launch_gemm_simt(const LaunchCtx& c, int dt, int wfmt, const GemmArgs& a);
 int gemm_simt_tile_m();
 
+// Skinny GEMM for 1..64 rows (batched decode with int8 or fp32 weights):
+// out[M, N] = a[M, K] w[N, K]^T, K split over CTAs with an fp32 workspace
+// (ws: 64 x N floats, 64 x 2N for EPI_SWIGLU; counters: one per 64 output
+// columns), both zero between calls.
+struct SkinnyArgs {
+  int M, N, K;
+  const void* a;
+  int lda;
+  const void* w;
+  const void* scale;
+  const void* bias;
+  int group;
+  int epilogue;
+  void* out;
+  int ldo;
+  float* ws;
+  int* counters;
+  int ktiles_per_split;  // set by the launcher
+};
+bool gemm_skinny_supported(int M, int N, int K);
+size_t gemm_skinny_ws_floats(int M, int N, int epilogue);
+int gemm_skinny_tiles(int N);
+cudaError_t launch_gemm_skinny(const LaunchCtx& c, int dt, int wfmt, SkinnyArgs a);
+
 // Tensor-core (tcgen05 / TMEM / TMA) bf16 GEMM: out[M, N] = a[M, K] w[N, K]^T
 // with EPI_STORE, EPI_RESIDUAL (out += R(.), in place) or EPI_SWIGLU (w has
 // 2N rows, gate first).  Dense bf16 weights only.

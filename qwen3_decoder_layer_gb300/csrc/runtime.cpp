@@ -79,7 +79,8 @@ struct qwen3_handle {
   void* fused_layers = nullptr;  // device FusedLayer table (dense stacks)
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
-      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, fsync;
+      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, fsync, skws,
+      skcnt;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -379,7 +380,7 @@ void qwen3_destroy(qwen3_handle* h) {
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                     &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err,
-                    &h->fsync};
+                    &h->fsync, &h->skws, &h->skcnt};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -620,6 +621,12 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   ENS(sumsq, Tz * (2 * (size_t)c.num_layers + 1) * sizeof(double), true);
   ENS(dev_err, 64, true);
   ENS(fsync, (size_t)(2 + 4 * c.n_kv_heads) * 4, true);
+  if (!P.gemv && T <= 64) {  // skinny GEMM split-K workspace (kept zero by the kernel)
+    const size_t nmax = std::max({(size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, (size_t)c.hidden,
+                                  2 * (size_t)c.intermediate});
+    ENS(skws, 64 * nmax * 4, true);
+    ENS(skcnt, (size_t)gemm_skinny_tiles((int)nmax) * 4, true);
+  }
   // attention partials: sized for the worst case of this row count when graphs replay it
   size_t parts = (size_t)std::max(P.n_parts, 1);
   if (P.gemv) {
@@ -908,6 +915,13 @@ cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const char* tc_name, const
     t.M = g.M; t.N = g.N; t.K = g.K; t.a = g.a; t.lda = g.lda; t.w = g.w; t.out = g.out; t.ldo = g.ldo;
     t.epilogue = g.epilogue; t.err = B.err;
     return launch(L, tc_name, [&] { return launch_gemm_tc(L.ctx, t); });
+  }
+  if (g.M <= 64 && !g.a_rows && !g.c_rows && !g.tile_start && gemm_skinny_supported(g.M, g.N, g.K) && h->skws.p) {
+    SkinnyArgs k{};
+    k.M = g.M; k.N = g.N; k.K = g.K; k.a = g.a; k.lda = g.lda; k.w = g.w; k.scale = g.scale; k.bias = g.bias;
+    k.group = g.group; k.epilogue = g.epilogue; k.out = g.out; k.ldo = g.ldo;
+    k.ws = static_cast<float*>(h->skws.p); k.counters = static_cast<int*>(h->skcnt.p);
+    return launch(L, simt_name, [&] { return launch_gemm_skinny(L.ctx, h->dt, wfmt, k); });
   }
   return launch(L, simt_name, [&] { return launch_gemm_simt(L.ctx, h->dt, wfmt, g); });
 }
