@@ -7,7 +7,8 @@
 // Split-K ("flash-decoding"): the keys of each query block (rows of one
 // sequence, x G query heads of kv head j) are cut into chunks of SUBS
 // sub-chunks of CK keys.  A work item is one (query block, chunk, kv head);
-// a persistent grid walks the item list.
+// each block of the grid walks a contiguous range of the item list (kv head
+// on y), so that most consecutive items continue the same query block.
 //
 // Warp-specialised block.  One producer warp streams the sub-chunks of the
 // block's items, in order, into a 4-stage shared-memory ring (one item) with
@@ -19,9 +20,11 @@
 // appended in this call computed from the qkv row (and stored to the cache
 // by the item owning the row), scores, a warp-local softmax, P.V -- with no
 // block barrier, producing a warp partial (m, l, o).  A block barrier, one
-// merge of the 16 partials, and the item's partial (m, l, o) goes to global
-// memory.  The last item of a (query block, kv head) -- found with an atomic
-// counter, no waiting -- merges the chunks: M = max m_c,
+// merge of the 16 partials per RUN of consecutive items of one query block
+// (queries staged once per run, each warp carrying its online-softmax state
+// (m, l, o) across the run), and the run's partial goes to global memory.
+// The last run of a (query block, kv head) -- found with an atomic counter,
+// no waiting -- merges the runs: M = max m_c,
 // out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c, rounded once to the
 // model dtype.
 #include <math_constants.h>
@@ -86,6 +89,384 @@ __device__ __forceinline__ ItemKeys item_keys(const AttnItem& item, const AttnQB
 
 template <typename Dt, int D, int NQ>
 __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs a) {
+  extern __shared__ __align__(128) uint8_t ad_smem[];
+  using LY = ADLayout<Dt, D, NQ>;
+  constexpr int CK = LY::CK;
+  constexpr int KW = LY::KW;            // keys per warp
+  constexpr int EPV = 16 / sizeof(Dt);  // elements per 16-byte vector
+  constexpr int LPK = D / EPV;          // lanes per key in the score loop
+  constexpr int KPS = 32 / LPK;         // keys per score step
+  constexpr int DPL = D / 32;           // head elements per lane
+  constexpr int WP = LY::WPITCH;
+  constexpr int MP = LY::MPITCH;
+  float* qs = reinterpret_cast<float*>(ad_smem + LY::OFF_QS);
+  float* ps_all = reinterpret_cast<float*>(ad_smem + LY::OFF_PS);
+  float* wp = reinterpret_cast<float*>(ad_smem + LY::OFF_WP);
+  float* mrg = reinterpret_cast<float*>(ad_smem + LY::OFF_MRG);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
+  uint64_t* empty = full + AD_STAGES;
+  __shared__ int s_flag, s_fail;
+  __shared__ int s_issued[AD_STAGES];  // uses of each stage issued so far
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = blockIdx.y;
+  const int G = a.H / a.KV;
+  const int qkv_ld = (a.H + 2 * a.KV) * D;
+  const int n_items = *a.n_items;
+  auto tiles = [&](int s) { return ad_smem + (size_t)s * LY::STAGE; };
+
+  if (tid == 0) {
+    for (int s = 0; s < AD_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], AD_WPS);
+    }
+    mbar_fence_init();
+    s_fail = 0;
+  }
+  if (tid < AD_STAGES) s_issued[tid] = 0;
+  __syncthreads();
+
+  if (warp == AD_CWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const Dt* kc = static_cast<const Dt*>(a.kc);
+      const Dt* vc = static_cast<const Dt*>(a.vc);
+      int g = 0;
+      // at most one item per block: item x; else the contiguous range (as the consumers)
+      const int it_lo = n_items <= (int)gridDim.x ? (int)blockIdx.x
+                                                  : (int)(blockIdx.x * (unsigned)n_items / gridDim.x);
+      const int it_hi = n_items <= (int)gridDim.x ? min((int)blockIdx.x + 1, n_items)
+                                                  : (int)((blockIdx.x + 1) * (unsigned)n_items / gridDim.x);
+      for (int it = it_lo; it < it_hi; ++it) {
+        const AttnItem item = a.items[it];
+        const AttnQBlock qb = a.qblocks[item.qb];
+        const ItemKeys ik = item_keys<Dt>(item, qb);
+        for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
+          const int s = g % AD_STAGES;
+          if (g >= AD_STAGES && !mbar_wait(&empty[s], (uint32_t)((g / AD_STAGES - 1) & 1), a.err, 2)) {
+            s_fail = 1;
+            return;
+          }
+          const int k0 = ik.key0 + sub * CK;
+          const int nk = min(CK, ik.key0 + ik.nkeys - k0);
+          const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
+          const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
+          mbar_expect_tx(&full[s], 2 * bytes);
+          tma_load_1d(tiles(s), kc + off, bytes, &full[s]);
+          tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
+          *(volatile int*)&s_issued[s] = g / AD_STAGES + 1;
+        }
+      }
+      // L2 prefetch of this block's share of the next kernel's operand
+      if (a.pf && a.pf_bytes) {
+        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+        const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
+        for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
+          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  pdl_wait();
+  pdl_launch();
+  const Dt* qkv = static_cast<const Dt*>(a.qkv);
+  float* ps = ps_all + (size_t)warp * NQ * KW;  // this warp's scores / probabilities
+  const int wsub = warp / AD_WPS;               // sub-chunk of this warp
+  const int wk0 = (warp % AD_WPS) * KW;         // its first key inside the sub-chunk
+  int g = 0;                                    // block-wide sub-chunk sequence position
+  // This block owns items [lo(x), lo(x + 1)) of kv head j, lo(x) = x n / gx:
+  // runs of consecutive chunks of one query block, so the queries are staged
+  // once per run and each warp carries its online-softmax state (m, l, o)
+  // across the run's chunks.  One partial per run; the last run of a query
+  // block (an atomic counter over its runs) combines them.
+  const int gx = gridDim.x;
+  auto lo_of = [&](int x) { return (int)((unsigned)x * (unsigned)n_items / (unsigned)gx); };  // n_items * gx < 2^32
+  // (with at most one item per block, block x takes item x)
+  const int it_lo = n_items <= gx ? (int)blockIdx.x : lo_of(blockIdx.x);
+  const int it_hi = n_items <= gx ? min((int)blockIdx.x + 1, n_items) : lo_of(blockIdx.x + 1);
+  float m_w[NQ], l_w[NQ], o_w[NQ][DPL];
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      m_w[i] = -CUDART_INF_F;
+      l_w[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
+    }
+  };
+  reset_state();
+  __shared__ int s_run[2];  // this block's run index within the query block, number of runs
+
+  // merge the warps' states of the run over query block b into its partial;
+  // the last run of b combines
+  auto flush = [&](int b) {
+    const AttnQBlock qb = a.qblocks[b];
+    const int nq = qb.nrows * G;
+    float* mine = wp + (size_t)warp * NQ * WP;
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      store_lane_vec<DPL>(mine + i * WP + lane * DPL, o_w[i]);
+      if (lane == 0) { mine[i * WP + D] = m_w[i]; mine[i * WP + D + 1] = l_w[i]; }
+    }
+    if (tid == 0) {  // runs of b: blocks with a non-empty range meeting b's items [part_base, part_base + n_chunks)
+      const int s0 = qb.part_base, s1 = qb.part_base + qb.n_chunks;
+      if (n_items <= gx) {  // one item per block: the run index is the item's chunk
+        s_run[0] = it_lo - s0;
+        s_run[1] = s1 - s0;
+      } else {  // every range is non-empty; the block holding item i is ceil((i + 1) gx / n) - 1
+        auto owner = [&](int i) { return (int)(((unsigned)(i + 1) * (unsigned)gx + n_items - 1) / (unsigned)n_items) - 1; };
+        const int x0 = owner(s0);
+        s_run[0] = (int)blockIdx.x - x0;
+        s_run[1] = owner(s1 - 1) - x0 + 1;
+      }
+    }
+    csync();
+    if (s_fail) return;
+    const size_t part0 = ((size_t)(qb.part_base + s_run[0]) * a.KV + j) * a.nq_max;
+    if (warp < nq) {
+      const int i = warp;
+      const float m = lane < AD_CWARPS ? wp[((size_t)lane * NQ + i) * WP + D] : -CUDART_INF_F;
+      const float M = warp_max(m);
+      const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+      const float L = warp_sum(lane < AD_CWARPS ? f * wp[((size_t)lane * NQ + i) * WP + D + 1] : 0.f);
+      if (lane < AD_CWARPS) mrg[i * MP + lane] = f;
+      if (lane == 0) {
+        a.part_ml[(part0 + i) * 2] = M;
+        a.part_ml[(part0 + i) * 2 + 1] = L;
+      }
+    }
+    csync();
+    for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
+      const int i = idx / D, d = idx % D;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < AD_CWARPS; ++w) v = fmaf(wp[((size_t)w * NQ + i) * WP + d], mrg[i * MP + w], v);
+      a.part_o[(part0 + i) * D + d] = v;
+    }
+    __threadfence();
+    csync();
+    if (tid == 0) {
+      const int prev = atomicAdd(a.counters + (size_t)b * a.KV + j, 1);
+      s_flag = (prev == s_run[1] - 1);
+    }
+    csync();
+    if (s_flag) {
+      __threadfence();
+      const int nc = s_run[1];
+      const size_t pbase = (size_t)qb.part_base * a.KV + j;  // partial of run c: (pbase + c * KV) * nq_max
+      const bool staged = (size_t)nc * nq <= LY::WP_FLOATS;
+      float* fs = wp;  // [c][i]: run maxima, then their weights e^(m_c - M_i)
+      if (staged) {
+        for (int idx = tid; idx < nc * nq; idx += AD_CTHREADS) {
+          const int c = idx / nq, i = idx % nq;
+          fs[idx] = __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
+        }
+        csync();
+      }
+      for (int i = warp; i < nq; i += AD_CWARPS) {
+        auto mval = [&](int c) {
+          return staged ? fs[c * nq + i] : __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
+        };
+        float M = -CUDART_INF_F;
+        for (int c = lane; c < nc; c += 32) M = fmaxf(M, mval(c));
+        M = warp_max(M);
+        float Lsum = 0.f;
+        for (int c = lane; c < nc; c += 32) {
+          const float m = mval(c);
+          const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+          Lsum = fmaf(__ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2 + 1), f, Lsum);
+          if (staged) fs[c * nq + i] = f;
+        }
+        Lsum = warp_sum(Lsum);
+        if (lane == 0) { mrg[i * MP + AD_CWARPS] = M; mrg[i * MP + AD_CWARPS + 1] = Lsum; }
+      }
+      csync();
+      for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
+        const int i = idx / D, d = idx % D;
+        const float M = mrg[i * MP + AD_CWARPS];
+        float v = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < nc; ++c) {
+          const size_t p = (pbase + (size_t)c * a.KV) * a.nq_max + i;
+          float f;
+          if (staged) {
+            f = fs[c * nq + i];
+          } else {
+            const float m = __ldcg(a.part_ml + p * 2);
+            f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+          }
+          v = fmaf(__ldcg(a.part_o + p * D + d), f, v);
+        }
+        const int row = qb.row0 + i / G, head = j * G + i % G;
+        static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / mrg[i * MP + AD_CWARPS + 1]);
+      }
+      if (tid == 0) a.counters[(size_t)b * a.KV + j] = 0;
+    }
+    csync();
+  };
+
+  int cur = -1;  // query block of the current run
+  for (int it = it_lo; it < it_hi; ++it) {
+    const AttnItem item = a.items[it];
+    const AttnQBlock qb = a.qblocks[item.qb];
+    const ItemKeys ik = item_keys<Dt>(item, qb);
+    const int nq = qb.nrows * G;  // <= NQ
+    if (item.qb != cur) {
+      if (cur >= 0) {
+        flush(cur);
+        if (s_fail) break;
+        reset_state();
+      }
+      cur = item.qb;
+      // queries: RMSNorm + RoPE of this block's q heads of kv group j (warp per query)
+      if (warp < NQ) {
+        const int i = warp;
+        float x[DPL];
+        if (i < nq) {
+          const int row = qb.row0 + i / G, hh = j * G + i % G;
+          const Dt* src = qkv + (size_t)row * qkv_ld + (size_t)hh * D + lane * DPL;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) x[e] = to_f(src[e]);
+          norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.q_gain), a.cos_t, a.sin_t, qb.pos0 + i / G, a.eps);
+        } else {
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) x[e] = 0.f;
+        }
+        store_lane_vec<DPL>(qs + i * D + lane * DPL, x);
+      }
+      csync();
+    }
+
+    // ---- this warp's keys of the item, folded into its running state
+    if (wsub < ik.nsub) {
+      const int s = (g + wsub) % AD_STAGES;
+      const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
+      const int nk = min(KW, ik.key0 + ik.nkeys - key0 - wk0);  // this warp's keys (may be <= 0)
+      Dt* Kt = reinterpret_cast<Dt*>(tiles(s)) + (size_t)wk0 * D;
+      Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE) + (size_t)wk0 * D;
+      // A warp may reach a stage before the previous use of it has landed
+      // (it skips the sub-chunks a shorter item does not have): wait until the
+      // producer has issued this use, so that the parity wait below cannot
+      // match the previous phase.
+      int landed = 1;
+      if (lane == 0) {
+        const int use = (g + wsub) / AD_STAGES;
+        const long long t0 = clock64();
+        while (*(volatile int*)&s_issued[s] <= use) {
+          if (clock64() - t0 > (1ll << 31)) {
+            atomicExch(a.err, 2);
+            landed = 0;
+            break;
+          }
+        }
+        if (landed) landed = mbar_wait(&full[s], (uint32_t)(use & 1), a.err, 2);
+      }
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, landed, 0)) {
+        s_fail = 1;
+      } else if (nk > 0) {
+        const int kb = key0 + wk0;  // absolute position of this warp's first key
+        // keys appended by this call among this warp's keys
+        const int n0 = max(kb, qb.seg_pos0), n1 = min(kb + nk, qb.seg_pos0 + qb.seg_n);
+        for (int u = n0; u < n1; ++u) {
+          const int row = qb.seg_row0 + (u - qb.seg_pos0);
+          float x[DPL], v[DPL];
+          const Dt* ksrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + j) * D + lane * DPL;
+          const Dt* vsrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + a.KV + j) * D + lane * DPL;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) { x[e] = to_f(ksrc[e]); v[e] = to_f(vsrc[e]); }
+          norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.k_gain), a.cos_t, a.sin_t, u, a.eps);
+          const bool owner = row >= qb.row0 && row < qb.row0 + qb.nrows;
+          const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) {
+            Kt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(x[e]);
+            Vt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+            if (owner) {
+              static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
+              static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
+            }
+          }
+        }
+        __syncwarp();
+        // scores: LPK lanes per key, KPS keys per step
+        const int sub_l = lane % LPK, kq = lane / LPK;
+#pragma unroll
+        for (int st = 0; st < KW / KPS; ++st) {
+          const int u = st * KPS + kq;
+          float kv[EPV];
+          if (u < nk) {
+            Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            const float4* qp = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV);
+            float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPV / 4; ++e) {
+              const float4 q4 = qp[e];
+              d0 = fmaf(q4.x, kv[4 * e], d0);
+              d1 = fmaf(q4.y, kv[4 * e + 1], d1);
+              d0 = fmaf(q4.z, kv[4 * e + 2], d0);
+              d1 = fmaf(q4.w, kv[4 * e + 3], d1);
+            }
+            float d = d0 + d1;
+#pragma unroll
+            for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            if (sub_l == 0)
+              ps[i * KW + u] = (u < nk && i < nq && kb + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
+          }
+        }
+        __syncwarp();
+        // online softmax update of the warp's running state (lanes over keys)
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          const float sv = lane < KW ? ps[i * KW + lane] : -CUDART_INF_F;
+          const float mx = warp_max(sv);
+          const float m_new = fmaxf(m_w[i], mx);
+          const float p = (sv == -CUDART_INF_F) ? 0.f : expf(sv - m_new);
+          const float alpha = (m_w[i] == -CUDART_INF_F) ? 0.f : expf(m_w[i] - m_new);
+          const float ls = warp_sum(p);
+          if (lane < KW) ps[i * KW + lane] = p;
+          if (m_new != -CUDART_INF_F) {
+            l_w[i] = fmaf(l_w[i], alpha, ls);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o_w[i][e] *= alpha;
+            m_w[i] = m_new;
+          }
+        }
+        __syncwarp();
+        // P.V: lane holds head elements lane*DPL .. +DPL
+#pragma unroll 4
+        for (int u = 0; u < nk; ++u) {
+          float v[DPL];
+          load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            const float p = ps[i * KW + u];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o_w[i][e] = fmaf(p, v[e], o_w[i][e]);
+          }
+        }
+      }
+      // this warp is done with its part of the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    g += ik.nsub;
+  }
+  if (cur >= 0 && !s_fail) flush(cur);
+}
+
+// One item per block and step of the persistent loop (used when the grid has
+// at least as many blocks as items, e.g. batch-1 decode): the queries are
+// staged and the warp partials merged for every item.
+template <typename Dt, int D, int NQ>
+__global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDecArgs a) {
   extern __shared__ __align__(128) uint8_t ad_smem[];
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
@@ -395,11 +776,15 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
 
 template <typename Dt, int D, int NQ>
 cudaError_t ad_launch(const LaunchCtx& c, const AttnDecArgs& a) {
-  auto kern = attn_decode_kernel<Dt, D, NQ>;
+  auto kern = a.runs ? attn_decode_kernel<Dt, D, NQ> : attn_decode_item_kernel<Dt, D, NQ>;
   using LY = ADLayout<Dt, D, NQ>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::TOTAL);
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<Dt, D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)LY::TOTAL);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_decode_item_kernel<Dt, D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)LY::TOTAL);
     if (e != cudaSuccess) return e;
     configured = true;
   }

@@ -307,6 +307,7 @@ struct AttnDecArgs {
   void* out;
   int grid_x;
   int nq;              // largest query-vector count (rows x G) of any query block, <= attn_decode2_nq_max()
+  int runs;            // 1: blocks walk contiguous item ranges (more items than blocks); 0: one item per block
   int* err;
   const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
   size_t pf_bytes;

@@ -793,6 +793,7 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
     a.counters = B.counters; a.out = B.attn; a.err = B.err;
     a.grid_x = std::max(1, (h->num_sms + KV - 1) / KV);
     a.nq = P.max_nq;
+    a.runs = P.n_items > a.grid_x;
     a.pf = pf; a.pf_bytes = pf_bytes;
     return launch(L, "attn_decode", [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
@@ -1054,7 +1055,8 @@ extern "C" qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T,
   const bool graph = h->use_graphs && !h->profile && P.gemv;
   cudaError_t e;
   if (graph) {
-    const GraphKey key{T, P.attn * 64 + P.max_nq, x, out};
+    const int runs = P.attn == ATTN_DECODE && P.n_items > std::max(1, (h->num_sms + h->cfg.n_kv_heads - 1) / h->cfg.n_kv_heads);
+    const GraphKey key{T, P.attn * 64 + P.max_nq + (runs ? 32 : 0), x, out};
     if (h->graphs.size() > 32) {  // callers cycling through buffers: start over
       for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
       h->graphs.clear();
