@@ -10,10 +10,11 @@
 // for N = 2048.  Each CTA streams its weight slice once, dequantises it into
 // shared memory as fp32, and accumulates a 2x4 or 4x4 (x2 for gate|up)
 // register tile per thread in fp32.  With one K split the epilogue runs from
-// registers; otherwise partial tiles are added into an fp32 workspace with
-// atomics and the last CTA of a tile (an atomic counter) applies the
-// epilogue -- rounding, residual add or SiLU * up -- and leaves the workspace
-// tile and its counter at zero for the next call.
+// registers; otherwise each split stores its partial tile to its own slice of
+// an fp32 workspace and the last CTA of a tile (an atomic counter) adds the
+// slices in split order -- the result does not depend on which CTA finishes
+// when -- and applies the epilogue (rounding, residual add or SiLU * up),
+// leaving the counter at zero for the next call.
 #include <algorithm>
 
 #include "common.cuh"
@@ -23,7 +24,7 @@ namespace q3 {
 
 namespace {
 
-constexpr int SK_BN = 64, SK_BK = 32, SK_THREADS = 256;
+constexpr int SK_BN = 64, SK_BK = 32, SK_THREADS = 256, SK_MAX_SPLIT = 8;
 
 template <typename Dt, int WF>
 __device__ __forceinline__ void load_w_tile(float (*Ws)[2 * SK_BN + 4], const SkinnyArgs& a, int k0, int n0,
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(SK_THREADS) gemm_skinny_kernel(SkinnyArgs a) {
     }
   };
   const int ldw = PAIR ? 2 * a.N : a.N;  // workspace row pitch (gate sums, then up sums)
+  const size_t slice = (size_t)a.M * ldw;  // floats per split
   if (gridDim.y == 1) {
 #pragma unroll
     for (int i = 0; i < TM; ++i)
@@ -160,8 +162,9 @@ __global__ void __launch_bounds__(SK_THREADS) gemm_skinny_kernel(SkinnyArgs a) {
     for (int j = 0; j < 4; ++j) {
       const int m = ty * TM + i, n = n0 + tx * 4 + j;
       if (m < a.M && n < a.N) {
-        atomicAdd(a.ws + (size_t)m * ldw + n, acc[i][j]);
-        if (PAIR) atomicAdd(a.ws + (size_t)m * ldw + a.N + n, acc2[PAIR ? i : 0][j]);
+        float* w = a.ws + ks * slice + (size_t)m * ldw + n;
+        __stcg(w, acc[i][j]);
+        if (PAIR) __stcg(w + a.N, acc2[PAIR ? i : 0][j]);
       }
     }
   __threadfence();
@@ -173,13 +176,11 @@ __global__ void __launch_bounds__(SK_THREADS) gemm_skinny_kernel(SkinnyArgs a) {
   for (int idx = tid; idx < a.M * SK_BN; idx += SK_THREADS) {
     const int m = idx / SK_BN, n = n0 + idx % SK_BN;
     if (n >= a.N) continue;
-    float* pg = a.ws + (size_t)m * ldw + n;
-    const float g = __ldcg(pg);
-    float u = 0.f;
-    __stcg(pg, 0.f);
-    if (PAIR) {
-      u = __ldcg(pg + a.N);
-      __stcg(pg + a.N, 0.f);
+    const float* pg = a.ws + (size_t)m * ldw + n;
+    float g = 0.f, u = 0.f;
+    for (int k = 0; k < (int)gridDim.y; ++k) {
+      g += __ldcg(pg + k * slice);
+      if (PAIR) u += __ldcg(pg + k * slice + a.N);
     }
     finish(m, n, g, u);
   }
@@ -207,7 +208,7 @@ cudaError_t sk_mt(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
 bool gemm_skinny_supported(int M, int N, int K) { return M >= 1 && M <= 64 && N >= 1 && K % SK_BK == 0; }
 
 size_t gemm_skinny_ws_floats(int M, int N, int epilogue) {
-  return (size_t)64 * (epilogue == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N);
+  return (size_t)SK_MAX_SPLIT * M * (epilogue == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N);
 }
 int gemm_skinny_tiles(int N) { return (N + SK_BN - 1) / SK_BN; }
 
@@ -215,7 +216,7 @@ cudaError_t launch_gemm_skinny(const LaunchCtx& c, int dt, int wfmt, SkinnyArgs 
   if (!gemm_skinny_supported(a.M, a.N, a.K)) return cudaErrorInvalidValue;
   const int tiles = gemm_skinny_tiles(a.N), ktiles = a.K / SK_BK;
   // split K so that the grid holds about two CTAs per SM
-  int split = std::max(1, std::min(ktiles, (2 * c.num_sms + tiles - 1) / tiles));
+  int split = std::max(1, std::min({ktiles, (2 * c.num_sms + tiles - 1) / tiles, SK_MAX_SPLIT}));
   a.ktiles_per_split = (ktiles + split - 1) / split;
   split = (ktiles + a.ktiles_per_split - 1) / a.ktiles_per_split;
   if (split > 1 && (!a.ws || !a.counters)) return cudaErrorInvalidValue;

@@ -4,9 +4,10 @@
 //
 //   C[M, N] = A[M, K] . B[N, K]^T      (A: activations, B: nn.Linear weight; both K-major)
 //
-// One CTA computes a 128 x 256 tile with tcgen05.mma (cta_group::1,
-// kind::f16, M = 128, N = 256, K = 16 per instruction) accumulating in
-// tensor memory.  A 4-stage ring of 128 x 64 (A) and 256 x 64 (B) bf16 tiles
+// A persistent grid (one CTA per SM) walks the 128 x 256 output tiles; each
+// tile is computed with tcgen05.mma (cta_group::1, kind::f16, M = 128,
+// N = 256, K = 16 per instruction) into one of two tensor-memory
+// accumulators, so that the epilogue of a tile overlaps the MMAs of the next.  A 4-stage ring of 128 x 64 (A) and 256 x 64 (B) bf16 tiles
 // is filled by 2-D TMA loads with 128-byte swizzle; mbarriers hand stages
 // from the TMA warp to the MMA warp (full) and back (empty, signalled by
 // tcgen05.commit).  Four epilogue warps read the accumulator with
@@ -15,6 +16,8 @@
 // For SiLU * up the B tile is two 128-row boxes: gate rows n0.. and up rows
 // N + n0.., so TMEM columns 0..127 hold g and 128..255 hold u of the same
 // output columns.
+#include <algorithm>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -24,7 +27,7 @@ namespace {
 
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
 constexpr int TC_THREADS = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA
-constexpr uint32_t TC_TMEM_COLS = 256;
+constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column accumulators
 constexpr size_t TC_A_BYTES = (size_t)TC_BM * TC_BK * 2;   // 16 KB
 constexpr size_t TC_B_BYTES = (size_t)TC_BN * TC_BK * 2;   // 32 KB
 constexpr size_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
@@ -43,20 +46,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_STAGES * TC_STAGE_BYTES);
   uint64_t* empty = full + TC_STAGES;
-  uint64_t* accum = empty + TC_STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* acc_full = empty + TC_STAGES;  // [2] accumulator b holds a finished tile
+  uint64_t* acc_empty = acc_full + 2;      // [2] the epilogue has read accumulator b
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * TC_BM;
-  const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;  // output columns of this tile
-  const int n0 = blockIdx.x * ncol;
+  const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;  // output columns of a tile
+  const int tiles_m = (a.M + TC_BM - 1) / TC_BM, tiles = tiles_m * (a.N / ncol);
   const int nk = a.K / TC_BK;
+  // tile t -> rows (t % tiles_m), columns (t / tiles_m): blocks running at the
+  // same time share weight tiles in L2
 
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
     mbar_fence_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, TC_TMEM_COLS);
@@ -67,50 +75,63 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pdl_wait();
   pdl_launch();
 
-  bool ok = true;
   if (warp == 4) {
-    if (lane == 0) {  // TMA producer
-      for (int kt = 0; kt < nk && ok; ++kt) {
-        const int s = kt % TC_STAGES;
-        if (kt >= TC_STAGES) ok = mbar_wait(&empty[s], (uint32_t)((kt / TC_STAGES - 1) & 1), a.err, 3);
-        if (!ok) break;
-        uint8_t* sa = smem + s * TC_STAGE_BYTES;
-        uint8_t* sb = sa + TC_A_BYTES;
-        mbar_expect_tx(&full[s], (uint32_t)TC_STAGE_BYTES);
-        tma_load_2d(sa, &map_a, kt * TC_BK, m0, &full[s]);
-        if (EPI == EPI_SWIGLU) {
-          tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
-          tma_load_2d(sb + TC_B_BYTES / 2, &map_b, kt * TC_BK, a.N + n0, &full[s]);
-        } else {
-          tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
+    if (lane == 0) {  // TMA producer: the k-blocks of this block's tiles, in order
+      int q = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * ncol;
+        for (int kt = 0; kt < nk; ++kt, ++q) {
+          const int s = q % TC_STAGES;
+          if (q >= TC_STAGES && !(ok = mbar_wait(&empty[s], (uint32_t)((q / TC_STAGES - 1) & 1), a.err, 3))) break;
+          uint8_t* sa = smem + s * TC_STAGE_BYTES;
+          uint8_t* sb = sa + TC_A_BYTES;
+          mbar_expect_tx(&full[s], (uint32_t)TC_STAGE_BYTES);
+          tma_load_2d(sa, &map_a, kt * TC_BK, m0, &full[s]);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
+            tma_load_2d(sb + TC_B_BYTES / 2, &map_b, kt * TC_BK, a.N + n0, &full[s]);
+          } else {
+            tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
+          }
         }
       }
     }
   } else if (warp == 5) {
-    if (lane == 0) {  // MMA issuer
-      for (int kt = 0; kt < nk && ok; ++kt) {
-        const int s = kt % TC_STAGES;
-        ok = mbar_wait(&full[s], (uint32_t)((kt / TC_STAGES) & 1), a.err, 4);
-        if (!ok) break;
+    if (lane == 0) {  // MMA issuer: tile i accumulates in TMEM columns (i & 1) * 256
+      int q = 0, i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
+        const int b = i & 1, use = i >> 1;
+        if (use > 0 && !(ok = mbar_wait(&acc_empty[b], (uint32_t)((use - 1) & 1), a.err, 6))) break;
         fence_after();
-        const uint32_t sa = smem_u32(smem + s * TC_STAGE_BYTES);
-        const uint32_t sb = sa + (uint32_t)TC_A_BYTES;
+        const uint32_t d = tmem + (uint32_t)(b * TC_BN);
+        for (int kt = 0; kt < nk; ++kt, ++q) {
+          const int s = q % TC_STAGES;
+          if (!(ok = mbar_wait(&full[s], (uint32_t)((q / TC_STAGES) & 1), a.err, 4))) break;
+          fence_after();
+          const uint32_t sa = smem_u32(smem + s * TC_STAGE_BYTES);
+          const uint32_t sb = sa + (uint32_t)TC_A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk)
-          mma_bf16(tmem, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc, (kt | kk) != 0);
-        mma_commit(&empty[s]);
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc, (kt | kk) != 0);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&acc_full[b]);
       }
-      if (ok) mma_commit(accum);
     }
   } else {  // epilogue: warp q reads TMEM lanes 32q .. 32q + 31 = tile rows
-    int okl = 1;  // lane 0 waits for the accumulator; the other lanes wait at the warp barrier
-    if (lane == 0) okl = mbar_wait(accum, 0, a.err, 5);
-    __syncwarp();
-    ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
-    fence_after();
-    const int row = m0 + warp * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    if (ok) {
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int b = i & 1, use = i >> 1;
+      const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * ncol;
+      int okl = 1;  // lane 0 waits for the accumulator; the other lanes wait at the warp barrier
+      if (lane == 0) okl = mbar_wait(&acc_full[b], (uint32_t)(use & 1), a.err, 5);
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, okl, 0)) break;
+      fence_after();
+      const int row = m0 + warp * 32 + lane;
+      const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * TC_BN);
       if (EPI == EPI_SWIGLU) {
         for (int c = 0; c < TC_BN / 2; c += 32) {
           uint32_t g[32], u[32];
@@ -119,13 +140,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (row < a.M) {
             float o[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gv = rd<bf16>(__uint_as_float(g[i])), uv = rd<bf16>(__uint_as_float(u[i]));
-              o[i] = rd<bf16>(silu_f(gv)) * uv;
+            for (int e = 0; e < 32; ++e) {
+              const float gv = rd<bf16>(__uint_as_float(g[e])), uv = rd<bf16>(__uint_as_float(u[e]));
+              o[e] = rd<bf16>(silu_f(gv)) * uv;
             }
             uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(a.out) + (size_t)row * a.ldo + n0 + c);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = Vec16<bf16>::pack(o + 8 * q);
+            for (int v = 0; v < 4; ++v) dst[v] = Vec16<bf16>::pack(o + 8 * v);
           }
         }
       } else {
@@ -137,21 +158,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             float o[32];
             if (EPI == EPI_RESIDUAL) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              for (int v = 0; v < 4; ++v) {
                 float hv[8];
-                Vec16<bf16>::unpack(reinterpret_cast<const uint4*>(p)[q], hv);
+                Vec16<bf16>::unpack(reinterpret_cast<const uint4*>(p)[v], hv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o[8 * q + i] = hv[i] + rd<bf16>(__uint_as_float(r[8 * q + i]));
+                for (int e = 0; e < 8; ++e) o[8 * v + e] = hv[e] + rd<bf16>(__uint_as_float(r[8 * v + e]));
               }
             } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+              for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]);
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(p)[q] = Vec16<bf16>::pack(o + 8 * q);
+            for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(p)[v] = Vec16<bf16>::pack(o + 8 * v);
           }
         }
       }
+      // accumulator b may be overwritten by the tile after next
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(&acc_empty[b]);
     }
   }
   fence_before();
@@ -181,7 +206,8 @@ cudaError_t tc_launch(const LaunchCtx& c, const CUtensorMap& ma, const CUtensorM
     configured = true;
   }
   const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
-  const dim3 grid(a.N / ncol, (a.M + TC_BM - 1) / TC_BM);
+  const int tiles = (a.N / ncol) * ((a.M + TC_BM - 1) / TC_BM);
+  const dim3 grid(std::min(tiles, c.num_sms));  // persistent: tiles t = blockIdx.x, + gridDim.x, ...
   return launch_k(kern, grid, dim3(TC_THREADS), TC_SMEM, c, ma, mb, a);
 }
 

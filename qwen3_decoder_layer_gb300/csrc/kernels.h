@@ -101,9 +101,10 @@ cudaError_t launch_gemm_simt(const LaunchCtx& c, int dt, int wfmt, const GemmArg
 int gemm_simt_tile_m();
 
 // Skinny GEMM for 1..64 rows (batched decode with int8 or fp32 weights):
-// out[M, N] = a[M, K] w[N, K]^T, K split over CTAs with an fp32 workspace
-// (ws: 64 x N floats, 64 x 2N for EPI_SWIGLU; counters: one per 64 output
-// columns), both zero between calls.
+// out[M, N] = a[M, K] w[N, K]^T, K split over up to 8 CTAs; each split's
+// partial tile goes to its own slice of an fp32 workspace (gemm_skinny_ws_floats
+// floats) and the last CTA of a tile sums the slices in order; counters (one
+// per 64 output columns) are zero between calls.
 struct SkinnyArgs {
   int M, N, K;
   const void* a;

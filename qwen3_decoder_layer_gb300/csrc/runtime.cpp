@@ -624,7 +624,7 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   if (!P.gemv && T <= 64) {  // skinny GEMM split-K workspace (kept zero by the kernel)
     const size_t nmax = std::max({(size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, (size_t)c.hidden,
                                   2 * (size_t)c.intermediate});
-    ENS(skws, 64 * nmax * 4, true);
+    ENS(skws, gemm_skinny_ws_floats(64, (int)nmax, EPI_STORE) * 4, false);
     ENS(skcnt, (size_t)gemm_skinny_tiles((int)nmax) * 4, true);
   }
   // attention partials: sized for the worst case of this row count when graphs replay it
