@@ -38,7 +38,38 @@ using namespace tc;
 // Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = 256.
 constexpr uint32_t kIdesc = idesc_bf16(TC_BM, TC_BN, false);
 
-template <int EPI>
+// Where tile t lives: A rows [m0, mlim) (the tile reads 128 rows from m0;
+// rows from mlim on belong to the next group or lie outside and are not
+// stored), output columns from n0, weight rows from brow (gate) / brow_up.
+struct TileInfo {
+  int m0, mlim, n0;
+  int brow, brow_up;
+};
+template <bool GROUPED>
+__device__ __forceinline__ TileInfo tile_of(const GemmTcArgs& a, int t, int tiles_m, int ncol) {
+  TileInfo ti;
+  const int mt = t % tiles_m, tn = t / tiles_m;
+  ti.n0 = tn * ncol;
+  if (!GROUPED) {
+    ti.m0 = mt * TC_BM;
+    ti.mlim = a.M;
+    ti.brow = ti.n0;
+    ti.brow_up = a.N + ti.n0;
+  } else {
+    int lo = 0, hi = a.n_groups - 1;  // last group with tile_start <= mt
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.tile_start[mid] <= mt) lo = mid; else hi = mid - 1;
+    }
+    ti.m0 = a.row_off[lo] + (mt - a.tile_start[lo]) * TC_BM;
+    ti.mlim = a.row_off[lo] + a.row_cnt[lo];
+    ti.brow = (int)(lo * a.w_group_rows) + ti.n0;
+    ti.brow_up = (int)(lo * a.w_group_rows) + a.N + ti.n0;
+  }
+  return ti;
+}
+
+template <int EPI, bool GROUPED>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    GemmTcArgs a) {
@@ -51,7 +82,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;  // output columns of a tile
-  const int tiles_m = (a.M + TC_BM - 1) / TC_BM, tiles = tiles_m * (a.N / ncol);
   const int nk = a.K / TC_BK;
   // tile t -> rows (t % tiles_m), columns (t / tiles_m): blocks running at the
   // same time share weight tiles in L2
@@ -74,25 +104,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_launch();
+  // grouped: the tile count comes from the routing scan of the previous kernel
+  const int tiles_m = GROUPED ? a.tile_start[a.n_groups] : (a.M + TC_BM - 1) / TC_BM;
+  const int tiles = tiles_m * (a.N / ncol);
 
   if (warp == 4) {
     if (lane == 0) {  // TMA producer: the k-blocks of this block's tiles, in order
       int q = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * ncol;
+        const TileInfo ti = tile_of<GROUPED>(a, t, tiles_m, ncol);
         for (int kt = 0; kt < nk; ++kt, ++q) {
           const int s = q % TC_STAGES;
           if (q >= TC_STAGES && !(ok = mbar_wait(&empty[s], (uint32_t)((q / TC_STAGES - 1) & 1), a.err, 3))) break;
           uint8_t* sa = smem + s * TC_STAGE_BYTES;
           uint8_t* sb = sa + TC_A_BYTES;
           mbar_expect_tx(&full[s], (uint32_t)TC_STAGE_BYTES);
-          tma_load_2d(sa, &map_a, kt * TC_BK, m0, &full[s]);
+          tma_load_2d(sa, &map_a, kt * TC_BK, ti.m0, &full[s]);
           if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
-            tma_load_2d(sb + TC_B_BYTES / 2, &map_b, kt * TC_BK, a.N + n0, &full[s]);
+            tma_load_2d(sb, &map_b, kt * TC_BK, ti.brow, &full[s]);
+            tma_load_2d(sb + TC_B_BYTES / 2, &map_b, kt * TC_BK, ti.brow_up, &full[s]);
           } else {
-            tma_load_2d(sb, &map_b, kt * TC_BK, n0, &full[s]);
+            tma_load_2d(sb, &map_b, kt * TC_BK, ti.brow, &full[s]);
           }
         }
       }
@@ -124,27 +157,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int i = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int b = i & 1, use = i >> 1;
-      const int m0 = (t % tiles_m) * TC_BM, n0 = (t / tiles_m) * ncol;
+      const TileInfo ti = tile_of<GROUPED>(a, t, tiles_m, ncol);
+      const int n0 = ti.n0;
       int okl = 1;  // lane 0 waits for the accumulator; the other lanes wait at the warp barrier
       if (lane == 0) okl = mbar_wait(&acc_full[b], (uint32_t)(use & 1), a.err, 5);
       __syncwarp();
       if (!__shfl_sync(0xffffffffu, okl, 0)) break;
       fence_after();
-      const int row = m0 + warp * 32 + lane;
+      const int row = ti.m0 + warp * 32 + lane;
+      const bool live = row < ti.mlim;
+      const size_t orow = !live ? 0 : (GROUPED && a.c_rows) ? (size_t)a.c_rows[row] : (size_t)row;
       const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * TC_BN);
       if (EPI == EPI_SWIGLU) {
         for (int c = 0; c < TC_BN / 2; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(tl + c, g);
           tmem_ld32(tl + TC_BN / 2 + c, u);
-          if (row < a.M) {
+          if (live) {
             float o[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const float gv = rd<bf16>(__uint_as_float(g[e])), uv = rd<bf16>(__uint_as_float(u[e]));
               o[e] = rd<bf16>(silu_f(gv)) * uv;
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(a.out) + (size_t)row * a.ldo + n0 + c);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(a.out) + orow * a.ldo + n0 + c);
 #pragma unroll
             for (int v = 0; v < 4; ++v) dst[v] = Vec16<bf16>::pack(o + 8 * v);
           }
@@ -153,8 +189,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int c = 0; c < TC_BN; c += 32) {
           uint32_t r[32];
           tmem_ld32(tl + c, r);
-          if (row < a.M) {
-            bf16* p = static_cast<bf16*>(a.out) + (size_t)row * a.ldo + n0 + c;
+          if (live) {
+            bf16* p = static_cast<bf16*>(a.out) + orow * a.ldo + n0 + c;
             float o[32];
             if (EPI == EPI_RESIDUAL) {
 #pragma unroll
@@ -196,9 +232,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return make_map_bf16(m, base, 2, dims, strides, box_rows);
 }
 
-template <int EPI>
+template <int EPI, bool GROUPED>
 cudaError_t tc_launch(const LaunchCtx& c, const CUtensorMap& ma, const CUtensorMap& mb, const GemmTcArgs& a) {
-  auto kern = gemm_tc_kernel<EPI>;
+  auto kern = gemm_tc_kernel<EPI, GROUPED>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
@@ -206,7 +242,7 @@ cudaError_t tc_launch(const LaunchCtx& c, const CUtensorMap& ma, const CUtensorM
     configured = true;
   }
   const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
-  const int tiles = (a.N / ncol) * ((a.M + TC_BM - 1) / TC_BM);
+  const int tiles = (a.N / ncol) * (GROUPED ? a.max_tiles_m : (a.M + TC_BM - 1) / TC_BM);
   const dim3 grid(std::min(tiles, c.num_sms));  // persistent: tiles t = blockIdx.x, + gridDim.x, ...
   return launch_k(kern, grid, dim3(TC_THREADS), TC_SMEM, c, ma, mb, a);
 }
@@ -227,14 +263,19 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a) {
       (a.ldo % 8))
     return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
-  const uint64_t wrows = a.epilogue == EPI_SWIGLU ? 2ull * a.N : (uint64_t)a.N;
+  const uint64_t wrows = a.tile_start ? (uint64_t)a.w_rows_total : a.epilogue == EPI_SWIGLU ? 2ull * a.N : (uint64_t)a.N;
   if (!make_map(&ma, a.a, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, TC_BM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, a.w, wrows, (uint64_t)a.K, (uint64_t)a.K, a.epilogue == EPI_SWIGLU ? TC_BN / 2 : TC_BN))
     return cudaErrorInvalidValue;
+  if (a.tile_start) {
+    if (a.epilogue == EPI_STORE) return tc_launch<EPI_STORE, true>(c, ma, mb, a);
+    if (a.epilogue == EPI_SWIGLU) return tc_launch<EPI_SWIGLU, true>(c, ma, mb, a);
+    return cudaErrorInvalidValue;
+  }
   switch (a.epilogue) {
-    case EPI_STORE: return tc_launch<EPI_STORE>(c, ma, mb, a);
-    case EPI_RESIDUAL: return tc_launch<EPI_RESIDUAL>(c, ma, mb, a);
-    case EPI_SWIGLU: return tc_launch<EPI_SWIGLU>(c, ma, mb, a);
+    case EPI_STORE: return tc_launch<EPI_STORE, false>(c, ma, mb, a);
+    case EPI_RESIDUAL: return tc_launch<EPI_RESIDUAL, false>(c, ma, mb, a);
+    case EPI_SWIGLU: return tc_launch<EPI_SWIGLU, false>(c, ma, mb, a);
   }
   return cudaErrorInvalidValue;
 }

@@ -137,6 +137,18 @@ struct GemmTcArgs {
   int ldo;
   int epilogue;
   int* err;
+  // grouped mode (tile_start != NULL): rows sorted by group; group g owns rows
+  // row_off[g] .. + row_cnt[g] of a, its weight rows start at g * w_group_rows
+  // of w, tile_start is the prefix sum of its 128-row tiles (tile_start[n_groups]
+  // = total); output row of sorted row m is c_rows[m] (NULL = m).
+  const int* tile_start;
+  const int* row_off;
+  const int* row_cnt;
+  int n_groups;
+  int max_tiles_m;       // upper bound of tile_start[n_groups] (grid size)
+  long long w_group_rows;
+  long long w_rows_total;
+  const int* c_rows;
 };
 bool gemm_tc_supported(int M, int N, int K, int epilogue);
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a);
@@ -227,6 +239,15 @@ struct MoeScatterArgs {
   int* sorted_src;  // [T k] flat (token * k + slot) of each sorted row
 };
 cudaError_t launch_moe_scatter(const LaunchCtx& c, const MoeScatterArgs& a);
+
+// Gather rows into sorted order: out[r] = x[rows[r]] (dt, row length K).
+struct MoeGatherArgs {
+  const void* x;
+  const int* rows;
+  int n, K;
+  void* out;
+};
+cudaError_t launch_moe_gather(const LaunchCtx& c, int dt, const MoeGatherArgs& a);
 
 // pend[t] = R(sum_i w[t, i] z[t k + i]) in fp32; written to `out`, or, when
 // h != NULL, added to the residual in place (h = R(h + pend)) with the row's

@@ -5,6 +5,8 @@
 // gathered, projected, and put back with the inverse permutation).
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -136,6 +138,29 @@ __global__ void moe_combine_kernel(MoeCombineArgs a) {
 cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a) {
   if (a.E > 32 * kMaxEPerLane || a.k > 32 || a.k > a.E) return cudaErrorInvalidValue;
   return launch_k(router_topk_kernel, dim3((a.T + 7) / 8), dim3(256), 0, c, a);
+}
+
+// out[r] = x[rows[r]], 16-byte vectors.
+template <typename Dt>
+__global__ void __launch_bounds__(256) moe_gather_kernel(MoeGatherArgs a) {
+  constexpr int V = Vec16<Dt>::N;
+  pdl_wait();
+  pdl_launch();
+  const int vpr = a.K / V;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)a.n * vpr;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / vpr), v = (int)(i % vpr);
+    const Dt* src = static_cast<const Dt*>(a.x) + (size_t)a.rows[r] * a.K + (size_t)v * V;
+    *reinterpret_cast<uint4*>(static_cast<Dt*>(a.out) + (size_t)r * a.K + (size_t)v * V) = ld16(src);
+  }
+}
+
+cudaError_t launch_moe_gather(const LaunchCtx& c, int dt, const MoeGatherArgs& a) {
+  const size_t vec = (size_t)a.n * a.K / (dt == DT_BF16 ? 8 : 4);
+  const int grid = (int)std::min<size_t>((vec + 255) / 256, (size_t)c.num_sms * 8);
+  if (grid < 1) return cudaSuccess;
+  if (dt == DT_BF16) return launch_k(moe_gather_kernel<bf16>, dim3(grid), dim3(256), 0, c, a);
+  return launch_k(moe_gather_kernel<float>, dim3(grid), dim3(256), 0, c, a);
 }
 
 cudaError_t launch_moe_scan(const LaunchCtx& c, const MoeScanArgs& a) {

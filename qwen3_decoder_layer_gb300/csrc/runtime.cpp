@@ -80,7 +80,7 @@ struct qwen3_handle {
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
       cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, fsync, skws,
-      skcnt;
+      skcnt, ysort;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -380,7 +380,7 @@ void qwen3_destroy(qwen3_handle* h) {
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                     &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err,
-                    &h->fsync, &h->skws, &h->skcnt};
+                    &h->fsync, &h->skws, &h->skcnt, &h->ysort};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -598,7 +598,7 @@ struct Bufs {  // raw pointers for one forward
   void *hA, *hB, *pend, *y, *qkv, *q, *attn, *m;
   float *logits, *wts, *part_o, *part_ml;
   int *idx, *counts, *row_off, *row_cnt, *tile_start, *cursor, *sorted_tok, *sorted_src, *counters, *err;
-  void *mexp, *zexp;
+  void *mexp, *zexp, *ysort;
   double* sumsq;
   int32_t* desc;
 };
@@ -650,6 +650,7 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
     ENS(sorted_src, slots * 4, false);
     ENS(mexp, slots * c.moe_intermediate * e, false);
     ENS(zexp, slots * c.hidden * e, false);
+    if (h->dt == DT_BF16 && T > 4) ENS(ysort, slots * c.hidden * e, false);  // rows in expert order (tensor-core path)
   }
   ENS(desc, P.blob.size() * 4 + 64, false);
 #undef ENS
@@ -665,6 +666,7 @@ Bufs bufs_of(qwen3_handle* h) {
   b.row_off = (int*)h->row_off.p; b.row_cnt = (int*)h->row_cnt.p; b.tile_start = (int*)h->tile_start.p;
   b.cursor = (int*)h->cursor.p; b.sorted_tok = (int*)h->sorted_tok.p; b.sorted_src = (int*)h->sorted_src.p;
   b.counters = (int*)h->counters.p; b.err = (int*)h->dev_err.p; b.mexp = h->mexp.p; b.zexp = h->zexp.p;
+  b.ysort = h->ysort.p;
   b.sumsq = (double*)h->sumsq.p; b.desc = (int32_t*)h->desc.p;
   return b;
 }
@@ -738,7 +740,10 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
     e = launch(L, "gemv_expert_down", [&] { return launch_gemv(L.ctx, dt, W_DT, d); });
     if (e != cudaSuccess) return e;
   } else {
-    const int BM = gemm_simt_tile_m();
+    // tensor-core grouped GEMMs (bf16 experts whose shapes fit the 128 x 256 tiles), else CUDA cores
+    const bool tc = h->use_tc && dt == DT_BF16 && B.ysort && mI % (128) == 0 && hid % 256 == 0 &&
+                    gemm_tc_supported(slots, mI, hid, EPI_SWIGLU) && gemm_tc_supported(slots, hid, mI, EPI_STORE);
+    const int BM = tc ? 128 : gemm_simt_tile_m();
     MoeScanArgs sc{};
     sc.counts = B.counts; sc.E = E; sc.bm = BM; sc.row_off = B.row_off; sc.row_cnt = B.row_cnt;
     sc.tile_start = B.tile_start; sc.cursor = B.cursor;
@@ -750,6 +755,26 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
     e = launch(L, "moe_scatter", [&] { return launch_moe_scatter(L.ctx, sa); });
     if (e != cudaSuccess) return e;
     const int max_tiles = (slots + BM - 1) / BM + E;
+    if (tc) {
+      MoeGatherArgs ga{};
+      ga.x = y; ga.rows = B.sorted_tok; ga.n = slots; ga.K = hid; ga.out = B.ysort;
+      e = launch(L, "moe_gather", [&] { return launch_moe_gather(L.ctx, dt, ga); });
+      if (e != cudaSuccess) return e;
+      GemmTcArgs t{};
+      t.M = slots; t.N = mI; t.K = hid; t.a = B.ysort; t.lda = hid; t.w = W.exp_gate_up; t.out = B.mexp;
+      t.ldo = mI; t.epilogue = EPI_SWIGLU; t.err = B.err; t.tile_start = B.tile_start; t.row_off = B.row_off;
+      t.row_cnt = B.row_cnt; t.n_groups = E; t.max_tiles_m = max_tiles; t.w_group_rows = 2LL * mI;
+      t.w_rows_total = 2LL * mI * E;
+      e = launch(L, "gemm_tc_expert_gate_up", [&] { return launch_gemm_tc(L.ctx, t); });
+      if (e != cudaSuccess) return e;
+      GemmTcArgs d{};
+      d.M = slots; d.N = hid; d.K = mI; d.a = B.mexp; d.lda = mI; d.w = W.exp_down; d.out = B.zexp; d.ldo = hid;
+      d.epilogue = EPI_STORE; d.err = B.err; d.tile_start = B.tile_start; d.row_off = B.row_off;
+      d.row_cnt = B.row_cnt; d.n_groups = E; d.max_tiles_m = max_tiles; d.w_group_rows = hid;
+      d.w_rows_total = (long long)hid * E; d.c_rows = B.sorted_src;
+      e = launch(L, "gemm_tc_expert_down", [&] { return launch_gemm_tc(L.ctx, d); });
+      if (e != cudaSuccess) return e;
+    } else {
     GemmArgs g{};
     g.M = slots; g.N = mI; g.K = hid; g.a = y; g.lda = hid; g.a_rows = B.sorted_tok; g.w = W.exp_gate_up;
     g.w_stride = (long long)2 * mI * hid; g.tile_start = B.tile_start; g.row_off = B.row_off;
@@ -763,6 +788,7 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
     d.max_tiles = max_tiles; d.epilogue = EPI_STORE; d.out = B.zexp; d.ldo = hid; d.c_rows = B.sorted_src;
     e = launch(L, "gemm_expert_down", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, d); });
     if (e != cudaSuccess) return e;
+    }
   }
   MoeCombineArgs cb{};
   cb.z = B.zexp; cb.w = w; cb.T = T; cb.k = k; cb.hidden = hid; cb.out = out; cb.h = h_res; cb.sumsq_out = sumsq_out;
