@@ -26,43 +26,6 @@ namespace {
 
 constexpr int SK_BN = 64, SK_BK = 32, SK_THREADS = 256, SK_MAX_SPLIT = 8;
 
-template <typename Dt, int WF>
-__device__ __forceinline__ void load_w_tile(float (*Ws)[2 * SK_BN + 4], const SkinnyArgs& a, int k0, int n0,
-                                            bool pair) {
-  // rows r of the tile: r < 64 -> weight row n0 + r; pair: r >= 64 -> up row N + n0 + r - 64
-  const int nrow = pair ? 2 * SK_BN : SK_BN;
-  constexpr int EPV = WF == W_U8 ? 16 : (int)(16 / sizeof(Dt));
-  constexpr int VPR = SK_BK / EPV;  // 16-byte vectors per tile row
-  const size_t wb = WF == W_U8 ? 1 : sizeof(Dt);
-  for (int idx = threadIdx.x; idx < nrow * VPR; idx += SK_THREADS) {
-    const int r = idx / VPR, v = idx % VPR;
-    const int n = pair ? (r < SK_BN ? n0 + r : n0 + r - SK_BN) : n0 + r;
-    const size_t row = pair && r >= SK_BN ? (size_t)a.N + n : (size_t)n;
-    float w[EPV];
-    if (n < a.N) {
-      const int k = k0 + v * EPV;
-      const uint4 q = ld_stream(static_cast<const char*>(a.w) + (row * a.K + k) * wb);
-      if (WF == W_U8) {
-        const size_t gi = row * (size_t)(a.K / a.group) + k / a.group;
-        const float s = __bfloat162float(static_cast<const bf16*>(a.scale)[gi]);
-        const float b = __bfloat162float(static_cast<const bf16*>(a.bias)[gi]);
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) w[4 * i + j] = fmaf(s, (float)((u[i] >> (8 * j)) & 0xffu), b);
-      } else {
-        Vec16<Dt>::unpack(q, w);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) w[e] = 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) Ws[v * EPV + e][r] = w[e];
-  }
-}
-
 template <typename Dt, int WF, int MT, int EPI>
 __global__ void __launch_bounds__(SK_THREADS) gemm_skinny_kernel(SkinnyArgs a) {
   constexpr bool PAIR = EPI == EPI_SWIGLU;
@@ -85,24 +48,80 @@ __global__ void __launch_bounds__(SK_THREADS) gemm_skinny_kernel(SkinnyArgs a) {
       acc[i][j] = 0.f;
       if (PAIR) acc2[PAIR ? i : 0][j] = 0.f;
     }
-  for (int kt = kt0; kt < kt1; ++kt) {
-    const int k0 = kt * SK_BK;
-    // A tile: MT rows x 64 (rows >= M are zero)
-    constexpr int AV = Vec16<Dt>::N;
-    for (int idx = tid; idx < MT * SK_BK / AV; idx += SK_THREADS) {
-      const int m = idx / (SK_BK / AV), v = idx % (SK_BK / AV);
-      float x[AV];
-      if (m < a.M) {
-        Vec16<Dt>::unpack(ld16(A + (size_t)m * a.lda + k0 + v * AV), x);
-      } else {
+  // Global -> registers for one k-tile (issued a tile ahead), registers ->
+  // shared memory (dequantised, fp32, transposed) for the current one.
+  constexpr int AV = Vec16<Dt>::N;
+  constexpr int EPV = WF == W_U8 ? 16 : (int)(16 / sizeof(Dt));
+  constexpr int VPR = SK_BK / EPV;                                  // 16-byte weight vectors per tile row
+  constexpr int NW = ((PAIR ? 2 : 1) * SK_BN * VPR + SK_THREADS - 1) / SK_THREADS;  // per thread
+  constexpr int NA = (MT * SK_BK / AV + SK_THREADS - 1) / SK_THREADS;
+  const size_t wb = WF == W_U8 ? 1 : sizeof(Dt);
+  uint4 wq[NW], aq[NA];
+  float wsc[NW], wbi[NW];
+  auto fetch = [&](int k0) {
 #pragma unroll
-        for (int e = 0; e < AV; ++e) x[e] = 0.f;
+    for (int q = 0; q < NW; ++q) {
+      const int idx = tid + q * SK_THREADS;
+      const int r = idx / VPR, v = idx % VPR;
+      const int n = PAIR ? (r < SK_BN ? n0 + r : n0 + r - SK_BN) : n0 + r;
+      wq[q] = make_uint4(0, 0, 0, 0);
+      wsc[q] = wbi[q] = 0.f;
+      if (r < (PAIR ? 2 : 1) * SK_BN && n < a.N) {
+        const size_t row = PAIR && r >= SK_BN ? (size_t)a.N + n : (size_t)n;
+        const int k = k0 + v * EPV;
+        wq[q] = ld_stream(static_cast<const char*>(a.w) + (row * a.K + k) * wb);
+        if (WF == W_U8) {
+          const size_t gi = row * (size_t)(a.K / a.group) + k / a.group;
+          wsc[q] = __bfloat162float(static_cast<const bf16*>(a.scale)[gi]);
+          wbi[q] = __bfloat162float(static_cast<const bf16*>(a.bias)[gi]);
+        }
       }
-#pragma unroll
-      for (int e = 0; e < AV; ++e) As[v * AV + e][m] = x[e];
     }
-    load_w_tile<Dt, WF>(Ws, a, k0, n0, PAIR);
+#pragma unroll
+    for (int q = 0; q < NA; ++q) {
+      const int idx = tid + q * SK_THREADS;
+      const int m = idx / (SK_BK / AV), v = idx % (SK_BK / AV);
+      aq[q] = make_uint4(0, 0, 0, 0);
+      if (idx < MT * SK_BK / AV && m < a.M) aq[q] = ld16(A + (size_t)m * a.lda + k0 + v * AV);
+    }
+  };
+  auto commit = [&]() {
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const int idx = tid + q * SK_THREADS;
+      const int r = idx / VPR, v = idx % VPR;
+      if (r < (PAIR ? 2 : 1) * SK_BN) {
+        float w[EPV];
+        if (WF == W_U8) {
+          const uint32_t u[4] = {wq[q].x, wq[q].y, wq[q].z, wq[q].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[4 * i + j] = fmaf(wsc[q], (float)((u[i] >> (8 * j)) & 0xffu), wbi[q]);
+        } else {
+          Vec16<Dt>::unpack(wq[q], w);
+        }
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) Ws[v * EPV + e][r] = w[e];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NA; ++q) {
+      const int idx = tid + q * SK_THREADS;
+      if (idx < MT * SK_BK / AV) {
+        const int m = idx / (SK_BK / AV), v = idx % (SK_BK / AV);
+        float x[AV];
+        Vec16<Dt>::unpack(aq[q], x);
+#pragma unroll
+        for (int e = 0; e < AV; ++e) As[v * AV + e][m] = x[e];
+      }
+    }
+  };
+  if (kt0 < kt1) fetch(kt0 * SK_BK);
+  for (int kt = kt0; kt < kt1; ++kt) {
+    commit();
     __syncthreads();
+    if (kt + 1 < kt1) fetch((kt + 1) * SK_BK);  // in flight during this tile's FMAs
 #pragma unroll 8
     for (int kk = 0; kk < SK_BK; ++kk) {
       float ar[TM];
