@@ -6,7 +6,9 @@
 //
 // Used for the MoE router logits and the gathered (unsorted) expert
 // projections of few rows: each warp streams whole weight rows with 16-byte
-// non-allocating loads while the input rows sit in shared memory as fp32.
+// non-allocating loads while the input rows sit in shared memory in the model
+// dtype (each lane reads its x elements as contiguous 16-byte vectors, free of
+// bank conflicts).
 // Before waiting on the producer kernel, every block asks L2 to prefetch its
 // weight rows (shared-weight mode).  Epilogues fuse rounding, fp32 output,
 // the residual add and SiLU * up.
@@ -46,27 +48,21 @@ template <typename Dt> struct WTraits<Dt, W_U8> {
   }
 };
 
-// Stage the input rows as fp32 in shared memory (16-byte vector loads).
+// Stage the input rows in shared memory in the model dtype (16-byte copies).
 template <typename Dt>
-__device__ void stage_x(const GemvArgs& a, float* xs) {
+__device__ void stage_x(const GemvArgs& a, Dt* xs) {
   constexpr int V = Vec16<Dt>::N;
-  const int K = a.K;
-  for (int t = 0; t < a.x_rows; ++t) {
-    float* xt = xs + (size_t)t * K;
-    const Dt* x = static_cast<const Dt*>(a.x) + (size_t)t * K;
-    for (int k = threadIdx.x * V; k < K; k += blockDim.x * V) {
-      float v[V];
-      Vec16<Dt>::unpack(ld16(x + k), v);
-#pragma unroll
-      for (int e = 0; e < V; ++e) xt[k + e] = v[e];
-    }
-  }
+  const Dt* x = static_cast<const Dt*>(a.x);
+  for (int c = threadIdx.x; c < a.x_rows * a.K / V; c += blockDim.x)
+    *reinterpret_cast<uint4*>(xs + (size_t)c * V) = ld16(x + (size_t)c * V);
 }
 
 template <typename Dt, int WF, int NT, int EPI>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
-  extern __shared__ float xs[];
+  extern __shared__ __align__(16) uint8_t gv_smem[];
+  Dt* xs = reinterpret_cast<Dt*>(gv_smem);
   using W = WTraits<Dt, WF>;
+  constexpr int XV = Vec16<Dt>::N;  // x elements per 16-byte vector
   constexpr bool PAIR = (EPI == EPI_SWIGLU);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool gather = a.slot_expert != nullptr;
@@ -100,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
     }
     const char* r0 = base + row * row_bytes;
     const char* r1 = base + (row + a.N) * row_bytes;
-    const float* xrow = xs + (size_t)(gather ? b / a.slot_div : 0) * a.K;
+    const Dt* xrow = xs + (size_t)(gather ? b / a.slot_div : 0) * a.K;
     float acc[NT], acc2[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = acc2[t] = 0.f;
@@ -119,22 +115,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
         const int v = v0 + 32 * i;
         if (v >= nvec) break;
         const int k0 = v * W::EPV;
-        float w0[W::EPV];
+        float w0[W::EPV], w1[W::EPV];
         W::get(q0[i], w0, a, row, k0);
+        if (PAIR) W::get(q1[i], w1, a, row + a.N, k0);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const float* xp = xrow + (size_t)t * a.K + k0;
+          float xv[W::EPV];
 #pragma unroll
-          for (int e = 0; e < W::EPV; ++e) acc[t] = fmaf(w0[e], xp[e], acc[t]);
-        }
-        if (PAIR) {
-          float w1[W::EPV];
-          W::get(q1[i], w1, a, row + a.N, k0);
+          for (int q = 0; q < W::EPV / XV; ++q)
+            Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(xrow + (size_t)t * a.K + k0 + q * XV), xv + q * XV);
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const float* xp = xrow + (size_t)t * a.K + k0;
+          for (int e = 0; e < W::EPV; ++e) acc[t] = fmaf(w0[e], xv[e], acc[t]);
+          if (PAIR) {
 #pragma unroll
-            for (int e = 0; e < W::EPV; ++e) acc2[t] = fmaf(w1[e], xp[e], acc2[t]);
+            for (int e = 0; e < W::EPV; ++e) acc2[t] = fmaf(w1[e], xv[e], acc2[t]);
           }
         }
       }

@@ -251,7 +251,7 @@ cudaError_t launch_moe_gather(const LaunchCtx& c, int dt, const MoeGatherArgs& a
 
 // pend[t] = R(sum_i w[t, i] z[t k + i]) in fp32; written to `out`, or, when
 // h != NULL, added to the residual in place (h = R(h + pend)) with the row's
-// sum of squares stored to sumsq_out[t].
+// sum of squares added to sumsq_out[t] (which must be zero beforehand).
 struct MoeCombineArgs {
   const void* z;
   const float* w;

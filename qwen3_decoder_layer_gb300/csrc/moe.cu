@@ -104,32 +104,34 @@ __global__ void moe_scatter_kernel(MoeScatterArgs a) {
   a.sorted_src[pos] = f;
 }
 
+// One thread per output element (blocks tile the row); with the residual add,
+// each block adds its share of the row's sum of squares (fp64 atomic; the
+// slot is zero at the start of the step).
 template <typename Dt>
-__global__ void moe_combine_kernel(MoeCombineArgs a) {
+__global__ void __launch_bounds__(256) moe_combine_kernel(MoeCombineArgs a) {
   __shared__ float red[64];
   pdl_wait();
   pdl_launch();
-  const int t = blockIdx.x;
+  const int t = blockIdx.y, n = blockIdx.x * blockDim.x + threadIdx.x;
   const Dt* z = static_cast<const Dt*>(a.z) + (size_t)t * a.k * a.hidden;
   const float* w = a.w + (size_t)t * a.k;
-  Dt* out = a.out ? static_cast<Dt*>(a.out) + (size_t)t * a.hidden : nullptr;
-  Dt* h = a.h ? static_cast<Dt*>(a.h) + (size_t)t * a.hidden : nullptr;
   F2 ss = {0.f, 0.f};
-  for (int n = threadIdx.x; n < a.hidden; n += blockDim.x) {
+  if (n < a.hidden) {
     float acc = 0.f;
     for (int i = 0; i < a.k; ++i) acc = fmaf(w[i], to_f(z[(size_t)i * a.hidden + n]), acc);
     const float pend = rd<Dt>(acc);
-    if (h) {
+    if (a.h) {
+      Dt* h = static_cast<Dt*>(a.h) + (size_t)t * a.hidden;
       const float hn = rd<Dt>(to_f(h[n]) + pend);
       h[n] = from_f<Dt>(hn);
       f2_add_sq(ss, hn);
     } else {
-      out[n] = from_f<Dt>(pend);
+      static_cast<Dt*>(a.out)[(size_t)t * a.hidden + n] = from_f<Dt>(pend);
     }
   }
-  if (h) {
+  if (a.h) {
     ss = f2_block_sum(ss, red);
-    if (threadIdx.x == 0) a.sumsq_out[t] = (double)ss.hi + (double)ss.lo;
+    if (threadIdx.x == 0) atomicAdd(a.sumsq_out + t, (double)ss.hi + (double)ss.lo);
   }
 }
 
@@ -173,8 +175,9 @@ cudaError_t launch_moe_scatter(const LaunchCtx& c, const MoeScatterArgs& a) {
 }
 
 cudaError_t launch_moe_combine(const LaunchCtx& c, int dt, const MoeCombineArgs& a) {
-  if (dt == DT_BF16) return launch_k(moe_combine_kernel<bf16>, dim3(a.T), dim3(256), 0, c, a);
-  return launch_k(moe_combine_kernel<float>, dim3(a.T), dim3(256), 0, c, a);
+  const dim3 grid((a.hidden + 255) / 256, a.T);
+  if (dt == DT_BF16) return launch_k(moe_combine_kernel<bf16>, grid, dim3(256), 0, c, a);
+  return launch_k(moe_combine_kernel<float>, grid, dim3(256), 0, c, a);
 }
 
 }  // namespace q3

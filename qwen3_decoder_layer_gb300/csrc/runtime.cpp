@@ -697,7 +697,7 @@ qwen3_status upload_plan(qwen3_handle* h, const Plan& P, cudaStream_t s) {
 
 // MoE block on y [T, hidden].  The weighted expert sum goes to `out`, or,
 // when h_res is given, is added to the residual h_res in place with the
-// rows' sums of squares stored to sumsq_out.  idx/w receive the routing.
+// rows' sums of squares added to sumsq_out (zero beforehand).  idx/w receive the routing.
 cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, int T, void* out, void* h_res,
                       double* sumsq_out, int* idx, float* w, const Bufs& B) {
   const qwen3_config& c = h->cfg;
