@@ -87,6 +87,79 @@ __device__ __forceinline__ ItemKeys item_keys(const AttnItem& item, const AttnQB
   return r;
 }
 
+// The last block to finish a (query block, kv head) combines its nc chunk
+// partials: M = max m_c, out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c,
+// rounded once to the model dtype.  Every partial is first loaded into
+// shared memory in one pass of independent loads (m, l into wp; o into
+// `ostage` when given, which must hold nc * nq * D floats), so that the
+// combine costs one round trip to L2 rather than one per chunk.
+template <typename Dt, int D, int NQ>
+__device__ void combine_parts(const AttnDecArgs& a, const AttnQBlock& qb, int j, int nc, int nq, int G, float* wp,
+                              float* mrg, float* ostage) {
+  using LY = ADLayout<Dt, D, NQ>;
+  constexpr int MP = LY::MPITCH;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t pbase = (size_t)qb.part_base * a.KV + j;  // partial of chunk c: (pbase + c * KV) * nq_max
+  auto pidx = [&](int c, int i) { return (pbase + (size_t)c * a.KV) * a.nq_max + i; };
+  const bool staged = 2 * (size_t)nc * nq <= LY::WP_FLOATS;
+  float* fm = wp;            // [c][i]: chunk maxima, then their weights e^(m_c - M_i)
+  float* fl = wp + nc * nq;  // [c][i]: chunk normalisers
+  __threadfence();
+  if (staged) {
+    for (int idx = tid; idx < nc * nq; idx += AD_CTHREADS) {
+      const int c = idx / nq, i = idx % nq;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + pidx(c, i));
+      fm[idx] = ml.x;
+      fl[idx] = ml.y;
+    }
+  }
+  if (ostage) {
+    const int per = nq * D / 4;  // float4 per chunk (queries of one chunk are contiguous)
+    for (int idx = tid; idx < nc * per; idx += AD_CTHREADS) {
+      const int c = idx / per, r = idx - c * per;
+      reinterpret_cast<float4*>(ostage)[idx] = __ldcg(reinterpret_cast<const float4*>(a.part_o + pidx(c, 0) * D) + r);
+    }
+  }
+  csync();
+  // per-query max and normaliser (warp per query, lanes over chunks)
+  for (int i = warp; i < nq; i += AD_CWARPS) {
+    auto mval = [&](int c) { return staged ? fm[c * nq + i] : __ldcg(a.part_ml + pidx(c, i) * 2); };
+    auto lval = [&](int c) { return staged ? fl[c * nq + i] : __ldcg(a.part_ml + pidx(c, i) * 2 + 1); };
+    float M = -CUDART_INF_F;
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, mval(c));
+    M = warp_max(M);
+    float Lsum = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+      const float m = mval(c);
+      const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+      Lsum = fmaf(lval(c), f, Lsum);
+      if (staged) fm[c * nq + i] = f;
+    }
+    Lsum = warp_sum(Lsum);
+    if (lane == 0) { mrg[i * MP + AD_CWARPS] = M; mrg[i * MP + AD_CWARPS + 1] = Lsum; }
+  }
+  csync();
+  // out[i][d] = sum_c f[c][i] o_c[i][d] / L_i, one thread per output element
+  for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
+    const int i = idx / D, d = idx % D;
+    const float M = mrg[i * MP + AD_CWARPS];
+    float v = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < nc; ++c) {
+      float f;
+      if (staged) {
+        f = fm[c * nq + i];
+      } else {
+        const float m = __ldcg(a.part_ml + pidx(c, i) * 2);
+        f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+      }
+      v = fmaf(ostage ? ostage[(size_t)c * nq * D + idx] : __ldcg(a.part_o + pidx(c, i) * D + d), f, v);
+    }
+    const int row = qb.row0 + i / G, head = j * G + i % G;
+    static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / mrg[i * MP + AD_CWARPS + 1]);
+  }
+}
+
 template <typename Dt, int D, int NQ>
 __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs a) {
   extern __shared__ __align__(128) uint8_t ad_smem[];
@@ -200,7 +273,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
 
   // merge the warps' states of the run over query block b into its partial;
   // the last run of b combines
-  auto flush = [&](int b) {
+  auto flush = [&](int b, bool last) {
     const AttnQBlock qb = a.qblocks[b];
     const int nq = qb.nrows * G;
     float* mine = wp + (size_t)warp * NQ * WP;
@@ -252,55 +325,10 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
     }
     csync();
     if (s_flag) {
-      __threadfence();
       const int nc = s_run[1];
-      const size_t pbase = (size_t)qb.part_base * a.KV + j;  // partial of run c: (pbase + c * KV) * nq_max
-      const bool staged = (size_t)nc * nq <= LY::WP_FLOATS;
-      float* fs = wp;  // [c][i]: run maxima, then their weights e^(m_c - M_i)
-      if (staged) {
-        for (int idx = tid; idx < nc * nq; idx += AD_CTHREADS) {
-          const int c = idx / nq, i = idx % nq;
-          fs[idx] = __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
-        }
-        csync();
-      }
-      for (int i = warp; i < nq; i += AD_CWARPS) {
-        auto mval = [&](int c) {
-          return staged ? fs[c * nq + i] : __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
-        };
-        float M = -CUDART_INF_F;
-        for (int c = lane; c < nc; c += 32) M = fmaxf(M, mval(c));
-        M = warp_max(M);
-        float Lsum = 0.f;
-        for (int c = lane; c < nc; c += 32) {
-          const float m = mval(c);
-          const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
-          Lsum = fmaf(__ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2 + 1), f, Lsum);
-          if (staged) fs[c * nq + i] = f;
-        }
-        Lsum = warp_sum(Lsum);
-        if (lane == 0) { mrg[i * MP + AD_CWARPS] = M; mrg[i * MP + AD_CWARPS + 1] = Lsum; }
-      }
-      csync();
-      for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
-        const int i = idx / D, d = idx % D;
-        const float M = mrg[i * MP + AD_CWARPS];
-        float v = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < nc; ++c) {
-          const size_t p = (pbase + (size_t)c * a.KV) * a.nq_max + i;
-          float f;
-          if (staged) {
-            f = fs[c * nq + i];
-          } else {
-            const float m = __ldcg(a.part_ml + p * 2);
-            f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
-          }
-          v = fmaf(__ldcg(a.part_o + p * D + d), f, v);
-        }
-        const int row = qb.row0 + i / G, head = j * G + i % G;
-        static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / mrg[i * MP + AD_CWARPS + 1]);
-      }
+      // the ring is idle once this block's last run is flushed
+      const bool os = last && (size_t)nc * nq * D <= AD_STAGES * LY::STAGE / 4;
+      combine_parts<Dt, D, NQ>(a, qb, j, nc, nq, G, wp, mrg, os ? reinterpret_cast<float*>(ad_smem) : nullptr);
       if (tid == 0) a.counters[(size_t)b * a.KV + j] = 0;
     }
     csync();
@@ -314,7 +342,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
     const int nq = qb.nrows * G;  // <= NQ
     if (item.qb != cur) {
       if (cur >= 0) {
-        flush(cur);
+        flush(cur, false);
         if (s_fail) break;
         reset_state();
       }
@@ -459,7 +487,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
     }
     g += ik.nsub;
   }
-  if (cur >= 0 && !s_fail) flush(cur);
+  if (cur >= 0 && !s_fail) flush(cur, true);
 }
 
 // One item per block and step of the persistent loop (used when the grid has
@@ -717,57 +745,10 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
     }
     csync();
     if (s_flag) {
-      __threadfence();
       const int nc = qb.n_chunks;
-      const size_t pbase = (size_t)qb.part_base * a.KV + j;  // partial of chunk c: (pbase + c * KV) * nq_max
-      const bool staged = (size_t)nc * nq <= LY::WP_FLOATS;
-      float* fs = wp;  // [c][i]: chunk maxima, then their weights e^(m_c - M_i)
-      if (staged) {
-        for (int idx = tid; idx < nc * nq; idx += AD_CTHREADS) {
-          const int c = idx / nq, i = idx % nq;
-          fs[idx] = __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
-        }
-        csync();
-      }
-      // per-query max and normaliser (warp per query, lanes over chunks)
-      for (int i = warp; i < nq; i += AD_CWARPS) {
-        auto mval = [&](int c) {
-          return staged ? fs[c * nq + i] : __ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2);
-        };
-        float M = -CUDART_INF_F;
-        for (int c = lane; c < nc; c += 32) M = fmaxf(M, mval(c));
-        M = warp_max(M);
-        float Lsum = 0.f;
-        for (int c = lane; c < nc; c += 32) {
-          const float m = mval(c);
-          const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
-          Lsum = fmaf(__ldcg(a.part_ml + ((pbase + (size_t)c * a.KV) * a.nq_max + i) * 2 + 1), f, Lsum);
-          if (staged) fs[c * nq + i] = f;
-        }
-        Lsum = warp_sum(Lsum);
-        if (lane == 0) { mrg[i * MP + AD_CWARPS] = M; mrg[i * MP + AD_CWARPS + 1] = Lsum; }
-      }
-      csync();
-      // out[i][d] = sum_c f[c][i] o_c[i][d] / L_i, one thread per output element
-      for (int idx = tid; idx < nq * D; idx += AD_CTHREADS) {
-        const int i = idx / D, d = idx % D;
-        const float M = mrg[i * MP + AD_CWARPS];
-        float v = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < nc; ++c) {
-          const size_t p = (pbase + (size_t)c * a.KV) * a.nq_max + i;
-          float f;
-          if (staged) {
-            f = fs[c * nq + i];
-          } else {
-            const float m = __ldcg(a.part_ml + p * 2);
-            f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
-          }
-          v = fmaf(__ldcg(a.part_o + p * D + d), f, v);
-        }
-        const int row = qb.row0 + i / G, head = j * G + i % G;
-        static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / mrg[i * MP + AD_CWARPS + 1]);
-      }
+      // the ring is idle once this block's last item has been consumed
+      const bool os = it + (int)gridDim.x >= n_items && (size_t)nc * nq * D <= AD_STAGES * LY::STAGE / 4;
+      combine_parts<Dt, D, NQ>(a, qb, j, nc, nq, G, wp, mrg, os ? reinterpret_cast<float*>(ad_smem) : nullptr);
       if (tid == 0) a.counters[(size_t)item.qb * a.KV + j] = 0;
     }
     csync();
