@@ -87,6 +87,162 @@ __device__ __forceinline__ ItemKeys item_keys(const AttnItem& item, const AttnQB
   return r;
 }
 
+// Sum over the LPK lanes of a key group of each lane's NS per-step partial
+// dot products, as a reduce-scatter: at each halving the lane pair keeps
+// opposite halves of its remaining steps and adds the partner's copy, so
+// NS - 1 shuffles leave each lane the full sum of step sub_l / (LPK / NS);
+// the lanes that share that step then add among themselves.
+template <int NS, int LPK>
+__device__ __forceinline__ float rs_sum(float (&v)[NS], int sub_l) {
+#pragma unroll
+  for (int c = NS, h = LPK / 2; c > 1; c >>= 1, h >>= 1) {
+    const bool up = (sub_l & h) != 0;
+#pragma unroll
+    for (int k = 0; k < c / 2; ++k) {
+      const float send = up ? v[k] : v[k + c / 2];
+      const float keep = up ? v[k + c / 2] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int h = LPK / (2 * NS); h >= 1; h >>= 1) r += __shfl_xor_sync(0xffffffffu, r, h);
+  return r;
+}
+
+// A warp's nk keys (rows of Kt, first absolute position kb) against the nq
+// staged queries: scores (scaled, causally masked at pos0 + i / G), folded
+// into the warp's running softmax state (m, l and o rescaled) and left as
+// probabilities in ps[i * KW + u] for the P.V pass.  LPK lanes share a key
+// (EPV elements each), KPS keys per step.  Up to four queries: every lane
+// keeps its partial dot product of each step and the partials are summed
+// across the key group once, after the last step (rs_sum); the queries sit
+// in registers when there are at most two.  Eight queries: one butterfly per
+// (step, query), the registers being needed for the state.
+template <typename Dt, int D, int NQ, int KW>
+__device__ __forceinline__ void warp_scores_softmax(const Dt* Kt, const float* qs, float* ps, int nk, int nq, int kb,
+                                                    int pos0, int G, float scale, float (&m_w)[NQ], float (&l_w)[NQ],
+                                                    float (&o_w)[NQ][D / 32]) {
+  constexpr int EPV = 16 / sizeof(Dt);
+  constexpr int LPK = D / EPV;
+  constexpr int KPS = 32 / LPK;
+  constexpr int NS = KW / KPS;
+  constexpr int DPL = D / 32;
+  const int lane = threadIdx.x & 31, sub_l = lane % LPK, kq = lane / LPK;
+  if constexpr (NQ <= 4) {
+    static_assert(NS <= LPK && (NS & (NS - 1)) == 0, "steps per key group");
+    constexpr bool QREG = NQ <= 2;
+    float qr[QREG ? NQ : 1][EPV];
+    if constexpr (QREG) {
+#pragma unroll
+      for (int i = 0; i < NQ; ++i)
+#pragma unroll
+        for (int e = 0; e < EPV / 4; ++e) {
+          const float4 q4 = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV)[e];
+          qr[i][4 * e] = q4.x; qr[i][4 * e + 1] = q4.y; qr[i][4 * e + 2] = q4.z; qr[i][4 * e + 3] = q4.w;
+        }
+    }
+    float dp[NQ][NS];
+#pragma unroll
+    for (int st = 0; st < NS; ++st) {
+      const int u = st * KPS + kq;
+      float kv[EPV];
+      if (u < nk) {
+        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPV / 4; ++e) {
+          float4 q4;
+          if constexpr (QREG) {
+            q4 = make_float4(qr[i][4 * e], qr[i][4 * e + 1], qr[i][4 * e + 2], qr[i][4 * e + 3]);
+          } else {
+            q4 = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV)[e];
+          }
+          d0 = fmaf(q4.x, kv[4 * e], d0);
+          d1 = fmaf(q4.y, kv[4 * e + 1], d1);
+          d0 = fmaf(q4.z, kv[4 * e + 2], d0);
+          d1 = fmaf(q4.w, kv[4 * e + 3], d1);
+        }
+        dp[i][st] = d0 + d1;
+      }
+    }
+    // lane (kq, sub_l) now reduces to the score of key u; LPK / NS lanes hold each key
+    const int u = (sub_l / (LPK / NS)) * KPS + kq;
+    const bool first = (sub_l % (LPK / NS)) == 0;
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      float sv = rs_sum<NS, LPK>(dp[i], sub_l);
+      sv = (u < nk && i < nq && kb + u <= pos0 + i / G) ? sv * scale : -CUDART_INF_F;
+      const float m_new = fmaxf(m_w[i], warp_max(sv));
+      const float p = (sv == -CUDART_INF_F) ? 0.f : expf(sv - m_new);
+      const float alpha = (m_w[i] == -CUDART_INF_F) ? 0.f : expf(m_w[i] - m_new);
+      const float ls = warp_sum(first ? p : 0.f);
+      if (first) ps[i * KW + u] = p;
+      if (m_new != -CUDART_INF_F) {
+        l_w[i] = fmaf(l_w[i], alpha, ls);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o_w[i][e] *= alpha;
+        m_w[i] = m_new;
+      }
+    }
+    __syncwarp();
+  } else {
+#pragma unroll
+    for (int st = 0; st < NS; ++st) {
+      const int u = st * KPS + kq;
+      float kv[EPV];
+      if (u < nk) {
+        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        const float4* qp = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV);
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPV / 4; ++e) {
+          const float4 q4 = qp[e];
+          d0 = fmaf(q4.x, kv[4 * e], d0);
+          d1 = fmaf(q4.y, kv[4 * e + 1], d1);
+          d0 = fmaf(q4.z, kv[4 * e + 2], d0);
+          d1 = fmaf(q4.w, kv[4 * e + 3], d1);
+        }
+        float d = d0 + d1;
+#pragma unroll
+        for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        if (sub_l == 0) ps[i * KW + u] = (u < nk && i < nq && kb + u <= pos0 + i / G) ? d * scale : -CUDART_INF_F;
+      }
+    }
+    __syncwarp();
+    // online softmax update of the warp's running state (lanes over keys)
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      const float sv = lane < KW ? ps[i * KW + lane] : -CUDART_INF_F;
+      const float mx = warp_max(sv);
+      const float m_new = fmaxf(m_w[i], mx);
+      const float p = (sv == -CUDART_INF_F) ? 0.f : expf(sv - m_new);
+      const float alpha = (m_w[i] == -CUDART_INF_F) ? 0.f : expf(m_w[i] - m_new);
+      const float ls = warp_sum(p);
+      if (lane < KW) ps[i * KW + lane] = p;
+      if (m_new != -CUDART_INF_F) {
+        l_w[i] = fmaf(l_w[i], alpha, ls);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o_w[i][e] *= alpha;
+        m_w[i] = m_new;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // The last block to finish a (query block, kv head) combines its nc chunk
 // partials: M = max m_c, out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c,
 // rounded once to the model dtype.  Every partial is first loaded into
@@ -166,9 +322,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
   constexpr int KW = LY::KW;            // keys per warp
-  constexpr int EPV = 16 / sizeof(Dt);  // elements per 16-byte vector
-  constexpr int LPK = D / EPV;          // lanes per key in the score loop
-  constexpr int KPS = 32 / LPK;         // keys per score step
   constexpr int DPL = D / 32;           // head elements per lane
   constexpr int WP = LY::WPITCH;
   constexpr int MP = LY::MPITCH;
@@ -418,56 +571,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           }
         }
         __syncwarp();
-        // scores: LPK lanes per key, KPS keys per step
-        const int sub_l = lane % LPK, kq = lane / LPK;
-#pragma unroll
-        for (int st = 0; st < KW / KPS; ++st) {
-          const int u = st * KPS + kq;
-          float kv[EPV];
-          if (u < nk) {
-            Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
-          } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) {
-            const float4* qp = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV);
-            float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPV / 4; ++e) {
-              const float4 q4 = qp[e];
-              d0 = fmaf(q4.x, kv[4 * e], d0);
-              d1 = fmaf(q4.y, kv[4 * e + 1], d1);
-              d0 = fmaf(q4.z, kv[4 * e + 2], d0);
-              d1 = fmaf(q4.w, kv[4 * e + 3], d1);
-            }
-            float d = d0 + d1;
-#pragma unroll
-            for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            if (sub_l == 0)
-              ps[i * KW + u] = (u < nk && i < nq && kb + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
-          }
-        }
-        __syncwarp();
-        // online softmax update of the warp's running state (lanes over keys)
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-          const float sv = lane < KW ? ps[i * KW + lane] : -CUDART_INF_F;
-          const float mx = warp_max(sv);
-          const float m_new = fmaxf(m_w[i], mx);
-          const float p = (sv == -CUDART_INF_F) ? 0.f : expf(sv - m_new);
-          const float alpha = (m_w[i] == -CUDART_INF_F) ? 0.f : expf(m_w[i] - m_new);
-          const float ls = warp_sum(p);
-          if (lane < KW) ps[i * KW + lane] = p;
-          if (m_new != -CUDART_INF_F) {
-            l_w[i] = fmaf(l_w[i], alpha, ls);
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o_w[i][e] *= alpha;
-            m_w[i] = m_new;
-          }
-        }
-        __syncwarp();
+        warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale, m_w, l_w, o_w);
         // P.V: lane holds head elements lane*DPL .. +DPL
 #pragma unroll 4
         for (int u = 0; u < nk; ++u) {
@@ -499,9 +603,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
   constexpr int KW = LY::KW;            // keys per warp
-  constexpr int EPV = 16 / sizeof(Dt);  // elements per 16-byte vector
-  constexpr int LPK = D / EPV;          // lanes per key in the score loop
-  constexpr int KPS = 32 / LPK;         // keys per score step
   constexpr int DPL = D / 32;           // head elements per lane
   constexpr int WP = LY::WPITCH;
   constexpr int MP = LY::MPITCH;
@@ -642,50 +743,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
           }
         }
         __syncwarp();
-        // scores: LPK lanes per key, KPS keys per step
-        const int sub_l = lane % LPK, kq = lane / LPK;
-#pragma unroll
-        for (int st = 0; st < KW / KPS; ++st) {
-          const int u = st * KPS + kq;
-          float kv[EPV];
-          if (u < nk) {
-            Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
-          } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) {
-            const float4* qp = reinterpret_cast<const float4*>(qs + i * D + sub_l * EPV);
-            float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPV / 4; ++e) {
-              const float4 q4 = qp[e];
-              d0 = fmaf(q4.x, kv[4 * e], d0);
-              d1 = fmaf(q4.y, kv[4 * e + 1], d1);
-              d0 = fmaf(q4.z, kv[4 * e + 2], d0);
-              d1 = fmaf(q4.w, kv[4 * e + 3], d1);
-            }
-            float d = d0 + d1;
-#pragma unroll
-            for (int off = LPK / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            if (sub_l == 0)
-              ps[i * KW + u] = (u < nk && i < nq && kb + u <= qb.pos0 + i / G) ? d * a.scale : -CUDART_INF_F;
-          }
-        }
-        __syncwarp();
-        // warp-local softmax over the warp's keys (lanes over keys)
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-          const float sv = lane < KW ? ps[i * KW + lane] : -CUDART_INF_F;
-          const float m = warp_max(sv);
-          const float p = (sv == -CUDART_INF_F) ? 0.f : expf(sv - m);
-          const float l = warp_sum(p);
-          if (lane < KW) ps[i * KW + lane] = p;
-          m_w[i] = m;
-          l_w[i] = l;
-        }
-        __syncwarp();
+        warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale, m_w, l_w, o_w);
         // P.V: lane holds head elements lane*DPL .. +DPL
 #pragma unroll 4
         for (int u = 0; u < nk; ++u) {
