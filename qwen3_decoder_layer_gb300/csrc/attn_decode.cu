@@ -44,7 +44,7 @@ constexpr int AD_CTHREADS = AD_CWARPS * 32;      // 512
 constexpr int AD_THREADS = AD_CTHREADS + 32;     // + producer warp
 constexpr int AD_NQ_MAX = 8;
 constexpr int AD_SUBS = 4;                       // sub-chunks per item
-constexpr int AD_STAGES = AD_SUBS;               // the ring holds one item
+constexpr int AD_STAGES_MAX = 6;                 // ring stages (one sub-chunk each), at most
 constexpr int AD_WPS = AD_CWARPS / AD_SUBS;      // warps per sub-chunk
 
 template <typename Dt> struct ADT {
@@ -56,7 +56,10 @@ template <typename Dt, int D, int NQ> struct ADLayout {
   static constexpr int KW = CK / AD_WPS;  // keys per warp
   static constexpr size_t TILE = (size_t)CK * D * sizeof(Dt);
   static constexpr size_t STAGE = 2 * TILE;
-  static constexpr size_t OFF_QS = AD_STAGES * STAGE;                             // [NQ][D] queries
+  // ring stages: one item (AD_SUBS stages), plus two when shared memory
+  // allows, so that a block's next item streams in while this one computes
+  static constexpr int STAGES = NQ <= 2 ? AD_STAGES_MAX : AD_SUBS;
+  static constexpr size_t OFF_QS = STAGES * STAGE;                                // [NQ][D] queries
   static constexpr size_t OFF_PS = OFF_QS + (size_t)NQ * D * 4;                   // [warp][NQ][KW] scores / p
   static constexpr int WPITCH = D + 4;                                            // o[D], m, l, pad
   static constexpr size_t OFF_WP = OFF_PS + (size_t)AD_CWARPS * NQ * KW * 4;      // [warp][NQ][WPITCH] partials
@@ -64,7 +67,7 @@ template <typename Dt, int D, int NQ> struct ADLayout {
   static constexpr int MPITCH = AD_CWARPS + 2;                                    // weights of the warps, M, L
   static constexpr size_t OFF_MRG = OFF_WP + WP_FLOATS * 4;                       // [NQ][MPITCH] merge scratch
   static constexpr size_t OFF_BAR = (OFF_MRG + (size_t)NQ * MPITCH * 4 + 15) & ~size_t(15);
-  static constexpr size_t TOTAL = OFF_BAR + 2 * AD_STAGES * 8 + 16;
+  static constexpr size_t TOTAL = OFF_BAR + 2 * STAGES * 8 + 16;
 };
 
 // Named barrier over the consumer warps only.
@@ -330,9 +333,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   float* wp = reinterpret_cast<float*>(ad_smem + LY::OFF_WP);
   float* mrg = reinterpret_cast<float*>(ad_smem + LY::OFF_MRG);
   uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
-  uint64_t* empty = full + AD_STAGES;
+  uint64_t* empty = full + LY::STAGES;
   __shared__ int s_flag, s_fail;
-  __shared__ int s_issued[AD_STAGES];  // uses of each stage issued so far
+  __shared__ int s_issued[AD_STAGES_MAX];  // uses of each stage issued so far
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.y;
   const int G = a.H / a.KV;
@@ -341,14 +344,14 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   auto tiles = [&](int s) { return ad_smem + (size_t)s * LY::STAGE; };
 
   if (tid == 0) {
-    for (int s = 0; s < AD_STAGES; ++s) {
+    for (int s = 0; s < LY::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], AD_WPS);
     }
     mbar_fence_init();
     s_fail = 0;
   }
-  if (tid < AD_STAGES) s_issued[tid] = 0;
+  if (tid < LY::STAGES) s_issued[tid] = 0;
   __syncthreads();
 
   if (warp == AD_CWARPS) {
@@ -367,8 +370,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
         const AttnQBlock qb = a.qblocks[item.qb];
         const ItemKeys ik = item_keys<Dt>(item, qb);
         for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
-          const int s = g % AD_STAGES;
-          if (g >= AD_STAGES && !mbar_wait(&empty[s], (uint32_t)((g / AD_STAGES - 1) & 1), a.err, 2)) {
+          const int s = g % LY::STAGES;
+          if (g >= LY::STAGES && !mbar_wait(&empty[s], (uint32_t)((g / LY::STAGES - 1) & 1), a.err, 2)) {
             s_fail = 1;
             return;
           }
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           mbar_expect_tx(&full[s], 2 * bytes);
           tma_load_1d(tiles(s), kc + off, bytes, &full[s]);
           tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
-          *(volatile int*)&s_issued[s] = g / AD_STAGES + 1;
+          *(volatile int*)&s_issued[s] = g / LY::STAGES + 1;
         }
       }
       // L2 prefetch of this block's share of the next kernel's operand
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
     if (s_flag) {
       const int nc = s_run[1];
       // the ring is idle once this block's last run is flushed
-      const bool os = last && (size_t)nc * nq * D <= AD_STAGES * LY::STAGE / 4;
+      const bool os = last && (size_t)nc * nq * D <= LY::STAGES * LY::STAGE / 4;
       combine_parts<Dt, D, NQ>(a, qb, j, nc, nq, G, wp, mrg, os ? reinterpret_cast<float*>(ad_smem) : nullptr);
       if (tid == 0) a.counters[(size_t)b * a.KV + j] = 0;
     }
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
 
     // ---- this warp's keys of the item, folded into its running state
     if (wsub < ik.nsub) {
-      const int s = (g + wsub) % AD_STAGES;
+      const int s = (g + wsub) % LY::STAGES;
       const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
       const int nk = min(KW, ik.key0 + ik.nkeys - key0 - wk0);  // this warp's keys (may be <= 0)
       Dt* Kt = reinterpret_cast<Dt*>(tiles(s)) + (size_t)wk0 * D;
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
       // match the previous phase.
       int landed = 1;
       if (lane == 0) {
-        const int use = (g + wsub) / AD_STAGES;
+        const int use = (g + wsub) / LY::STAGES;
         const long long t0 = clock64();
         while (*(volatile int*)&s_issued[s] <= use) {
           if (clock64() - t0 > (1ll << 31)) {
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
   float* wp = reinterpret_cast<float*>(ad_smem + LY::OFF_WP);
   float* mrg = reinterpret_cast<float*>(ad_smem + LY::OFF_MRG);
   uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
-  uint64_t* empty = full + AD_STAGES;
+  uint64_t* empty = full + LY::STAGES;
   __shared__ int s_flag, s_fail;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.y;
@@ -621,7 +624,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
   auto tiles = [&](int s) { return ad_smem + (size_t)s * LY::STAGE; };
 
   if (tid == 0) {
-    for (int s = 0; s < AD_STAGES; ++s) {
+    for (int s = 0; s < LY::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], AD_WPS);
     }
@@ -641,8 +644,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
         const AttnQBlock qb = a.qblocks[item.qb];
         const ItemKeys ik = item_keys<Dt>(item, qb);
         for (int sub = 0; sub < ik.nsub; ++sub, ++g) {
-          const int s = g % AD_STAGES;
-          if (g >= AD_STAGES && !mbar_wait(&empty[s], (uint32_t)((g / AD_STAGES - 1) & 1), a.err, 2)) {
+          const int s = g % LY::STAGES;
+          if (g >= LY::STAGES && !mbar_wait(&empty[s], (uint32_t)((g / LY::STAGES - 1) & 1), a.err, 2)) {
             s_fail = 1;
             return;
           }
@@ -708,13 +711,13 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
       for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
     }
     if (wsub < ik.nsub) {
-      const int s = (g + wsub) % AD_STAGES;
+      const int s = (g + wsub) % LY::STAGES;
       const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
       const int nk = min(KW, ik.key0 + ik.nkeys - key0 - wk0);  // this warp's keys (may be <= 0)
       Dt* Kt = reinterpret_cast<Dt*>(tiles(s)) + (size_t)wk0 * D;
       Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE) + (size_t)wk0 * D;
       int landed = 1;
-      if (lane == 0) landed = mbar_wait(&full[s], (uint32_t)(((g + wsub) / AD_STAGES) & 1), a.err, 2);
+      if (lane == 0) landed = mbar_wait(&full[s], (uint32_t)(((g + wsub) / LY::STAGES) & 1), a.err, 2);
       __syncwarp();
       if (!__shfl_sync(0xffffffffu, landed, 0)) {
         s_fail = 1;
@@ -805,7 +808,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
     if (s_flag) {
       const int nc = qb.n_chunks;
       // the ring is idle once this block's last item has been consumed
-      const bool os = it + (int)gridDim.x >= n_items && (size_t)nc * nq * D <= AD_STAGES * LY::STAGE / 4;
+      const bool os = it + (int)gridDim.x >= n_items && (size_t)nc * nq * D <= LY::STAGES * LY::STAGE / 4;
       combine_parts<Dt, D, NQ>(a, qb, j, nc, nq, G, wp, mrg, os ? reinterpret_cast<float*>(ad_smem) : nullptr);
       if (tid == 0) a.counters[(size_t)item.qb * a.KV + j] = 0;
     }
