@@ -1,4 +1,4 @@
-// Skinny GEMM for 5..64 activation rows: the linears of a batched decode step
+// Skinny GEMMs for 5..64 activation rows: the linears of a batched decode step
 // (maya2_mlx/backbone.py, Backbone.forward run on one new row per sequence)
 // when the weights are affine int8 (dequantised in fp32 inside the kernel, as
 // the scale * q + bias form of the int8 export prescribes) or the stack runs
@@ -222,6 +222,233 @@ cudaError_t sk_mt(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
   return a.M <= 32 ? sk_epi<Dt, WF, 32>(c, a, grid) : sk_epi<Dt, WF, 64>(c, a, grid);
 }
 
+// ---------------------------------------------------------------- int8 weights, up to 32 rows
+// Weight-streaming variant for affine int8 weights, bf16 activations and at
+// most MT (16 or 32) activation rows -- the batched decode step of an int8
+// stack.  Each lane owns two weight rows (SiLU * up: gate row n and up row
+// n; otherwise rows n and n + 32 of a 64-row tile) and dequantises them in
+// registers straight from global memory (scale * q + bias in fp32, the same
+// single-rounding form as above); the activation rows, staged once per CTA in
+// shared memory as fp32 [k][m], are read as warp-wide broadcasts, so a lane
+// does eight FMAs per 16-byte shared-memory load and no cross-lane
+// reduction.  The W8_WARPS warps of a CTA take consecutive 16-k half-steps of
+// the CTA's K range and add their partials in warp order through shared
+// memory; K splits over CTAs go through the workspace and the last CTA of a
+// tile adds them in split order, as above.
+constexpr int W8_WARPS = 8, W8_THREADS = W8_WARPS * 32;
+constexpr int W8_KC = 512;         // K per CTA at most (the staged activation slice)
+constexpr int W8_MAX_SPLIT = 16;   // the workspace holds SK_MAX_SPLIT x 64 rows = 16 x 32
+
+__device__ __forceinline__ float u8_to_f(uint32_t word, int byte) {
+  // 2^23 + q as a float, minus 2^23: exact for q in [0, 255]
+  return __int_as_float((int)__byte_perm(word, 0x4B000000u, 0x7540u | (unsigned)byte)) - 8388608.f;
+}
+
+template <int MT>
+__host__ __device__ constexpr size_t w8_smem_bytes() {
+  return (size_t)(W8_KC * MT > W8_WARPS * 2 * MT * 32 ? W8_KC * MT : W8_WARPS * 2 * MT * 32) * sizeof(float);
+}
+
+template <int MT, int EPI>
+__global__ void __launch_bounds__(W8_THREADS, 2) gemm_w8_kernel(SkinnyArgs a) {
+  constexpr bool PAIR = EPI == EPI_SWIGLU;
+  constexpr int TR = PAIR ? 32 : 64;  // output columns per tile
+  extern __shared__ __align__(16) float w8s[];  // As[k][MT] for the CTA's K range; then warp partials
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = blockIdx.x * TR + lane;
+  const bool live0 = n < a.N, live1 = PAIR ? n < a.N : n + 32 < a.N;
+  const size_t row0 = (size_t)n, row1 = PAIR ? (size_t)a.N + n : (size_t)n + 32;
+  const int nsteps = a.K / 32, spc = a.ktiles_per_split;
+  const int s0 = blockIdx.y * spc, s1 = min(nsteps, s0 + spc);
+  const int kbase = s0 * 32;
+  // this warp's half-steps (16 k each) of the CTA's range
+  const int nh = 2 * (s1 - s0);
+  const int h0 = 2 * s0 + (nh * warp) / W8_WARPS, h1 = 2 * s0 + (nh * (warp + 1)) / W8_WARPS;
+  const uint8_t* W = static_cast<const uint8_t*>(a.w);
+  const bf16* SC = static_cast<const bf16*>(a.scale);
+  const bf16* BI = static_cast<const bf16*>(a.bias);
+  const int gpr = a.K / a.group;  // groups per row
+  uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+  float sc0 = 0.f, bi0 = 0.f, sc1 = 0.f, bi1 = 0.f;
+  auto fetch = [&](int h, uint4& f0, uint4& f1, float& c0, float& b0, float& c1, float& b1) {
+    const int k = h * 16, g = k / a.group;
+    if (live0) {
+      f0 = ld_stream(W + row0 * a.K + k);
+      c0 = __bfloat162float(SC[row0 * gpr + g]);
+      b0 = __bfloat162float(BI[row0 * gpr + g]);
+    }
+    if (live1) {
+      f1 = ld_stream(W + row1 * a.K + k);
+      c1 = __bfloat162float(SC[row1 * gpr + g]);
+      b1 = __bfloat162float(BI[row1 * gpr + g]);
+    }
+  };
+  if (h0 < h1) fetch(h0, q0, q1, sc0, bi0, sc1, bi1);  // weights do not depend on the previous kernel
+  pdl_wait();
+  pdl_launch();
+  // stage the activation slice: As[k - kbase][m] = A[m][k] (rows >= M are zero)
+  {
+    const bf16* A = static_cast<const bf16*>(a.a);
+    const int nk8 = (s1 - s0) * 4;  // 8-element chunks of k
+    for (int idx = tid; idx < nk8 * MT; idx += W8_THREADS) {
+      const int m = idx % MT, c = idx / MT;
+      float x[8];
+      if (m < a.M) {
+        Vec16<bf16>::unpack(ld16(A + (size_t)m * a.lda + kbase + c * 8), x);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w8s[(c * 8 + e) * MT + m] = x[e];
+    }
+  }
+  __syncthreads();
+  float acc0[MT], acc1[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.f;
+  for (int h = h0; h < h1; ++h) {
+    const uint4 c0 = q0, c1 = q1;
+    const float cs0 = sc0, cb0 = bi0, cs1 = sc1, cb1 = bi1;
+    if (h + 1 < h1) fetch(h + 1, q0, q1, sc0, bi0, sc1, bi1);  // in flight during this half-step
+    const float* As = w8s + (size_t)(h * 16 - kbase) * MT;
+    const uint32_t u0[4] = {c0.x, c0.y, c0.z, c0.w}, u1[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const float w0 = fmaf(cs0, u8_to_f(u0[kk >> 2], kk & 3), cb0);
+      const float w1 = fmaf(cs1, u8_to_f(u1[kk >> 2], kk & 3), cb1);
+      const float4* ap = reinterpret_cast<const float4*>(As + kk * MT);
+#pragma unroll
+      for (int j = 0; j < MT / 4; ++j) {
+        const float4 av = ap[j];
+        acc0[4 * j] = fmaf(w0, av.x, acc0[4 * j]);
+        acc0[4 * j + 1] = fmaf(w0, av.y, acc0[4 * j + 1]);
+        acc0[4 * j + 2] = fmaf(w0, av.z, acc0[4 * j + 2]);
+        acc0[4 * j + 3] = fmaf(w0, av.w, acc0[4 * j + 3]);
+        acc1[4 * j] = fmaf(w1, av.x, acc1[4 * j]);
+        acc1[4 * j + 1] = fmaf(w1, av.y, acc1[4 * j + 1]);
+        acc1[4 * j + 2] = fmaf(w1, av.z, acc1[4 * j + 2]);
+        acc1[4 * j + 3] = fmaf(w1, av.w, acc1[4 * j + 3]);
+      }
+    }
+  }
+  // warp partials: red[warp][r][m][lane], added in warp order
+  __syncthreads();
+  float* red = w8s;
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    red[((warp * 2 + 0) * MT + m) * 32 + lane] = acc0[m];
+    red[((warp * 2 + 1) * MT + m) * 32 + lane] = acc1[m];
+  }
+  __syncthreads();
+  auto csum = [&](int r, int m, int l) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < W8_WARPS; ++w) v += red[((w * 2 + r) * MT + m) * 32 + l];
+    return v;
+  };
+  auto finish = [&](int m, int col, float g, float u) {
+    const size_t o = (size_t)m * a.ldo + col;
+    if (EPI == EPI_STORE) static_cast<bf16*>(a.out)[o] = from_f<bf16>(g);
+    else if (EPI == EPI_STORE_F32) static_cast<float*>(a.out)[o] = g;
+    else if (EPI == EPI_RESIDUAL) {
+      bf16* p = static_cast<bf16*>(a.out) + o;
+      *p = from_f<bf16>(to_f(*p) + rd<bf16>(g));
+    } else {
+      const float gg = rd<bf16>(g), uu = rd<bf16>(u);
+      static_cast<bf16*>(a.out)[o] = from_f<bf16>(rd<bf16>(silu_f(gg)) * uu);
+    }
+  };
+  const int c0 = blockIdx.x * TR;  // first column of the tile
+  const int ldw = PAIR ? 2 * a.N : a.N;
+  const size_t slice = (size_t)a.M * ldw;
+  if (gridDim.y == 1) {
+    if (PAIR) {
+      for (int idx = tid; idx < a.M * 32; idx += W8_THREADS) {
+        const int m = idx / 32, l = idx % 32;
+        if (c0 + l < a.N) finish(m, c0 + l, csum(0, m, l), csum(1, m, l));
+      }
+    } else {
+      for (int idx = tid; idx < a.M * 64; idx += W8_THREADS) {
+        const int m = idx / 64, cl = idx % 64;
+        if (c0 + cl < a.N) finish(m, c0 + cl, csum(cl / 32, m, cl % 32), 0.f);
+      }
+    }
+    return;
+  }
+  // this split's partial tile into its workspace slice (gate sums, then up sums)
+  for (int idx = tid; idx < a.M * 64; idx += W8_THREADS) {
+    const int m = idx / 64, cl = idx % 64, r = cl / 32, l = cl % 32;
+    const int col = PAIR ? (r ? a.N : 0) + c0 + l : c0 + cl;
+    if (c0 + (PAIR ? l : cl) < a.N) __stcg(a.ws + blockIdx.y * slice + (size_t)m * ldw + col, csum(r, m, l));
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.counters + blockIdx.x, 1) == (int)gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int idx = tid; idx < a.M * TR; idx += W8_THREADS) {
+    const int m = idx / TR, col = c0 + idx % TR;
+    if (col >= a.N) continue;
+    const float* pg = a.ws + (size_t)m * ldw + col;
+    float g = 0.f, u = 0.f;
+    for (int k = 0; k < (int)gridDim.y; ++k) {
+      g += __ldcg(pg + k * slice);
+      if (PAIR) u += __ldcg(pg + k * slice + a.N);
+    }
+    finish(m, col, g, u);
+  }
+  if (tid == 0) a.counters[blockIdx.x] = 0;
+}
+
+template <int MT, int EPI>
+cudaError_t w8_go(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
+  constexpr size_t smem = w8_smem_bytes<MT>();
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(gemm_w8_kernel<MT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_k(gemm_w8_kernel<MT, EPI>, grid, dim3(W8_THREADS), smem, c, a);
+}
+
+template <int MT>
+cudaError_t w8_epi(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
+  switch (a.epilogue) {
+    case EPI_STORE: return w8_go<MT, EPI_STORE>(c, a, grid);
+    case EPI_STORE_F32: return w8_go<MT, EPI_STORE_F32>(c, a, grid);
+    case EPI_RESIDUAL: return w8_go<MT, EPI_RESIDUAL>(c, a, grid);
+    case EPI_SWIGLU: return w8_go<MT, EPI_SWIGLU>(c, a, grid);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// The int8 variant takes bf16 activations, at most 32 rows, K a multiple of
+// 32 within W8_MAX_SPLIT CTA slices, and groups that are whole 16-k halves.
+bool w8_supported(int dt, int wfmt, const SkinnyArgs& a) {
+  return dt == DT_BF16 && wfmt == W_U8 && a.M >= 1 && a.M <= 32 && a.K % 32 == 0 && a.group % 16 == 0 &&
+         a.K % a.group == 0 && a.K <= W8_KC * W8_MAX_SPLIT;
+}
+
+cudaError_t launch_w8(const LaunchCtx& c, SkinnyArgs a) {
+  const bool pair = a.epilogue == EPI_SWIGLU;
+  const int tiles = (a.N + (pair ? 31 : 63)) / (pair ? 32 : 64), nsteps = a.K / 32;
+  // about two CTAs per SM, within the staged slice and the workspace's split count
+  int split = std::max((nsteps + W8_KC / 32 - 1) / (W8_KC / 32),
+                       std::min((2 * c.num_sms + tiles - 1) / tiles, W8_MAX_SPLIT));
+  split = std::min(split, nsteps);
+  a.ktiles_per_split = (nsteps + split - 1) / split;
+  split = (nsteps + a.ktiles_per_split - 1) / a.ktiles_per_split;
+  if (split > W8_MAX_SPLIT || a.ktiles_per_split * 32 > W8_KC) return cudaErrorInvalidValue;
+  if (split > 1 && (!a.ws || !a.counters)) return cudaErrorInvalidValue;
+  const dim3 grid(tiles, split);
+  return a.M <= 16 ? w8_epi<16>(c, a, grid) : w8_epi<32>(c, a, grid);
+}
+
 }  // namespace
 
 bool gemm_skinny_supported(int M, int N, int K) { return M >= 1 && M <= 64 && N >= 1 && K % SK_BK == 0; }
@@ -233,6 +460,7 @@ int gemm_skinny_tiles(int N) { return (N + SK_BN - 1) / SK_BN; }
 
 cudaError_t launch_gemm_skinny(const LaunchCtx& c, int dt, int wfmt, SkinnyArgs a) {
   if (!gemm_skinny_supported(a.M, a.N, a.K)) return cudaErrorInvalidValue;
+  if (w8_supported(dt, wfmt, a)) return launch_w8(c, a);
   const int tiles = gemm_skinny_tiles(a.N), ktiles = a.K / SK_BK;
   // split K so that the grid holds about two CTAs per SM
   int split = std::max(1, std::min({ktiles, (2 * c.num_sms + tiles - 1) / tiles, SK_MAX_SPLIT}));

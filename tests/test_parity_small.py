@@ -179,8 +179,12 @@ def test_moe_exact_tie_goes_to_lower_index(cuda_ok):
     stack.close()
 
 
-@pytest.mark.parametrize("n_prefill", [2, 40])
+@pytest.mark.parametrize("n_prefill", [2, 9, 24, 40])
 def test_int8_weights(cuda_ok, n_prefill):
+    """int8 weights through every linear path: the decode GEMV (2 rows), the
+    weight-streaming skinny GEMM for up to 16 and up to 32 rows (9, 24; the
+    intermediate size 1088 leaves a ragged last tile) and the tiled skinny GEMM
+    (40 rows), then two decode steps."""
     _prefill_decode(SMALL_INT8, n_prefill, 2, seed=1900 + n_prefill)
 
 
