@@ -225,19 +225,23 @@ cudaError_t sk_mt(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
 // ---------------------------------------------------------------- int8 weights, up to 32 rows
 // Weight-streaming variant for affine int8 weights, bf16 activations and at
 // most MT (16 or 32) activation rows -- the batched decode step of an int8
-// stack.  Each lane owns two weight rows (SiLU * up: gate row n and up row
-// n; otherwise rows n and n + 32 of a 64-row tile) and dequantises them in
-// registers straight from global memory (scale * q + bias in fp32, the same
-// single-rounding form as above); the activation rows, staged once per CTA in
-// shared memory as fp32 [k][m], are read as warp-wide broadcasts, so a lane
-// does eight FMAs per 16-byte shared-memory load and no cross-lane
-// reduction.  The W8_WARPS warps of a CTA take consecutive 16-k half-steps of
-// the CTA's K range and add their partials in warp order through shared
-// memory; K splits over CTAs go through the workspace and the last CTA of a
-// tile adds them in split order, as above.
+// stack.  Each lane owns four weight rows (SiLU * up: gate rows n, n + 32 and
+// the matching up rows; otherwise rows n + 32 r of a 128-row tile) and
+// dequantises them in registers straight from global memory (scale * q + bias
+// in fp32, the same single-rounding form as above).  The activation rows are
+// staged once per CTA in shared memory as fp32 [k][m] and read as warp-wide
+// broadcasts; a warp takes 16 of them, so each 16-byte shared-memory load
+// feeds 16 FMAs per lane -- four wavefronts per 16 FMA instructions, which
+// keeps the shared-memory pipe level with the FMA pipe -- and no cross-lane
+// reduction is needed.  The CTA's warps split the K range (and the two token
+// halves) and add their partials in a fixed order through shared memory; K
+// splits over CTAs go through the workspace and the last CTA of a tile adds
+// them in split order, as above.
 constexpr int W8_WARPS = 8, W8_THREADS = W8_WARPS * 32;
-constexpr int W8_KC = 512;         // K per CTA at most (the staged activation slice)
+constexpr int W8_KC = 768;         // K per CTA at most (the staged activation slice)
 constexpr int W8_MAX_SPLIT = 16;   // the workspace holds SK_MAX_SPLIT x 64 rows = 16 x 32
+constexpr int W8_R = 4;            // weight rows per lane
+constexpr int W8_MW = 16;          // activation rows per warp
 
 __device__ __forceinline__ float u8_to_f(uint32_t word, int byte) {
   // 2^23 + q as a float, minus 2^23: exact for q in [0, 255]
@@ -246,106 +250,142 @@ __device__ __forceinline__ float u8_to_f(uint32_t word, int byte) {
 
 template <int MT>
 __host__ __device__ constexpr size_t w8_smem_bytes() {
-  return (size_t)(W8_KC * MT > W8_WARPS * 2 * MT * 32 ? W8_KC * MT : W8_WARPS * 2 * MT * 32) * sizeof(float);
+  return (size_t)(W8_KC * MT > W8_WARPS * W8_R * W8_MW * 32 ? W8_KC * MT : W8_WARPS * W8_R * W8_MW * 32) *
+         sizeof(float);
 }
 
 template <int MT, int EPI>
 __global__ void __launch_bounds__(W8_THREADS, 2) gemm_w8_kernel(SkinnyArgs a) {
   constexpr bool PAIR = EPI == EPI_SWIGLU;
-  constexpr int TR = PAIR ? 32 : 64;  // output columns per tile
+  constexpr int TN = PAIR ? 64 : 128;      // output columns per tile
+  constexpr int TH = MT / W8_MW;           // token halves
+  constexpr int KP = W8_WARPS / TH;        // K parts per token half
   extern __shared__ __align__(16) float w8s[];  // As[k][MT] for the CTA's K range; then warp partials
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = blockIdx.x * TR + lane;
-  const bool live0 = n < a.N, live1 = PAIR ? n < a.N : n + 32 < a.N;
-  const size_t row0 = (size_t)n, row1 = PAIR ? (size_t)a.N + n : (size_t)n + 32;
+  const int th = warp % TH, kp = warp / TH;
+  const int c0 = blockIdx.x * TN;  // first output column of the tile
+  // this lane's weight rows; row r of the lane is output column col(r) (+ N for up rows)
+  size_t wrow[W8_R];
+  bool live[W8_R];
+#pragma unroll
+  for (int r = 0; r < W8_R; ++r) {
+    const int col = PAIR ? c0 + (r & 1) * 32 + lane : c0 + r * 32 + lane;
+    live[r] = col < a.N;
+    wrow[r] = (size_t)col + (PAIR && r >= 2 ? (size_t)a.N : 0);
+  }
   const int nsteps = a.K / 32, spc = a.ktiles_per_split;
   const int s0 = blockIdx.y * spc, s1 = min(nsteps, s0 + spc);
   const int kbase = s0 * 32;
   // this warp's half-steps (16 k each) of the CTA's range
   const int nh = 2 * (s1 - s0);
-  const int h0 = 2 * s0 + (nh * warp) / W8_WARPS, h1 = 2 * s0 + (nh * (warp + 1)) / W8_WARPS;
+  const int h0 = 2 * s0 + (nh * kp) / KP, h1 = 2 * s0 + (nh * (kp + 1)) / KP;
   const uint8_t* W = static_cast<const uint8_t*>(a.w);
-  const bf16* SC = static_cast<const bf16*>(a.scale);
-  const bf16* BI = static_cast<const bf16*>(a.bias);
+  const unsigned short* SC = static_cast<const unsigned short*>(a.scale);
+  const unsigned short* BI = static_cast<const unsigned short*>(a.bias);
   const int gpr = a.K / a.group;  // groups per row
-  uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
-  float sc0 = 0.f, bi0 = 0.f, sc1 = 0.f, bi1 = 0.f;
-  auto fetch = [&](int h, uint4& f0, uint4& f1, float& c0, float& b0, float& c1, float& b1) {
+  uint4 q[W8_R];
+  uint32_t sb[W8_R] = {};  // bf16 scale (low half) and bias (high half) of the half-step's group
+  // weights of half-step h; the group's scale and bias only where a group
+  // starts (or at the warp's first half-step) -- fsb keeps them otherwise
+  auto fetch = [&](int h, uint4 (&f)[W8_R], uint32_t (&fsb)[W8_R]) {
     const int k = h * 16, g = k / a.group;
-    if (live0) {
-      f0 = ld_stream(W + row0 * a.K + k);
-      c0 = __bfloat162float(SC[row0 * gpr + g]);
-      b0 = __bfloat162float(BI[row0 * gpr + g]);
-    }
-    if (live1) {
-      f1 = ld_stream(W + row1 * a.K + k);
-      c1 = __bfloat162float(SC[row1 * gpr + g]);
-      b1 = __bfloat162float(BI[row1 * gpr + g]);
+    const bool new_group = h == h0 || k % a.group == 0;
+#pragma unroll
+    for (int r = 0; r < W8_R; ++r) {
+      if (live[r]) {
+        f[r] = ld_stream(W + wrow[r] * a.K + k);
+        if (new_group) fsb[r] = (uint32_t)SC[wrow[r] * gpr + g] | ((uint32_t)BI[wrow[r] * gpr + g] << 16);
+      } else {
+        f[r] = make_uint4(0, 0, 0, 0);
+        fsb[r] = 0;
+      }
     }
   };
-  if (h0 < h1) fetch(h0, q0, q1, sc0, bi0, sc1, bi1);  // weights do not depend on the previous kernel
+  if (h0 < h1) fetch(h0, q, sb);  // weights do not depend on the previous kernel
   pdl_wait();
   pdl_launch();
-  // stage the activation slice: As[k - kbase][m] = A[m][k] (rows >= M are zero)
+  // stage the activation slice: As[k - kbase][m] = A[m][k] (rows >= M are zero); batches of
+  // independent loads so that a thread waits for L2 once per batch
   {
+    constexpr int SB = 8;
     const bf16* A = static_cast<const bf16*>(a.a);
-    const int nk8 = (s1 - s0) * 4;  // 8-element chunks of k
-    for (int idx = tid; idx < nk8 * MT; idx += W8_THREADS) {
-      const int m = idx % MT, c = idx / MT;
-      float x[8];
-      if (m < a.M) {
-        Vec16<bf16>::unpack(ld16(A + (size_t)m * a.lda + kbase + c * 8), x);
-      } else {
+    const int total = (s1 - s0) * 4 * MT;  // 8-element chunks of k, times MT rows
+    for (int base = tid; base < total; base += W8_THREADS * SB) {
+      uint4 v[SB];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      for (int u = 0; u < SB; ++u) {
+        const int idx = base + u * W8_THREADS, m = idx % MT, c = idx / MT;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (idx < total && m < a.M) v[u] = ld16(A + (size_t)m * a.lda + kbase + c * 8);
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w8s[(c * 8 + e) * MT + m] = x[e];
+      for (int u = 0; u < SB; ++u) {
+        const int idx = base + u * W8_THREADS, m = idx % MT, c = idx / MT;
+        if (idx < total) {
+          float x[8];
+          Vec16<bf16>::unpack(v[u], x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w8s[(c * 8 + e) * MT + m] = x[e];
+        }
+      }
     }
   }
   __syncthreads();
-  float acc0[MT], acc1[MT];
+  float acc[W8_R][W8_MW];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.f;
+  for (int r = 0; r < W8_R; ++r)
+#pragma unroll
+    for (int m = 0; m < W8_MW; ++m) acc[r][m] = 0.f;
   for (int h = h0; h < h1; ++h) {
-    const uint4 c0 = q0, c1 = q1;
-    const float cs0 = sc0, cb0 = bi0, cs1 = sc1, cb1 = bi1;
-    if (h + 1 < h1) fetch(h + 1, q0, q1, sc0, bi0, sc1, bi1);  // in flight during this half-step
-    const float* As = w8s + (size_t)(h * 16 - kbase) * MT;
-    const uint32_t u0[4] = {c0.x, c0.y, c0.z, c0.w}, u1[4] = {c1.x, c1.y, c1.z, c1.w};
+    uint4 c[W8_R];
+    uint32_t csb[W8_R];
+#pragma unroll
+    for (int r = 0; r < W8_R; ++r) { c[r] = q[r]; csb[r] = sb[r]; }
+    if (h + 1 < h1) fetch(h + 1, q, sb);  // in flight during this half-step
+    float scl[W8_R], bia[W8_R];
+#pragma unroll
+    for (int r = 0; r < W8_R; ++r) {
+      scl[r] = __uint_as_float(csb[r] << 16);
+      bia[r] = __uint_as_float(csb[r] & 0xffff0000u);
+    }
+    const float* As = w8s + (size_t)(h * 16 - kbase) * MT + th * W8_MW;
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      const float w0 = fmaf(cs0, u8_to_f(u0[kk >> 2], kk & 3), cb0);
-      const float w1 = fmaf(cs1, u8_to_f(u1[kk >> 2], kk & 3), cb1);
+      float w[W8_R];
+#pragma unroll
+      for (int r = 0; r < W8_R; ++r) {
+        const uint32_t word = kk < 4 ? c[r].x : kk < 8 ? c[r].y : kk < 12 ? c[r].z : c[r].w;
+        w[r] = fmaf(scl[r], u8_to_f(word, kk & 3), bia[r]);
+      }
       const float4* ap = reinterpret_cast<const float4*>(As + kk * MT);
 #pragma unroll
-      for (int j = 0; j < MT / 4; ++j) {
+      for (int j = 0; j < W8_MW / 4; ++j) {
         const float4 av = ap[j];
-        acc0[4 * j] = fmaf(w0, av.x, acc0[4 * j]);
-        acc0[4 * j + 1] = fmaf(w0, av.y, acc0[4 * j + 1]);
-        acc0[4 * j + 2] = fmaf(w0, av.z, acc0[4 * j + 2]);
-        acc0[4 * j + 3] = fmaf(w0, av.w, acc0[4 * j + 3]);
-        acc1[4 * j] = fmaf(w1, av.x, acc1[4 * j]);
-        acc1[4 * j + 1] = fmaf(w1, av.y, acc1[4 * j + 1]);
-        acc1[4 * j + 2] = fmaf(w1, av.z, acc1[4 * j + 2]);
-        acc1[4 * j + 3] = fmaf(w1, av.w, acc1[4 * j + 3]);
+#pragma unroll
+        for (int r = 0; r < W8_R; ++r) {
+          acc[r][4 * j] = fmaf(w[r], av.x, acc[r][4 * j]);
+          acc[r][4 * j + 1] = fmaf(w[r], av.y, acc[r][4 * j + 1]);
+          acc[r][4 * j + 2] = fmaf(w[r], av.z, acc[r][4 * j + 2]);
+          acc[r][4 * j + 3] = fmaf(w[r], av.w, acc[r][4 * j + 3]);
+        }
       }
     }
   }
-  // warp partials: red[warp][r][m][lane], added in warp order
+  // warp partials: red[kp][th][r][m][lane], added over kp in order
   __syncthreads();
   float* red = w8s;
 #pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    red[((warp * 2 + 0) * MT + m) * 32 + lane] = acc0[m];
-    red[((warp * 2 + 1) * MT + m) * 32 + lane] = acc1[m];
-  }
+  for (int r = 0; r < W8_R; ++r)
+#pragma unroll
+    for (int m = 0; m < W8_MW; ++m) red[(((kp * TH + th) * W8_R + r) * W8_MW + m) * 32 + lane] = acc[r][m];
   __syncthreads();
+  // full sum of lane row r of lane l for activation row m
   auto csum = [&](int r, int m, int l) {
+    const int t = m / W8_MW, mm = m % W8_MW;
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < W8_WARPS; ++w) v += red[((w * 2 + r) * MT + m) * 32 + l];
+    for (int p = 0; p < KP; ++p) v += red[(((p * TH + t) * W8_R + r) * W8_MW + mm) * 32 + l];
     return v;
   };
   auto finish = [&](int m, int col, float g, float u) {
@@ -360,28 +400,24 @@ __global__ void __launch_bounds__(W8_THREADS, 2) gemm_w8_kernel(SkinnyArgs a) {
       static_cast<bf16*>(a.out)[o] = from_f<bf16>(rd<bf16>(silu_f(gg)) * uu);
     }
   };
-  const int c0 = blockIdx.x * TR;  // first column of the tile
   const int ldw = PAIR ? 2 * a.N : a.N;
   const size_t slice = (size_t)a.M * ldw;
+  // tile column j (0 .. TN) of activation row m: lane j % 32, lane row j / 32 (pair: + 2 for up)
   if (gridDim.y == 1) {
-    if (PAIR) {
-      for (int idx = tid; idx < a.M * 32; idx += W8_THREADS) {
-        const int m = idx / 32, l = idx % 32;
-        if (c0 + l < a.N) finish(m, c0 + l, csum(0, m, l), csum(1, m, l));
-      }
-    } else {
-      for (int idx = tid; idx < a.M * 64; idx += W8_THREADS) {
-        const int m = idx / 64, cl = idx % 64;
-        if (c0 + cl < a.N) finish(m, c0 + cl, csum(cl / 32, m, cl % 32), 0.f);
-      }
+    for (int idx = tid; idx < a.M * TN; idx += W8_THREADS) {
+      const int m = idx / TN, j = idx % TN;
+      if (c0 + j < a.N) finish(m, c0 + j, csum(j / 32, m, j % 32), PAIR ? csum(j / 32 + 2, m, j % 32) : 0.f);
     }
     return;
   }
   // this split's partial tile into its workspace slice (gate sums, then up sums)
-  for (int idx = tid; idx < a.M * 64; idx += W8_THREADS) {
-    const int m = idx / 64, cl = idx % 64, r = cl / 32, l = cl % 32;
-    const int col = PAIR ? (r ? a.N : 0) + c0 + l : c0 + cl;
-    if (c0 + (PAIR ? l : cl) < a.N) __stcg(a.ws + blockIdx.y * slice + (size_t)m * ldw + col, csum(r, m, l));
+  for (int idx = tid; idx < a.M * TN; idx += W8_THREADS) {
+    const int m = idx / TN, j = idx % TN;
+    if (c0 + j < a.N) {
+      float* wsp = a.ws + blockIdx.y * slice + (size_t)m * ldw + c0 + j;
+      __stcg(wsp, csum(j / 32, m, j % 32));
+      if (PAIR) __stcg(wsp + a.N, csum(j / 32 + 2, m, j % 32));
+    }
   }
   __threadfence();
   __syncthreads();
@@ -389,8 +425,8 @@ __global__ void __launch_bounds__(W8_THREADS, 2) gemm_w8_kernel(SkinnyArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int idx = tid; idx < a.M * TR; idx += W8_THREADS) {
-    const int m = idx / TR, col = c0 + idx % TR;
+  for (int idx = tid; idx < a.M * TN; idx += W8_THREADS) {
+    const int m = idx / TN, col = c0 + idx % TN;
     if (col >= a.N) continue;
     const float* pg = a.ws + (size_t)m * ldw + col;
     float g = 0.f, u = 0.f;
@@ -436,14 +472,21 @@ bool w8_supported(int dt, int wfmt, const SkinnyArgs& a) {
 
 cudaError_t launch_w8(const LaunchCtx& c, SkinnyArgs a) {
   const bool pair = a.epilogue == EPI_SWIGLU;
-  const int tiles = (a.N + (pair ? 31 : 63)) / (pair ? 32 : 64), nsteps = a.K / 32;
-  // about two CTAs per SM, within the staged slice and the workspace's split count
-  int split = std::max((nsteps + W8_KC / 32 - 1) / (W8_KC / 32),
-                       std::min((2 * c.num_sms + tiles - 1) / tiles, W8_MAX_SPLIT));
-  split = std::min(split, nsteps);
+  const int tn = pair ? 64 : 128, tiles = (a.N + tn - 1) / tn, nsteps = a.K / 32;
+  // the fewest K splits (each within the staged slice) that fill whole waves
+  // of two resident CTAs per SM best
+  const int smin = (nsteps + W8_KC / 32 - 1) / (W8_KC / 32), slots = 2 * c.num_sms;
+  int split = 0;
+  double best = -1.0;
+  for (int sp = smin; sp <= std::min(W8_MAX_SPLIT, nsteps); ++sp) {
+    const int ctas = tiles * sp, waves = (ctas + slots - 1) / slots;
+    const double util = (double)ctas / ((double)waves * slots);
+    if (util > best + 1e-9) { best = util; split = sp; }
+  }
+  if (split == 0) return cudaErrorInvalidValue;
   a.ktiles_per_split = (nsteps + split - 1) / split;
   split = (nsteps + a.ktiles_per_split - 1) / a.ktiles_per_split;
-  if (split > W8_MAX_SPLIT || a.ktiles_per_split * 32 > W8_KC) return cudaErrorInvalidValue;
+  if (a.ktiles_per_split * 32 > W8_KC) return cudaErrorInvalidValue;
   if (split > 1 && (!a.ws || !a.counters)) return cudaErrorInvalidValue;
   const dim3 grid(tiles, split);
   return a.M <= 16 ? w8_epi<16>(c, a, grid) : w8_epi<32>(c, a, grid);
