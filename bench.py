@@ -411,6 +411,13 @@ def run_workload(args):
     wl, K, W = args.workload, args.steps, args.warmup
     cfg = {"prefill": I.DENSE_1P7B_PREFILL, "moe_decode": I.MOE_A3B_4LAYER, "moe_prefill": I.MOE_A3B_4LAYER,
            "batched_int8": I.DENSE_1P7B_INT8_B32}[wl]
+    # reduced case for profiler captures (fewer layers, one short context): same shapes per layer,
+    # a few GB on the device; its line says so and is not a measurement of the workload
+    reduced = bool(args.layers or args.ctx)
+    if args.layers:
+        cfg = I.with_sizes(cfg, num_layers=args.layers)
+    if args.ctx and wl in ("moe_decode", "batched_int8"):
+        cfg = I.with_sizes(cfg, capacity=args.ctx + W + K + 16)
     weights = I.make_weights(cfg, seed=I.SEEDS[cfg.name], device="cuda")
     stack = Q.Qwen3Stack(cfg, weights)
     gen = torch.Generator(device="cuda")
@@ -452,6 +459,8 @@ def run_workload(args):
         else:
             n_seq = cfg.max_seqs
             ctx = I.batch_context_lengths(n_seq, 1024, 16384, seed=3600)
+        if args.ctx:
+            ctx = [args.ctx] * n_seq
         assert max(ctx) + W + K <= cfg.capacity, "steps + warmup exceed the cache capacity"
         for s_, n in enumerate(ctx):
             fill(s_, n)
@@ -508,6 +517,8 @@ def run_workload(args):
             "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16" if cfg.weight_format != "int8" else
             "bf16 activations, int8 weights", "data": "synthetic (seeded)", "workload": wl,
             "config": {"workload": f"{cfg.name}: {steps_desc}", "layers": cfg.num_layers},
+            **({"reduced": "profiling case (--layers / --ctx): not a measurement of the workload"}
+               if reduced else {}),
             "kernels": kernels, "clocks": clocks.summary()}
     if wl == "prefill":
         T = 2048
@@ -553,6 +564,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode", choices=WORKLOADS,
                     help="decode (default: the headline line) or one of the other scope-table workloads")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run a non-decode workload with this many layers")
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="profiling only: every sequence of moe_decode / batched_int8 at this context")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {"decode": 256, "prefill": 10, "moe_decode": 56, "moe_prefill": 10, "batched_int8": 64}[
