@@ -119,11 +119,17 @@ struct SkinnyArgs {
   float* ws;
   int* counters;
   int ktiles_per_split;  // set by the launcher
+  int* err;              // device error flag (tensor-core variant's bounded waits)
 };
 bool gemm_skinny_supported(int M, int N, int K);
 size_t gemm_skinny_ws_floats(int M, int N, int epilogue);
 int gemm_skinny_tiles(int N);
 cudaError_t launch_gemm_skinny(const LaunchCtx& c, int dt, int wfmt, SkinnyArgs a);
+// Tensor-core form for affine int8 weights, bf16 activations and 1..32 rows
+// (integer codes through tcgen05.mma, group scale and bias in the epilogue);
+// groups must be whole multiples of 64.  Same arguments and workspace.
+bool gemm_w8_tc_supported(int M, int N, int K, int group, int epilogue);
+cudaError_t launch_gemm_w8_tc(const LaunchCtx& c, SkinnyArgs a);
 
 // Tensor-core (tcgen05 / TMEM / TMA) bf16 GEMM: out[M, N] = a[M, K] w[N, K]^T
 // with EPI_STORE, EPI_RESIDUAL (out += R(.), in place) or EPI_SWIGLU (w has

@@ -947,7 +947,9 @@ cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const char* tc_name, const
     SkinnyArgs k{};
     k.M = g.M; k.N = g.N; k.K = g.K; k.a = g.a; k.lda = g.lda; k.w = g.w; k.scale = g.scale; k.bias = g.bias;
     k.group = g.group; k.epilogue = g.epilogue; k.out = g.out; k.ldo = g.ldo;
-    k.ws = static_cast<float*>(h->skws.p); k.counters = static_cast<int*>(h->skcnt.p);
+    k.ws = static_cast<float*>(h->skws.p); k.counters = static_cast<int*>(h->skcnt.p); k.err = B.err;
+    if (h->use_tc && h->dt == DT_BF16 && wfmt == W_U8 && gemm_w8_tc_supported(g.M, g.N, g.K, g.group, g.epilogue))
+      return launch(L, tc_name, [&] { return launch_gemm_w8_tc(L.ctx, k); });
     return launch(L, simt_name, [&] { return launch_gemm_skinny(L.ctx, h->dt, wfmt, k); });
   }
   return launch(L, simt_name, [&] { return launch_gemm_simt(L.ctx, h->dt, wfmt, g); });

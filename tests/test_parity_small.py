@@ -182,10 +182,21 @@ def test_moe_exact_tie_goes_to_lower_index(cuda_ok):
 @pytest.mark.parametrize("n_prefill", [2, 9, 24, 40])
 def test_int8_weights(cuda_ok, n_prefill):
     """int8 weights through every linear path: the decode GEMV (2 rows), the
-    weight-streaming skinny GEMM for up to 16 and up to 32 rows (9, 24; the
-    intermediate size 1088 leaves a ragged last tile) and the tiled skinny GEMM
-    (40 rows), then two decode steps."""
+    tensor-core int8 GEMM for up to 32 rows (9, 24; the intermediate size 1088
+    leaves a ragged last tile, and the narrow linears split K over CTAs) and
+    the tiled skinny GEMM (40 rows), then two decode steps."""
     _prefill_decode(SMALL_INT8, n_prefill, 2, seed=1900 + n_prefill)
+
+
+@pytest.mark.parametrize("n_prefill", [9, 24])
+def test_int8_weights_cuda_cores(cuda_ok, n_prefill):
+    """The same rows with tensor cores switched off: the CUDA-core int8 GEMM."""
+    p = Parity(SMALL_INT8, seed=1950 + n_prefill)
+    Q.qwen3_set_option(p.stack.h, Q.QWEN3_OPT_TENSOR_CORES, 0)
+    p.step(I.make_rows(SMALL_INT8, n_prefill, seed=1951 + n_prefill).cuda())
+    p.step(I.make_rows(SMALL_INT8, 1, seed=1952 + n_prefill).cuda())
+    p.close()
+    p.check()
 
 
 @pytest.mark.parametrize("graphs,pdl", [(0, 0), (0, 1), (1, 0)])
