@@ -162,30 +162,42 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
       if (i >= WT_CSTAGES && !mbar_wait(&cempty[c], (uint32_t)((i / WT_CSTAGES - 1) & 1), err, 15)) break;
       const uint8_t* st = smem + s * WT_LSTAGE;
       uint8_t* cq = smem + WT_OFF_C + c * WT_CSTAGE;
+      // Every shared-memory read of the group is issued before the first store
+      // (the stores could alias the reads as far as the compiler knows, and
+      // would otherwise serialise them).
       // codes: task t = (row t / 4, 16-byte chunk t % 4) -> bf16 chunks 2 (t % 4), + 1 of the row
+      uint4 w[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = ct + 256 * u;
+        w[u] = *reinterpret_cast<const uint4*>(st + WT_ACT_BYTES + (t >> 2) * WT_BK + (t & 3) * 16);
+      }
+      const uint4 act = reinterpret_cast<const uint4*>(st)[ct];  // activation chunk ct (of 256)
+      // group sums of the activation rows (the first four converter warps):
+      // row m = ct / 4 sums its logical chunks 2p, 2p + 1
+      const int m = (ct & 127) >> 2, p = ct & 3;
+      uint4 sv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) sv[h] = *reinterpret_cast<const uint4*>(st + sw128_off(m, 2 * p + h));
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int t = ct + 256 * u, r = t >> 2, j = t & 3;
-        const uint4 w = *reinterpret_cast<const uint4*>(st + WT_ACT_BYTES + r * WT_BK + j * 16);
         uint4 lo, hi;
-        lo.x = u8_bf16_pair(w.x, 0); lo.y = u8_bf16_pair(w.x, 2);
-        lo.z = u8_bf16_pair(w.y, 0); lo.w = u8_bf16_pair(w.y, 2);
-        hi.x = u8_bf16_pair(w.z, 0); hi.y = u8_bf16_pair(w.z, 2);
-        hi.z = u8_bf16_pair(w.w, 0); hi.w = u8_bf16_pair(w.w, 2);
+        lo.x = u8_bf16_pair(w[u].x, 0); lo.y = u8_bf16_pair(w[u].x, 2);
+        lo.z = u8_bf16_pair(w[u].y, 0); lo.w = u8_bf16_pair(w[u].y, 2);
+        hi.x = u8_bf16_pair(w[u].z, 0); hi.y = u8_bf16_pair(w[u].z, 2);
+        hi.z = u8_bf16_pair(w[u].w, 0); hi.w = u8_bf16_pair(w[u].w, 2);
         *reinterpret_cast<uint4*>(cq + sw128_off(r, 2 * j)) = lo;
         *reinterpret_cast<uint4*>(cq + sw128_off(r, 2 * j + 1)) = hi;
       }
-      // activation tile copied as is (same swizzled layout), 4 KB = 256 chunks
-      reinterpret_cast<uint4*>(cq + WT_Q_BYTES)[ct] = reinterpret_cast<const uint4*>(st)[ct];
-      // group sums of the activation rows (the first four converter warps):
-      // row m = ct / 4 sums its logical chunks 2p, 2p + 1
+      // activation tile copied as is (same swizzled layout)
+      reinterpret_cast<uint4*>(cq + WT_Q_BYTES)[ct] = act;
       if (ct < 128) {
-        const int m = ct >> 2, p = ct & 3;
         float sum = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float x[8];
-          Vec16<bf16>::unpack(*reinterpret_cast<const uint4*>(st + sw128_off(m, 2 * p + h)), x);
+          Vec16<bf16>::unpack(sv[h], x);
 #pragma unroll
           for (int e = 0; e < 8; ++e) sum += x[e];
         }
