@@ -212,7 +212,7 @@ QWEN3_API qwen3_status qwen3_get_length(const qwen3_handle* h, int32_t seq, int3
 #define QWEN3_OPT_CUDA_GRAPHS 1   /* 1 (default) = replay a captured graph per row count for decode-sized calls */
 #define QWEN3_OPT_PROFILE 2       /* 1 = launch directly and time every kernel with CUDA events */
 #define QWEN3_OPT_PDL 3           /* 1 (default) = programmatic dependent launch between kernels */
-#define QWEN3_OPT_TENSOR_CORES 4  /* 1 (default) = tcgen05 GEMMs for bf16 prefill linears; 0 = CUDA cores */
+#define QWEN3_OPT_TENSOR_CORES 4  /* 1 (default) = tcgen05 for bf16 prefill linears and attention, MoE expert GEMMs, and int8 linears of 5..32 rows; 0 = CUDA cores */
 #define QWEN3_OPT_L2_PREFETCH 5   /* 1 (default) = decode kernels prefetch the next linear's weights into L2 */
 #define QWEN3_OPT_FUSED_DECODE 6  /* 1 = dense decode steps run as one persistent cooperative kernel; 0 (default) = five kernels per layer */
 QWEN3_API qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value);
