@@ -225,7 +225,8 @@ cudaError_t sk_mt(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
 // ---------------------------------------------------------------- int8 weights, up to 32 rows
 // Weight-streaming variant for affine int8 weights, bf16 activations and at
 // most MT (16 or 32) activation rows -- the batched decode step of an int8
-// stack.  Each lane owns four weight rows (SiLU * up: gate rows n, n + 32 and
+// stack when tensor cores are switched off (the tensor-core form is
+// gemm_w8_tc.cu).  Each lane owns four weight rows (SiLU * up: gate rows n, n + 32 and
 // the matching up rows; otherwise rows n + 32 r of a 128-row tile) and
 // dequantises them in registers straight from global memory (scale * q + bias
 // in fp32, the same single-rounding form as above).  The activation rows are
