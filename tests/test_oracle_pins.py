@@ -353,6 +353,28 @@ def test_dequant_affine_closed_forms():
     assert np.all(mid == 0.0)
 
 
+def test_int8_product_regroups_by_group():
+    """The int8 linear y = x W^T with W dequantised per group (the int8 export's
+    scale * q + bias) equals, by exact algebra, the per-group form
+    sum_g scale[n, g] * (x[:, g] . q[n, g]) + bias[n, g] * sum(x[:, g]) -- the
+    form the tensor-core int8 GEMM evaluates.  Pinned with an independent fp64
+    einsum over the groups (no call to dequant_affine on that side)."""
+    rng = np.random.default_rng(93)
+    n_out, k, group, m = 5, 256, 64, 7
+    codes = rng.integers(0, 256, (n_out, k))
+    scale = rng.uniform(0.001, 0.02, (n_out, k // group))
+    bias = rng.uniform(-0.5, 0.5, (n_out, k // group))
+    x = rng.standard_normal((m, k))
+    y = x @ dequant_affine(codes, scale, bias, group).T
+    xg = x.reshape(m, k // group, group)
+    qg = codes.reshape(n_out, k // group, group).astype(np.float64)
+    regrouped = (np.einsum("mgj,ngj,ng->mn", xg, qg, scale) +
+                 np.einsum("mgj,ng->mn", xg, bias))
+    assert np.allclose(y, regrouped, rtol=1e-12, atol=1e-12)
+    # a dropped bias term or a transposed scale would fail:
+    assert not np.allclose(y, np.einsum("mgj,ngj,ng->mn", xg, qg, scale), atol=1e-3)
+
+
 def test_int8_stack_equals_dense_stack_on_dequantised_weights():
     """An int8 stack is the dense stack run on the dequantised matrices."""
     cfg = I.with_sizes(TINY, dtype="bf16", weight_format="int8", group_size=16)
