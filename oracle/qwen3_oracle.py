@@ -28,7 +28,7 @@ Arithmetic is float64 (numpy).  ``prec`` selects where results are rounded:
   to the model dtype at exactly the Backbone's rounding points.  The GPU is
   compared against this mode.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 RMSNorm's "two roundings" = round(x * rsqrt(mean(x^2)+eps)) then
 round(that * gain); RoPE table inv_freq_i = theta^(-2i/D) rounded to the table
 dtype, angle p*inv_freq in fp64, cos/sin rounded to the table dtype, halves
@@ -36,7 +36,8 @@ duplicated; half-split (rotate-half) RoPE; query at position p sees keys 0..p of
 its own sequence; q head h uses kv head h // (H/KV); router top-k chosen on the
 unrounded router logits with ties to the lowest expert index; the MoE weighted
 sum accumulates unrounded and is rounded once; int8 codes are unsigned and
-dequantise as scale*q + bias (not rounded).
+dequantise as scale*q + bias (not rounded); a MoE stack's layer is sparse iff
+it is not listed in mlp_only_layers and (index + 1) % decoder_sparse_step == 0.
 
 Parity status: every function here is pinned by a CPU test in
 ``tests/test_oracle_pins.py``; the only unpinned part is which exact rounding
@@ -152,6 +153,48 @@ def router_topk(logits, k: int, norm_topk_prob: bool):
     return idx.astype(np.int64), w, P
 
 
+def moe_layer(cfg, layer: int) -> bool:
+    """Which layers of a Qwen3-MoE stack carry the sparse block
+    (@mlx-bun/inference qwen3-moe.ts, ``Qwen3MoeDecoderLayer``): a layer is MoE
+    iff the model has experts, the layer is not in ``mlp_only_layers``, and
+    (index + 1) % decoder_sparse_step == 0; every other layer is the dense MLP."""
+    if cfg.num_experts <= 0:
+        return False
+    if layer in tuple(getattr(cfg, "mlp_only_layers", ())):
+        return False
+    return (layer + 1) % cfg.decoder_sparse_step == 0
+
+
+def embed_rows(table, ids, prec: str):
+    """Embedding lookup (maya2_mlx/backbone.py, ``Backbone.embed_tokens``: the
+    rows of the embedding table at the token ids, in the model dtype)."""
+    T = np.asarray(table, dtype=np.float64)
+    return rnd(T[np.asarray(ids, dtype=np.int64)], prec)
+
+
+def head_logits(x, W, prec: str):
+    """Output head (maya2_mlx/backbone.py, ``Backbone.cb0_logits``: the product
+    with the head's [out, hidden] matrix in the model dtype, then widened to
+    fp32).  The product is accumulated in float64 and rounded once to the model
+    dtype; the widening to fp32 is exact.  A tied head
+    (@mlx-bun/inference qwen3.ts, ``embed.asLinear``) passes the embedding
+    table as W."""
+    return rnd(np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T, prec)
+
+
+def l2_pool_last(h, prec: str):
+    """Pooled sentence vector (@mlx-bun/inference qwen3.ts, ``embedPooled``):
+    the last row of the final-norm hidden states divided by its L2 norm.  The
+    page runs square, sum, sqrt and divide as separate array operations in the
+    model dtype, so each result is rounded to it: sq = R(v*v), ss = R(sum sq)
+    (the sum itself accumulated wide), n = R(sqrt(ss)), out = R(v / n)."""
+    v = np.asarray(h, dtype=np.float64)[-1]
+    sq = rnd(v * v, prec)
+    ss = rnd(np.sum(sq), prec)
+    n = rnd(np.sqrt(ss), prec)
+    return rnd(v / n, prec)
+
+
 # --------------------------------------------------------------------------
 # the stack
 # --------------------------------------------------------------------------
@@ -195,6 +238,14 @@ class Qwen3Oracle:
             return dequant_affine(lw["w"], lw["scale"], lw["bias"], self.cfg.group_size)
         return lw["w"].astype(np.float64)
 
+    def expert_weight(self, lw, e: int):
+        """The float64 [out, in] matrix of expert e of a stacked expert linear
+        ([E, out, in]; int8 experts dequantise like any int8 linear, as
+        qwen3-moe.ts's QuantizedSwitchLinear stacks quantised expert matrices)."""
+        if "scale" in lw:
+            return dequant_affine(lw["w"][e], lw["scale"][e], lw["bias"][e], self.cfg.group_size)
+        return lw["w"][e].astype(np.float64)
+
     def matmul(self, x, lw):
         """x [T, in] @ W^T, float64 accumulation (Q.mm), not rounded here."""
         return self._mm(x, self.linear_weight(lw))
@@ -232,13 +283,16 @@ class Qwen3Oracle:
         return self._seq(seq)["length"]
 
     # -- one forward -----------------------------------------------------------
-    def forward(self, x, seq_ids=None, positions=None, return_moe=False, trace=None):
+    def forward(self, x, seq_ids=None, positions=None, return_moe=False, trace=None, taps=None):
         """x [T, hidden] at the given (sequence, position) of each row ->
         final-norm hidden states [T, hidden] (Backbone.forward).  Rows of a
         sequence must continue that sequence's cache (positions
         length, length+1, ...), as Backbone.forward appends at
         length..length+T-1 and raises on overflow.  If ``trace`` is a list,
-        each layer appends a dict of its intermediate tensors."""
+        each layer appends a dict of its intermediate tensors.  ``taps`` is a
+        dict keyed by layer index: each listed layer stores there the residual
+        entering it ("h_in"), the residual after its attention ("h") and its MLP
+        output ("pend") -- the pieces a one-layer stack needs to reproduce it."""
         cfg, R = self.cfg, (lambda a: rnd(a, self.prec))
         x = _f64(x)
         T = x.shape[0]
@@ -274,6 +328,8 @@ class Qwen3Oracle:
         for li, L in enumerate(self.layers):
             if pend is not None:
                 h = R(h + pend)                                   # one rounding
+            if taps is not None and li in taps:
+                taps[li] = {"h_in": h}
             y = self.rms(h, L["in_norm"])
             qkv = R(self.matmul(y, L["qkv"]))
             q = qkv[:, :H * D].reshape(T, H, D)
@@ -303,11 +359,17 @@ class Qwen3Oracle:
                     a[rows, hh, :] = R(self.attend(q[rows, hh, :], Kj, Vj, visible, scale))
             h = R(h + R(self.matmul(a.reshape(T, H * D), L["o"])))
             y2 = self.rms(h, L["post_norm"])
-            if cfg.is_moe_layer(li):
+            if moe_layer(cfg, li):
+                if "router" not in L:
+                    raise ValueError(f"layer {li} is a MoE layer but its weights have no router")
                 pend, idx, w = self.moe_block(li, y2)
                 moe_trace.append((idx, w))
             else:
+                if "gate_up" not in L:
+                    raise ValueError(f"layer {li} is a dense layer but its weights have no MLP")
                 pend = self.dense_mlp(L, y2)
+            if taps is not None and li in taps:
+                taps[li].update(h=h, pend=pend)
             if trace is not None:
                 trace.append({"y": y, "qkv": qkv, "q": q, "k": k, "v": v, "a": a,
                               "h": h, "y2": y2, "pend": pend})
@@ -360,11 +422,11 @@ class Qwen3Oracle:
         for e in np.unique(idx):
             tt, ss = np.nonzero(idx == e)
             xe = y2[tt]
-            Wgu = L["exp_gate_up"]["w"][e]
+            Wgu = self.expert_weight(L["exp_gate_up"], e)
             g = R(self._mm(xe, Wgu[:mI]))
             u = R(self._mm(xe, Wgu[mI:]))
             m = R(R(self.silu(g)) * u)
-            z[tt, ss] = R(self._mm(m, L["exp_down"]["w"][e]))
+            z[tt, ss] = R(self._mm(m, self.expert_weight(L["exp_down"], e)))
         pend = R(np.einsum("tk,tkh->th", w, z))
         return pend, idx, w
 

@@ -56,16 +56,21 @@ class Qwen3Config:
     moe_intermediate: int = 0
     norm_topk_prob: bool = True
     decoder_sparse_step: int = 1
+    mlp_only_layers: tuple = ()     # layers of a MoE stack that keep the dense MLP
     name: str = field(default="custom", compare=False)
 
     @property
     def qkv_rows(self) -> int:
         return (self.n_heads + 2 * self.n_kv_heads) * self.head_dim
 
-    def is_moe_layer(self, layer: int) -> bool:
-        """Qwen3-MoE layer rule (qwen3-moe.ts, Qwen3MoeDecoderLayer): a layer
-        is sparse iff experts exist and (layer + 1) % decoder_sparse_step == 0."""
-        return self.num_experts > 0 and (layer + 1) % self.decoder_sparse_step == 0
+    def has_experts(self, layer: int) -> bool:
+        """Whether the generator draws expert weights (rather than a dense MLP)
+        for this layer: the layer schedule the config describes (experts exist,
+        the layer is not in mlp_only_layers, (layer + 1) % decoder_sparse_step
+        == 0).  Only the weight layout depends on it; the oracle and the
+        library each decide a layer's kind with their own code."""
+        return (self.num_experts > 0 and layer not in tuple(self.mlp_only_layers)
+                and (layer + 1) % self.decoder_sparse_step == 0)
 
     def torch_dtype(self) -> torch.dtype:
         return DTYPES[self.dtype]
@@ -124,13 +129,19 @@ def _int8_linear(out_f, in_f, group, g, device):
     return {"w": codes, "scale": scale, "bias": bias}
 
 
+def _stack(parts):
+    """Stack per-expert int8 linears into [E, ...] codes, scales and biases."""
+    return {k: torch.stack([p[k] for p in parts]) for k in parts[0]}
+
+
 def make_weights(cfg: Qwen3Config, seed: int | None = None, device="cpu") -> dict:
     """Random-init weights with the stack's architecture.
 
     Draw order (fixed): for each layer, in_norm, post_norm, q_norm, k_norm,
     qkv, o, gate_up, down (dense layers) or router, expert gate|up, expert down
-    (MoE layers); then the final norm.  Linear weights are nn.Linear
-    ``[out, in]`` row-major; q|k|v rows and gate|up rows are concatenated
+    (MoE layers; int8 experts: every expert's gate|up codes, scales and biases,
+    then every expert's down); then the final norm.  Linear weights are
+    nn.Linear ``[out, in]`` row-major; q|k|v rows and gate|up rows are concatenated
     (the fused projections of the MLX Backbone).  Gains are 1 + N(0, 0.1),
     weights N(0, 0.02).
     """
@@ -154,11 +165,15 @@ def make_weights(cfg: Qwen3Config, seed: int | None = None, device="cpu") -> dic
             "qkv": lin(cfg.qkv_rows, H),
             "o": lin(H, cfg.n_heads * D),
         }
-        if cfg.is_moe_layer(i):
+        if cfg.has_experts(i):
             E, mI = cfg.num_experts, cfg.moe_intermediate
             L["router"] = {"w": _normal((E, H), 0.02, g, device, dt)}
-            L["exp_gate_up"] = {"w": _normal((E, 2 * mI, H), 0.02, g, device, dt)}
-            L["exp_down"] = {"w": _normal((E, H, mI), 0.02, g, device, dt)}
+            if cfg.weight_format == "int8":
+                L["exp_gate_up"] = _stack([_int8_linear(2 * mI, H, cfg.group_size, g, device) for _ in range(E)])
+                L["exp_down"] = _stack([_int8_linear(H, mI, cfg.group_size, g, device) for _ in range(E)])
+            else:
+                L["exp_gate_up"] = {"w": _normal((E, 2 * mI, H), 0.02, g, device, dt)}
+                L["exp_down"] = {"w": _normal((E, H, mI), 0.02, g, device, dt)}
         else:
             L["gate_up"] = lin(2 * cfg.intermediate, H)
             L["down"] = lin(H, cfg.intermediate)

@@ -14,8 +14,9 @@ import pytest
 import torch
 import torch.nn.functional as F
 
-from oracle import (Qwen3Oracle, rnd, rms_norm, rope, rope_table, softmax, attention_probs,
-                    silu, dequant_affine, router_topk)
+from oracle import (Qwen3Oracle, Qwen3OracleF32Acc, rnd, rms_norm, rope, rope_table, softmax,
+                    attention_probs, silu, dequant_affine, router_topk, moe_layer, embed_rows, head_logits,
+                    l2_pool_last)
 from qwen3_decoder_layer_gb300 import inputs as I
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -214,7 +215,7 @@ def _brute_force(cfg, w, x):
         a = torch.einsum("htu,uhd->thd", torch.softmax(S, -1), v).reshape(T, H * D)
         h = h + a @ d(L["o"]["w"]).T
         y2 = F.rms_norm(h, (hid,), d(L["post_norm"]), eps)
-        if cfg.is_moe_layer(li):
+        if "router" in L:                       # the layer's kind from the weights it was given
             mI = cfg.moe_intermediate
             P = torch.softmax(y2 @ d(L["router"]["w"]).T, -1)
             wk, ik = torch.topk(P, cfg.top_k, dim=-1)
@@ -393,3 +394,151 @@ def test_int8_stack_equals_dense_stack_on_dequantised_weights():
     a = Qwen3Oracle(cfg, w, prec="exact").forward(x)
     b = Qwen3Oracle(I.with_sizes(cfg, weight_format="dense"), dense, prec="exact").forward(x)
     assert np.max(np.abs(a - b)) < 1e-12
+
+
+# ---------------------------------------------------------------- mixed dense / MoE stacks
+@pytest.mark.parametrize("step,mlp_only,expect", [
+    (1, (), [0, 1, 2, 3, 4, 5]),
+    (2, (), [1, 3, 5]),
+    (2, (3,), [1, 5]),
+    (3, (0, 2), [5]),
+    (1, (0, 1, 2, 3, 4, 5), []),
+])
+def test_moe_layer_rule(step, mlp_only, expect):
+    """qwen3-moe.ts Qwen3MoeDecoderLayer: a layer is sparse iff it is not in
+    mlp_only_layers and (index + 1) % decoder_sparse_step == 0 (enumerated by
+    hand for six layers); without experts no layer is sparse."""
+    cfg = I.with_sizes(TINY_MOE, num_layers=6, decoder_sparse_step=step, mlp_only_layers=mlp_only)
+    assert [i for i in range(6) if moe_layer(cfg, i)] == expect
+    assert not any(moe_layer(I.with_sizes(cfg, num_experts=0), i) for i in range(6))
+
+
+MIXED = I.with_sizes(TINY_MOE, name="pin_mixed", num_layers=4, decoder_sparse_step=2, mlp_only_layers=(3,))
+
+
+def test_mixed_stack_matches_brute_force():
+    """A 4-layer stack with decoder_sparse_step 2 and layer 3 kept dense (only
+    layer 1 sparse) equals the brute-force forward, which reads each layer's
+    kind from the weights it is given."""
+    w = I.make_weights(MIXED, seed=23)
+    assert ["router" in L for L in w["layers"]] == [False, True, False, False]
+    x = I.make_rows(MIXED, 10, seed=24)
+    got = Qwen3Oracle(MIXED, w, prec="exact").forward(x)
+    assert np.max(np.abs(got - _brute_force(MIXED, w, x))) < 1e-12
+
+
+def test_oracle_refuses_weights_of_another_schedule():
+    w = I.make_weights(MIXED, seed=25)
+    other = I.with_sizes(MIXED, mlp_only_layers=())      # layer 3 would be sparse
+    with pytest.raises(ValueError):
+        Qwen3Oracle(other, w, prec="exact").forward(I.make_rows(MIXED, 2, seed=26))
+
+
+def test_int8_experts_equal_dense_experts_on_dequantised_weights():
+    """int8 experts (stacked affine-quantised matrices, QuantizedSwitchLinear)
+    equal the same MoE stack with each expert matrix dequantised explicitly."""
+    cfg = I.with_sizes(TINY_MOE, dtype="bf16", weight_format="int8", group_size=16, name="pin_int8_moe")
+    w = I.make_weights(cfg, seed=27)
+    dense = {"final_norm": w["final_norm"], "layers": []}
+    for L in w["layers"]:
+        D2 = {}
+        for k, v in L.items():
+            if isinstance(v, dict) and "scale" in v:
+                codes, sc, bi = v["w"].numpy(), v["scale"].double().numpy(), v["bias"].double().numpy()
+                if codes.ndim == 3:
+                    mats = [dequant_affine(codes[e], sc[e], bi[e], 16) for e in range(codes.shape[0])]
+                    D2[k] = {"w": torch.from_numpy(np.stack(mats))}
+                else:
+                    D2[k] = {"w": torch.from_numpy(dequant_affine(codes, sc, bi, 16))}
+            else:
+                D2[k] = v
+        dense["layers"].append(D2)
+    assert w["layers"][0]["exp_gate_up"]["w"].dtype == torch.uint8
+    x = I.make_rows(cfg, 7, seed=28)
+    a = Qwen3Oracle(cfg, w, prec="exact").forward(x)
+    b = Qwen3Oracle(I.with_sizes(cfg, weight_format="dense"), dense, prec="exact").forward(x)
+    assert np.max(np.abs(a - b)) < 1e-12
+
+
+# ---------------------------------------------------------------- embedding, output head, pooling
+def test_embed_rows_is_a_row_gather():
+    """Backbone.embed_tokens: the table's rows at the ids (torch's embedding)."""
+    rng = np.random.default_rng(111)
+    table = torch.from_numpy(rng.standard_normal((50, 24))).to(torch.bfloat16)
+    ids = [3, 49, 0, 3, 17]
+    ref = F.embedding(torch.tensor(ids), table).double().numpy()
+    assert np.array_equal(embed_rows(table.double().numpy(), ids, "bf16"), ref)
+
+
+def test_head_logits_round_once_then_widen():
+    """Backbone.cb0_logits: x W^T in the model dtype, then fp32.  A non-square
+    head (2049 outputs, as cb0_head) against torch's float64 linear rounded by
+    torch's own bf16 cast; a tied head is the product with the embedding table."""
+    rng = np.random.default_rng(112)
+    x = rnd(rng.standard_normal((3, 64)), "bf16")
+    W = rnd(0.05 * rng.standard_normal((2049, 64)), "bf16")
+    got = head_logits(x, W, "bf16")
+    ref = F.linear(torch.from_numpy(x), torch.from_numpy(W)).to(torch.bfloat16).float().double().numpy()
+    assert got.shape == (3, 2049) and np.array_equal(got, ref)
+    table = rnd(rng.standard_normal((40, 64)), "bf16")
+    tied = head_logits(x, table, "exact")
+    assert np.allclose(tied, np.einsum("th,vh->tv", x, table), rtol=0, atol=1e-12)
+
+
+def test_l2_pool_last_unit_norm_and_torch_ops():
+    """qwen3.ts embedPooled: the last row over its L2 norm.  Exact mode: unit
+    norm, parallel to the last row, blind to earlier rows and to the row's
+    scale.  bf16: the page's four array operations run as torch bf16 ops."""
+    rng = np.random.default_rng(113)
+    h = rng.standard_normal((5, 64))
+    v = l2_pool_last(h, "exact")
+    assert abs(np.linalg.norm(v) - 1) < 1e-14 and np.allclose(v, h[-1] / np.linalg.norm(h[-1]), atol=1e-15)
+    h2 = h.copy()
+    h2[:-1] = 0
+    h2[-1] *= 37.0
+    assert np.allclose(l2_pool_last(h2, "exact"), v, atol=1e-14)
+    hb = rnd(h, "bf16")
+    t = torch.from_numpy(hb[-1]).to(torch.bfloat16)
+    sq = torch.square(t)
+    ss = torch.sum(sq.float()).to(torch.bfloat16)
+    ref = (t / torch.sqrt(ss)).double().numpy()
+    assert np.array_equal(l2_pool_last(hb, "bf16"), ref)
+
+
+# ---------------------------------------------------------------- the float32 twin
+def test_twin_steps_equal_oracle_steps_to_float32_precision():
+    """Qwen3OracleF32Acc restates each step in float32: on non-square random
+    inputs every step equals the oracle's float64 step to float32 precision,
+    so a dropped term, a wrong sign or a transposed operand in the twin fails."""
+    cfg = I.with_sizes(TINY, dtype="fp32")
+    w = I.make_weights(cfg, seed=121)
+    o, t = Qwen3Oracle(cfg, w, prec="exact"), Qwen3OracleF32Acc(cfg, w, prec="exact")
+    rng = np.random.default_rng(122)
+    v = rng.standard_normal((6, 64))
+    g = 1 + 0.1 * rng.standard_normal(64)
+    rel = lambda a, b: np.max(np.abs(a - b)) / np.max(np.abs(b))
+    assert rel(t.rms(v, g), o.rms(v, g)) < 1e-6
+    x = rng.standard_normal((6, 4, 16))
+    c, s = rope_table(50, 16, 1e4, "exact")
+    pos = np.array([0, 3, 9, 17, 33, 49])
+    assert rel(t.rope(x, c[pos][:, None], s[pos][:, None]), o.rope(x, c[pos][:, None], s[pos][:, None])) < 1e-6
+    q, K, V = rng.standard_normal((3, 16)), rng.standard_normal((11, 16)), rng.standard_normal((11, 16))
+    vis = np.arange(11)[None, :] <= np.array([4, 7, 10])[:, None]
+    assert rel(t.attend(q, K, V, vis, 0.25), o.attend(q, K, V, vis, 0.25)) < 1e-5
+    gg = 4 * rng.standard_normal(100)
+    assert rel(t.silu(gg), o.silu(gg)) < 1e-6
+    A, B = rng.standard_normal((5, 64)), rng.standard_normal((9, 64))
+    assert rel(t._mm(A, B), o._mm(A, B)) < 1e-5
+
+
+def test_twin_bf16_drift_is_zero_on_the_tiny_stack_and_small_in_fp32():
+    """On the 2-layer 256-wide workload the twin's bf16 rounding decisions all
+    agree with the oracle's (zero drift); in fp32 its distance is float32 noise."""
+    for dtype, bound in (("bf16", 0.0), ("fp32", 2e-6)):
+        cfg = I.with_sizes(I.TINY_FP32, dtype=dtype)
+        w = I.make_weights(cfg, seed=7)
+        o, t = Qwen3Oracle(cfg, w), Qwen3OracleF32Acc(cfg, w)
+        for n in (16, 1, 1):
+            x = I.make_rows(cfg, n, seed=100 + n)
+            a, b = o.forward(x), t.forward(x)
+            assert np.max(np.abs(a - b)) / np.sqrt(np.mean(a * a)) <= bound
