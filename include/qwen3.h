@@ -79,7 +79,7 @@ typedef struct {
   int32_t capacity;          /* static KV-cache positions per sequence */
   int32_t max_seqs;          /* independent sequences held by the cache */
   int32_t dtype;             /* QWEN3_DTYPE_F32 or QWEN3_DTYPE_BF16 */
-  int32_t weight_format;     /* QWEN3_WEIGHTS_DENSE or QWEN3_WEIGHTS_INT8 (dense layers' linears) */
+  int32_t weight_format;     /* QWEN3_WEIGHTS_DENSE or QWEN3_WEIGHTS_INT8 (every linear but the router) */
   int32_t group_size;        /* int8 group along the input dim (64); multiple of 16 */
   int32_t num_experts;       /* 0 = dense stack */
   int32_t top_k;             /* num_experts_per_tok */
@@ -112,9 +112,12 @@ typedef struct {
   qwen3_linear o;            /* [hidden, n_heads head_dim] */
   qwen3_linear gate_up;      /* dense layers: [2 intermediate, hidden], rows gate | up */
   qwen3_linear down;         /* dense layers: [hidden, intermediate] */
-  const void* router;        /* MoE layers: dt [num_experts, hidden] (the `gate` Linear) */
-  const void* exp_gate_up;   /* MoE layers: dt [num_experts, 2 moe_intermediate, hidden], per expert rows gate | up */
-  const void* exp_down;      /* MoE layers: dt [num_experts, hidden, moe_intermediate] */
+  const void* router;        /* MoE layers: dt [num_experts, hidden] (the `gate` Linear; never quantised) */
+  qwen3_linear exp_gate_up;  /* MoE layers: [num_experts, 2 moe_intermediate, hidden], per expert rows gate | up */
+  qwen3_linear exp_down;     /* MoE layers: [num_experts, hidden, moe_intermediate] */
+  /* Expert linears follow weight_format like the others: dense dt, or int8
+   * codes with bf16 scale / bias [num_experts, rows, in / group_size] (the
+   * stacked quantised expert matrices of qwen3-moe.ts QuantizedSwitchLinear). */
 } qwen3_layer_weights;
 
 /* Validate a config on the host only (no device work).  QWEN3_OK or the
@@ -199,6 +202,46 @@ QWEN3_API qwen3_status qwen3_moe_layer(qwen3_handle* h, int32_t layer, const voi
 QWEN3_API qwen3_status qwen3_moe_layer_static(qwen3_handle* h, int32_t layer, const void* y, int32_t T, void* out,
                                     int32_t* topk_idx, float* topk_w, void* stream);
 
+/* Embedding rows (maya2_mlx/backbone.py, Backbone.embed_tokens: the rows of
+ * the embedding table at the token ids, in the model dtype):
+ *   table  dt [vocab, hidden] device, caller-owned, 16-byte aligned
+ *   ids    int32 [n] HOST, each in [0, vocab) (checked before any work:
+ *          QWEN3_E_ARG names the first bad id)
+ *   out    dt [n, hidden] device
+ * out[t] = table[ids[t]].  The ids are copied to the device on `stream`. */
+QWEN3_API qwen3_status qwen3_embed(qwen3_handle* h, const void* table, int32_t vocab, const int32_t* ids, int32_t n,
+                         void* out, void* stream);
+
+/* Output head (maya2_mlx/backbone.py, Backbone.cb0_logits: the product with
+ * the head's matrix in the model dtype, then fp32; @mlx-bun/inference
+ * qwen3-moe.ts / qwen3.ts: a separate lm_head, or the tied embedding's
+ * asLinear):
+ *   w       dt [n_out, hidden] device (the head's nn.Linear weight, or the
+ *           embedding table for a tied head), 16-byte aligned
+ *   x       dt [T, hidden] device: final-norm hidden states
+ *   logits  fp32 [T, n_out] device
+ * logits[t, o] = fp32(R(sum_k x[t, k] w[o, k])): accumulated in fp32, rounded
+ * once to the model dtype, widened exactly.  Any n_out (e.g. 2049). */
+QWEN3_API qwen3_status qwen3_head(qwen3_handle* h, const void* w, int32_t n_out, const void* x, int32_t T,
+                        float* logits, void* stream);
+
+/* Pooled sentence vector (@mlx-bun/inference qwen3.ts, embedPooled): clears
+ * sequence `seq` (as qwen3_reset), runs the stack over the T rows of x at
+ * positions 0..T-1 of that sequence, and writes the last row's final-norm
+ * hidden state v divided by its L2 norm:
+ *   out = R(v / R(sqrt(R(sum_k R(v_k^2)))))   (each array operation of the page
+ *   rounded to the model dtype; the sum accumulated in fp32)
+ *   x    dt [T, hidden] device (embedded tokens, the pooling token last)
+ *   out  dt [hidden] device
+ * T must be in [1, capacity] (QWEN3_E_CAPACITY otherwise).  Sequence `seq`
+ * ends holding these T positions. */
+QWEN3_API qwen3_status qwen3_embed_pooled(qwen3_handle* h, const void* x, int32_t T, int32_t seq, void* out,
+                                void* stream);
+
+/* Device bytes held by the handle's grow-only workspace (everything the
+ * handle allocates after qwen3_create apart from pinned host staging). */
+QWEN3_API qwen3_status qwen3_workspace_bytes(const qwen3_handle* h, int64_t* bytes);
+
 /* Device pointers of one (sequence, layer) cache slab: K and V, each dt
  * [n_kv_heads][capacity][head_dim], K post-RoPE.  Owned by the library; valid
  * until qwen3_destroy.  Used to pre-fill a cache, then qwen3_set_length. */
@@ -214,7 +257,10 @@ QWEN3_API qwen3_status qwen3_get_length(const qwen3_handle* h, int32_t seq, int3
 #define QWEN3_OPT_PDL 3           /* 1 (default) = programmatic dependent launch between kernels */
 #define QWEN3_OPT_TENSOR_CORES 4  /* 1 (default) = tcgen05 for bf16 prefill linears and attention, MoE expert GEMMs, and int8 linears of 5..32 rows; 0 = CUDA cores */
 #define QWEN3_OPT_L2_PREFETCH 5   /* 1 (default) = decode kernels prefetch the next linear's weights into L2 */
-#define QWEN3_OPT_FUSED_DECODE 6  /* 1 = dense decode steps run as one persistent cooperative kernel; 0 (default) = five kernels per layer */
+#define QWEN3_OPT_CLUSTER_ATTENTION 8 /* 1 (default) = decode attention of few sequences on thread-block clusters
+                                         (partials merged in distributed shared memory); 0 = split-K with a global merge */
+#define QWEN3_OPT_FAIL_ALLOC 7    /* failure injection: n > 0 makes the n-th next workspace allocation fail as if
+                                     cudaMalloc had (QWEN3_E_OOM, no state change); 0 (default) = off */
 QWEN3_API qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value);
 
 /* Kernel timing collected while QWEN3_OPT_PROFILE is on (synchronises the
@@ -229,6 +275,13 @@ QWEN3_API qwen3_status qwen3_profile_reset(qwen3_handle* h);
  * was owed (a TMA copy that never completed), QWEN3_OK with *code = 0
  * otherwise.  Kernels never trap; they record the code and return. */
 QWEN3_API qwen3_status qwen3_device_error(qwen3_handle* h, int32_t* code);
+
+/* Self test of the device-side failure report: enqueues one kernel that
+ * waits for an mbarrier nothing completes, with the same bounded wait the
+ * library's kernels use; after its limit (about a second) it records code 99
+ * and returns, so the next qwen3_device_error reports QWEN3_E_DEVICE with
+ * code 99 and the context stays usable.  No counterpart on the pages. */
+QWEN3_API qwen3_status qwen3_selftest_bounded_wait(qwen3_handle* h, void* stream);
 
 /* Number of kernel launches made by the last successful qwen3_forward. */
 QWEN3_API int64_t qwen3_last_launch_count(const qwen3_handle* h);

@@ -22,7 +22,8 @@ STATUS = {0: "QWEN3_OK", 1: "QWEN3_E_ARG", 2: "QWEN3_E_DTYPE", 3: "QWEN3_E_CAPAC
           8: "QWEN3_E_UNSUPPORTED", 9: "QWEN3_E_DEVICE"}
 QWEN3_OPT_CUDA_GRAPHS, QWEN3_OPT_PROFILE, QWEN3_OPT_PDL, QWEN3_OPT_TENSOR_CORES = 1, 2, 3, 4
 QWEN3_OPT_L2_PREFETCH = 5
-QWEN3_OPT_FUSED_DECODE = 6
+QWEN3_OPT_FAIL_ALLOC = 7
+QWEN3_OPT_CLUSTER_ATTENTION = 8
 
 
 class Qwen3Error(RuntimeError):
@@ -54,7 +55,7 @@ class qwen3_layer_weights(ctypes.Structure):
                 ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
                 ("qkv", qwen3_linear), ("o", qwen3_linear), ("gate_up", qwen3_linear),
                 ("down", qwen3_linear), ("router", ctypes.c_void_p),
-                ("exp_gate_up", ctypes.c_void_p), ("exp_down", ctypes.c_void_p)]
+                ("exp_gate_up", qwen3_linear), ("exp_down", qwen3_linear)]
 
 
 _P = ctypes.c_void_p
@@ -69,6 +70,10 @@ _SIGS = {
     "qwen3_forward": (_I32, [_P, _P, _I32, _PI32, _PI32, _P, _P]),
     "qwen3_moe_layer": (_I32, [_P, _I32, _P, _I32, _P, _P, _P, _P]),
     "qwen3_moe_layer_static": (_I32, [_P, _I32, _P, _I32, _P, _P, _P, _P]),
+    "qwen3_embed": (_I32, [_P, _P, _I32, _PI32, _I32, _P, _P]),
+    "qwen3_head": (_I32, [_P, _P, _I32, _P, _I32, _P, _P]),
+    "qwen3_embed_pooled": (_I32, [_P, _P, _I32, _I32, _P, _P]),
+    "qwen3_workspace_bytes": (_I32, [_P, ctypes.POINTER(ctypes.c_int64)]),
     "qwen3_cache_view": (_I32, [_P, _I32, _I32, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
     "qwen3_set_length": (_I32, [_P, _I32, _I32]),
     "qwen3_get_length": (_I32, [_P, _I32, _PI32]),
@@ -79,6 +84,7 @@ _SIGS = {
     "qwen3_profile_reset": (_I32, [_P]),
     "qwen3_last_launch_count": (ctypes.c_int64, [_P]),
     "qwen3_device_error": (_I32, [_P, _PI32]),
+    "qwen3_selftest_bounded_wait": (_I32, [_P, _P]),
     "qwen3_last_error": (ctypes.c_char_p, [_P]),
     "qwen3_status_string": (ctypes.c_char_p, [_I32]),
 }
@@ -130,8 +136,10 @@ def make_config(cfg) -> qwen3_config:
     c.dtype = {"fp32": 0, "bf16": 1}.get(cfg.dtype, 99)
     c.weight_format = {"dense": 0, "int8": 1}[cfg.weight_format]
     c.norm_topk_prob = int(bool(cfg.norm_topk_prob))
-    c.mlp_only_layers = None
-    c.n_mlp_only_layers = 0
+    dense = [int(i) for i in getattr(cfg, "mlp_only_layers", ())]
+    c._mlp_only = (ctypes.c_int32 * max(len(dense), 1))(*dense)   # kept alive with the struct
+    c.mlp_only_layers = ctypes.cast(c._mlp_only, ctypes.POINTER(ctypes.c_int32)) if dense else None
+    c.n_mlp_only_layers = len(dense)
     return c
 
 
@@ -156,8 +164,9 @@ def qwen3_create(cfg, weights: dict):
                 setattr(w, name, qwen3_linear(_ptr(lw["w"]), _ptr(lw.get("scale")), _ptr(lw.get("bias"))))
         if "router" in L:
             w.router = _ptr(L["router"]["w"])
-            w.exp_gate_up = _ptr(L["exp_gate_up"]["w"])
-            w.exp_down = _ptr(L["exp_down"]["w"])
+            for name in ("exp_gate_up", "exp_down"):
+                lw = L[name]
+                setattr(w, name, qwen3_linear(_ptr(lw["w"]), _ptr(lw.get("scale")), _ptr(lw.get("bias"))))
     h = ctypes.c_void_p()
     st = lib().qwen3_create(ctypes.byref(c), arr, _ptr(weights["final_norm"]), ctypes.byref(h))
     if st != QWEN3_OK:
@@ -190,6 +199,31 @@ def qwen3_moe_layer_static(h, layer: int, y, out, topk_idx, topk_w, stream=None)
     (no allocation; T bounded by that array's size)."""
     _check(h, lib().qwen3_moe_layer_static(h, layer, _ptr(y), int(y.shape[0]), _ptr(out), _ptr(topk_idx),
                                            _ptr(topk_w), _stream(stream)))
+
+
+def qwen3_embed(h, table, ids, out, stream=None) -> None:
+    """out[t] = table[ids[t]] (ids: a list of host ints)."""
+    n = len(ids)
+    arr = (ctypes.c_int32 * n)(*[int(i) for i in ids])
+    _check(h, lib().qwen3_embed(h, _ptr(table), int(table.shape[0]), arr, n, _ptr(out), _stream(stream)))
+
+
+def qwen3_head(h, w, x, logits, stream=None) -> None:
+    """logits fp32 [T, n_out] = fp32(R(x w^T))."""
+    _check(h, lib().qwen3_head(h, _ptr(w), int(w.shape[0]), _ptr(x), int(x.shape[0]), _ptr(logits),
+                               _stream(stream)))
+
+
+def qwen3_embed_pooled(h, x, seq: int, out, stream=None) -> None:
+    """out [hidden] = the last row's final-norm hidden state over its L2 norm,
+    after running the T rows of x from position 0 of sequence `seq`."""
+    _check(h, lib().qwen3_embed_pooled(h, _ptr(x), int(x.shape[0]), int(seq), _ptr(out), _stream(stream)))
+
+
+def qwen3_workspace_bytes(h) -> int:
+    n = ctypes.c_int64()
+    _check(h, lib().qwen3_workspace_bytes(h, ctypes.byref(n)))
+    return n.value
 
 
 def qwen3_cache_view(h, seq: int, layer: int):
@@ -240,6 +274,10 @@ def qwen3_device_error(h) -> int:
     if st not in (QWEN3_OK, 9):
         _check(h, st)
     return code.value
+
+
+def qwen3_selftest_bounded_wait(h, stream=None) -> None:
+    _check(h, lib().qwen3_selftest_bounded_wait(h, _stream(stream)))
 
 
 def qwen3_last_error(h) -> str:

@@ -22,8 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libqwen3_gb300.so")
 
 SOURCES = ["runtime.cpp", "norm.cu", "gemv.cu", "gemm_simt.cu", "attention.cu", "moe.cu", "decode.cu", "attn_decode.cu", "gemm_tc.cu",
-           "attn_tc.cu", "moe_static.cu", "gemm_skinny.cu", "gemm_w8_tc.cu",
-           "decode_fused.cu", "decode_fused_bf16.cu", "decode_fused_bf16_u8.cu", "decode_fused_f32.cu"]
+           "attn_tc.cu", "head.cu", "moe_static.cu", "gemm_skinny.cu", "gemm_w8_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -190,12 +190,8 @@ int attn_prefill_nq_max() { return PRE_NQ; }
 template <typename Dt, int D>
 static cudaError_t launch_pre(const LaunchCtx& c, const AttnArgs& a) {
   auto kern = attn_prefill_kernel<Dt, D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prefill_smem<D>());
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_max_smem((const void*)kern, (int)prefill_smem<D>());
+  if (e != cudaSuccess) return e;
   return launch_k(kern, dim3(a.grid_x, a.KV), dim3(PRE_THREADS), prefill_smem<D>(), c, a);
 }
 

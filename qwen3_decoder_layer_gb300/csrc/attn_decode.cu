@@ -68,12 +68,44 @@ template <typename Dt, int D, int NQ> struct ADLayout {
   static constexpr size_t OFF_MRG = OFF_WP + WP_FLOATS * 4;                       // [NQ][MPITCH] merge scratch
   static constexpr size_t OFF_BAR = (OFF_MRG + (size_t)NQ * MPITCH * 4 + 15) & ~size_t(15);
   static constexpr size_t TOTAL = OFF_BAR + 2 * STAGES * 8 + 16;
+  // cluster variant: this CTA's merged partial [NQ][D + 2] (o, then m and l),
+  // read by the other CTAs of the cluster
+  static constexpr int CPITCH = D + 2;
+  static constexpr size_t OFF_CP = (TOTAL + 15) & ~size_t(15);
+  static constexpr size_t TOTAL_CL = OFF_CP + (size_t)NQ * CPITCH * 4;
 };
 
 // Named barrier over the consumer warps only.
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(AD_CTHREADS) : "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Thread-block cluster: rank of this CTA, CTAs in the cluster, a barrier over
+// every thread of the cluster (release / acquire), and loads from another
+// CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // Keys of an item: [key0, key0 + nkeys) in nsub sub-chunks.
@@ -816,20 +848,245 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
   }
 }
 
+// One (query block, kv head) per thread-block cluster (batch-1 and small
+// batches): the cluster's CTAs split the block's keys 0..last into equal runs
+// of whole sub-chunks, each CTA loads its whole run into its ring at launch
+// (every stage used once, no refills), its warps compute as in the kernels
+// above, the warp partials merge into the CTA's partial in shared memory, and
+// after a cluster barrier each CTA combines one slice of the output elements
+// from all the CTAs' partials through distributed shared memory:
+// out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c, rounded once.  No
+// partial goes through global memory and no CTA waits on another's atomic.
+template <typename Dt, int D, int NQ>
+__global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(AttnDecArgs a) {
+  extern __shared__ __align__(128) uint8_t ad_smem[];
+  using LY = ADLayout<Dt, D, NQ>;
+  constexpr int CK = LY::CK;
+  constexpr int KW = LY::KW;
+  constexpr int DPL = D / 32;
+  constexpr int WP = LY::WPITCH;
+  constexpr int MP = LY::MPITCH;
+  constexpr int CP = LY::CPITCH;
+  float* qs = reinterpret_cast<float*>(ad_smem + LY::OFF_QS);
+  float* ps_all = reinterpret_cast<float*>(ad_smem + LY::OFF_PS);
+  float* wp = reinterpret_cast<float*>(ad_smem + LY::OFF_WP);
+  float* mrg = reinterpret_cast<float*>(ad_smem + LY::OFF_MRG);
+  float* cp = reinterpret_cast<float*>(ad_smem + LY::OFF_CP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ad_smem + LY::OFF_BAR);
+  __shared__ int s_fail;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = blockIdx.y;
+  const int G = a.H / a.KV;
+  const int qkv_ld = (a.H + 2 * a.KV) * D;
+  const uint32_t rank = cluster_rank(), ncl = cluster_size();
+  const AttnQBlock qb = a.qblocks[blockIdx.x / ncl];
+  const int nq = qb.nrows * G;  // <= NQ
+  // this CTA's keys: whole sub-chunks, [k_lo, k_hi) of 0 .. last position
+  const int n_keys = qb.pos0 + qb.nrows;
+  const int per = ((n_keys + (int)ncl - 1) / (int)ncl + CK - 1) / CK * CK;
+  const int k_lo = min((int)rank * per, n_keys), k_hi = min(k_lo + per, n_keys);
+  int nsub = (k_hi - k_lo + CK - 1) / CK;  // <= LY::STAGES (the host checks attn_decode_cluster_keys)
+  auto tiles = [&](int s) { return ad_smem + (size_t)s * LY::STAGE; };
+
+  if (tid == 0) {
+    for (int s = 0; s < LY::STAGES; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+    s_fail = 0;
+    if (nsub > LY::STAGES) {  // a run longer than the ring: refuse rather than overrun it
+      atomicExch(a.err, 14);
+      s_fail = 1;
+    }
+  }
+  if (nsub > LY::STAGES) nsub = 0;
+  __syncthreads();
+
+  if (warp == AD_CWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const Dt* kc = static_cast<const Dt*>(a.kc);
+      const Dt* vc = static_cast<const Dt*>(a.vc);
+      for (int sub = 0; sub < nsub && sub < LY::STAGES; ++sub) {
+        const int k0 = k_lo + sub * CK;
+        const int nk = min(CK, k_hi - k0);
+        const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
+        const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
+        mbar_expect_tx(&full[sub], 2 * bytes);
+        tma_load_1d(tiles(sub), kc + off, bytes, &full[sub]);
+        tma_load_1d(tiles(sub) + LY::TILE, vc + off, bytes, &full[sub]);
+      }
+      if (a.pf && a.pf_bytes) {  // L2 prefetch of this CTA's share of the next kernel's operand
+        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+        const size_t pshare = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
+        for (size_t b0 = pshare * b, b1 = min(pshare * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
+          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- consumers
+    pdl_wait();
+    pdl_launch();
+    const Dt* qkv = static_cast<const Dt*>(a.qkv);
+    float* ps = ps_all + (size_t)warp * NQ * KW;
+    const int wsub = warp / AD_WPS;
+    const int wk0 = (warp % AD_WPS) * KW;
+    if (warp < NQ) {  // queries: RMSNorm + RoPE (warp per query)
+      const int i = warp;
+      float x[DPL];
+      if (i < nq) {
+        const int row = qb.row0 + i / G, hh = j * G + i % G;
+        const Dt* src = qkv + (size_t)row * qkv_ld + (size_t)hh * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) x[e] = to_f(src[e]);
+        norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.q_gain), a.cos_t, a.sin_t, qb.pos0 + i / G, a.eps);
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) x[e] = 0.f;
+      }
+      store_lane_vec<DPL>(qs + i * D + lane * DPL, x);
+    }
+    csync();
+    float m_w[NQ], l_w[NQ], o_w[NQ][DPL];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      m_w[i] = -CUDART_INF_F;
+      l_w[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
+    }
+    for (int sub = wsub; sub < nsub; sub += AD_SUBS) {
+      const int key0 = k_lo + sub * CK;
+      const int nk = min(KW, k_hi - key0 - wk0);
+      Dt* Kt = reinterpret_cast<Dt*>(tiles(sub)) + (size_t)wk0 * D;
+      Dt* Vt = reinterpret_cast<Dt*>(tiles(sub) + LY::TILE) + (size_t)wk0 * D;
+      int landed = 1;
+      if (lane == 0) landed = mbar_wait(&full[sub], 0u, a.err, 2);
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, landed, 0)) {
+        s_fail = 1;
+        break;
+      }
+      if (nk <= 0) continue;
+      const int kb = key0 + wk0;
+      const int n0 = max(kb, qb.seg_pos0), n1 = min(kb + nk, qb.seg_pos0 + qb.seg_n);
+      for (int u = n0; u < n1; ++u) {  // keys appended by this call: from the qkv row
+        const int row = qb.seg_row0 + (u - qb.seg_pos0);
+        float x[DPL], v[DPL];
+        const Dt* ksrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + j) * D + lane * DPL;
+        const Dt* vsrc = qkv + (size_t)row * qkv_ld + (size_t)(a.H + a.KV + j) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) { x[e] = to_f(ksrc[e]); v[e] = to_f(vsrc[e]); }
+        norm_rope_head<Dt, D>(x, static_cast<const Dt*>(a.k_gain), a.cos_t, a.sin_t, u, a.eps);
+        const bool owner = row >= qb.row0 && row < qb.row0 + qb.nrows;
+        const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          Kt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(x[e]);
+          Vt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+          if (owner) {
+            static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
+            static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
+          }
+        }
+      }
+      __syncwarp();
+      warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale, m_w, l_w, o_w);
+#pragma unroll 4
+      for (int u = 0; u < nk; ++u) {
+        float v[DPL];
+        load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          const float p = ps[i * KW + u];
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o_w[i][e] = fmaf(p, v[e], o_w[i][e]);
+        }
+      }
+    }
+    // warp partials -> the CTA's partial cp[i] = (sum_w f_w o_w, M, sum_w f_w l_w)
+    float* mine = wp + (size_t)warp * NQ * WP;
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      store_lane_vec<DPL>(mine + i * WP + lane * DPL, o_w[i]);
+      if (lane == 0) { mine[i * WP + D] = m_w[i]; mine[i * WP + D + 1] = l_w[i]; }
+    }
+    csync();
+    if (warp < NQ) {
+      const int i = warp;
+      const float m = lane < AD_CWARPS ? wp[((size_t)lane * NQ + i) * WP + D] : -CUDART_INF_F;
+      const float M = warp_max(m);
+      const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+      const float L = warp_sum(lane < AD_CWARPS ? f * wp[((size_t)lane * NQ + i) * WP + D + 1] : 0.f);
+      if (lane < AD_CWARPS) mrg[i * MP + lane] = f;
+      if (lane == 0) { cp[i * CP + D] = M; cp[i * CP + D + 1] = L; }
+    }
+    csync();
+    for (int idx = tid; idx < NQ * D; idx += AD_CTHREADS) {
+      const int i = idx / D, d = idx % D;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < AD_CWARPS; ++w) v = fmaf(wp[((size_t)w * NQ + i) * WP + d], mrg[i * MP + w], v);
+      cp[i * CP + d] = v;
+    }
+  }
+  // every CTA's partial is in its shared memory
+  __syncwarp();
+  cluster_sync_all();
+  if (warp < AD_CWARPS && !s_fail) {
+    // this CTA's slice of the nq x D outputs, combined over the cluster
+    const int total = nq * D;
+    const int share = (total + (int)ncl - 1) / (int)ncl;
+    const uint32_t cp_addr = smem_u32(cp);
+    for (int idx = (int)rank * share + tid; idx < min(total, ((int)rank + 1) * share); idx += AD_CTHREADS) {
+      const int i = idx / D, d = idx % D;
+      float M = -CUDART_INF_F;
+      for (uint32_t c = 0; c < ncl; ++c)
+        M = fmaxf(M, ld_cluster(cluster_map(cp_addr + (uint32_t)(i * CP + D) * 4u, c)));
+      float L = 0.f, v = 0.f;
+      for (uint32_t c = 0; c < ncl; ++c) {
+        const uint32_t base = cluster_map(cp_addr + (uint32_t)(i * CP) * 4u, c);
+        const float m = ld_cluster(base + (uint32_t)D * 4u);
+        const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
+        L = fmaf(ld_cluster(base + (uint32_t)(D + 1) * 4u), f, L);
+        v = fmaf(ld_cluster(base + (uint32_t)d * 4u), f, v);
+      }
+      const int row = qb.row0 + i / G, head = j * G + i % G;
+      static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / L);
+    }
+  }
+  // no CTA leaves (freeing its shared memory) while another may still read it
+  cluster_sync_all();
+}
+
 template <typename Dt, int D, int NQ>
 cudaError_t ad_launch(const LaunchCtx& c, const AttnDecArgs& a) {
-  auto kern = a.runs ? attn_decode_kernel<Dt, D, NQ> : attn_decode_item_kernel<Dt, D, NQ>;
   using LY = ADLayout<Dt, D, NQ>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<Dt, D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)LY::TOTAL);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_decode_item_kernel<Dt, D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)LY::TOTAL);
+  if (a.cluster > 1) {
+    auto ck = attn_decode_cluster_kernel<Dt, D, NQ>;
+    cudaError_t e = set_max_smem((const void*)ck, (int)LY::TOTAL_CL);
     if (e != cudaSuccess) return e;
-    configured = true;
+    if (a.cluster > 8) {
+      e = cudaFuncSetAttribute(ck, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid_x, a.KV);
+    cfg.blockDim = dim3(AD_THREADS);
+    cfg.dynamicSmemBytes = LY::TOTAL_CL;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = c.pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, ck, a);
   }
+  auto kern = a.runs ? attn_decode_kernel<Dt, D, NQ> : attn_decode_item_kernel<Dt, D, NQ>;
+  cudaError_t e = set_max_smem((const void*)kern, (int)LY::TOTAL);
+  if (e != cudaSuccess) return e;
   return launch_k(kern, dim3(a.grid_x, a.KV), dim3(AD_THREADS), LY::TOTAL, c, a);
 }
 
@@ -842,6 +1099,61 @@ cudaError_t ad_nq(const LaunchCtx& c, const AttnDecArgs& a) {
 }
 
 }  // namespace
+
+// Keys one cluster of `cl` CTAs can take for a query block of nq query
+// vectors (every CTA holds its whole run in its ring).
+int attn_decode_cluster_keys(int dt, int nq, int cl) {
+  const int ck = dt == DT_BF16 ? ADT<bf16>::CK : ADT<float>::CK;
+  const int stages = nq <= 2 ? AD_STAGES_MAX : AD_SUBS;
+  return cl * stages * ck;
+}
+
+namespace {
+template <typename Dt, int D, int NQ>
+int ad_cluster_fit(int cl, int kv, int clusters_x) {
+  using LY = ADLayout<Dt, D, NQ>;
+  auto ck = attn_decode_cluster_kernel<Dt, D, NQ>;
+  if (set_max_smem((const void*)ck, (int)LY::TOTAL_CL) != cudaSuccess) return 0;
+  if (cl > 8 && cudaFuncSetAttribute(ck, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cl * clusters_x, kv);
+  cfg.blockDim = dim3(AD_THREADS);
+  cfg.dynamicSmemBytes = LY::TOTAL_CL;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ck, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+template <typename Dt, int D>
+int ad_cluster_fit_nq(int nq, int cl, int kv, int clusters_x) {
+  if (nq <= 1) return ad_cluster_fit<Dt, D, 1>(cl, kv, clusters_x);
+  if (nq <= 2) return ad_cluster_fit<Dt, D, 2>(cl, kv, clusters_x);
+  if (nq <= 4) return ad_cluster_fit<Dt, D, 4>(cl, kv, clusters_x);
+  return ad_cluster_fit<Dt, D, 8>(cl, kv, clusters_x);
+}
+}  // namespace
+
+// How many clusters of `cl` CTAs of the cluster kernel can be resident at
+// once on the current device (0 if the launch shape is not possible).
+int attn_decode_cluster_capacity(int dt, int D, int nq, int cl, int kv, int clusters_x) {
+  if (D == 128) return dt == DT_BF16 ? ad_cluster_fit_nq<bf16, 128>(nq, cl, kv, clusters_x)
+                                     : ad_cluster_fit_nq<float, 128>(nq, cl, kv, clusters_x);
+  if (D == 64) return dt == DT_BF16 ? ad_cluster_fit_nq<bf16, 64>(nq, cl, kv, clusters_x)
+                                    : ad_cluster_fit_nq<float, 64>(nq, cl, kv, clusters_x);
+  return 0;
+}
 
 int attn_decode2_chunk(int dt) { return (dt == DT_BF16 ? ADT<bf16>::CK : ADT<float>::CK) * AD_SUBS; }
 int attn_decode2_nq_max() { return AD_NQ_MAX; }

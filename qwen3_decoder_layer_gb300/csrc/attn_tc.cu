@@ -247,7 +247,26 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         *reinterpret_cast<uint4*>(Ph + off) = make_uint4(ph[cc * 4], ph[cc * 4 + 1], ph[cc * 4 + 2], ph[cc * 4 + 3]);
         *reinterpret_cast<uint4*>(Pl + off) = make_uint4(pl[cc * 4], pl[cc * 4 + 1], pl[cc * 4 + 2], pl[cc * 4 + 3]);
       }
-      fence_proxy_async();  // P's generic-proxy stores before the MMA's reads
+      // Last tile: its value rows past the block's last key hold whatever the
+      // cache held there; their probabilities are 0, but 0 * (a non-finite
+      // value) is not 0 in the P.V product, so those rows are zeroed first
+      // (half hf clears column block hf; a whole 128-byte row is the same row
+      // under the swizzle).  The tile has landed: S of this tile was computed.
+      const int last_key = qb.pos0 + qb.nrows - 1;
+      if (j == n_tiles - 1 && j * AT_BN + AT_BN - 1 > last_key && hf < L::NC) {
+        const int st = j % AT_STAGES;
+        if (ok && lane == 0) mbar_wait(&kv_full[st], (uint32_t)((j / AT_STAGES) & 1), a.err, 13);
+        __syncwarp();
+        for (int c = hf; c < L::NC; c += 2) {
+          if (j * AT_BN + r > last_key) {
+            uint4* vrow = reinterpret_cast<uint4*>(smem + L::KV_OFF + st * L::STAGE + (L::NC + c) * L::SUB +
+                                                   (size_t)r * 128);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) vrow[cc] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      fence_proxy_async();  // P's (and zeroed V rows') generic-proxy stores before the MMA's reads
       fence_before();
       mbar_arrive_cta(p_full);
       m = m_use;
@@ -291,12 +310,8 @@ template <int D>
 cudaError_t at_launch(const LaunchCtx& c, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const AttnTcArgs& a) {
   auto kern = attn_tc_kernel<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATL<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_max_smem((const void*)kern, (int)ATL<D>::SMEM);
+  if (e != cudaSuccess) return e;
   return launch_k(kern, dim3(a.n_qblocks * a.H), dim3(AT_THREADS), ATL<D>::SMEM, c, mq, mk, mv, a);
 }
 

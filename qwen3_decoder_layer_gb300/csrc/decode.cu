@@ -311,12 +311,8 @@ __global__ void __launch_bounds__(G2_MAX_WARPS * 32, 1) gemv2_kernel(Gemv2Args a
 template <typename Dt, int WF, int NT, int EPI>
 cudaError_t g2_launch(const LaunchCtx& c, const Gemv2Args& a) {
   auto kern = gemv2_kernel<Dt, WF, NT, EPI>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G2_SMEM_LIMIT);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_max_smem((const void*)kern, (int)G2_SMEM_LIMIT);
+  if (e != cudaSuccess) return e;
   const G2Layout L = g2_layout(WF == W_U8 ? 1 : (int)sizeof(Dt), (int)sizeof(Dt), NT, a.K, EPI == EPI_SWIGLU,
                                a.stages, a.nwarps);
   int grid = (a.N + a.nwarps - 1) / a.nwarps;

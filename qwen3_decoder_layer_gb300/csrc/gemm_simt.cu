@@ -52,8 +52,10 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
     r_end = min(r_begin + BM, a.M);
   }
   const int n0 = blockIdx.x * BNO;
-  const char* wbase = static_cast<const char*>(a.w) +
-                      (size_t)grp * (size_t)a.w_stride * (WF == W_U8 ? 1 : sizeof(Dt));
+  const char* wbase = static_cast<const char*>(a.w);
+  // group grp's matrix starts at weight row grp * (w_stride / K): rows (and the
+  // int8 scale / bias rows) are counted across the stacked matrices
+  const size_t grow0 = a.tile_start ? (size_t)grp * (size_t)(a.w_stride / a.K) : 0;
   const Dt* A = static_cast<const Dt*>(a.a);
 
   // loaders: A tile 64 x 16 and B tile 64 x 16, 4 elements per thread each
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       As[lk + e][lr] = a_ok ? to_f(A[arow * a.lda + k0 + lk + e]) : 0.f;
-      Bs[lk + e][lr] = b_ok ? load_w<Dt, WF>(a, wbase, (size_t)bn, k0 + lk + e) : 0.f;
+      Bs[lk + e][lr] = b_ok ? load_w<Dt, WF>(a, wbase, grow0 + (size_t)bn, k0 + lk + e) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
       const size_t o = orow * a.ldo + n;
       if (EPI == EPI_STORE) static_cast<Dt*>(a.out)[o] = from_f<Dt>(acc[i][j]);
       else if (EPI == EPI_STORE_F32) static_cast<float*>(a.out)[o] = acc[i][j];
+      else if (EPI == EPI_STORE_RF32) static_cast<float*>(a.out)[o] = rd<Dt>(acc[i][j]);
       else {  // residual
         Dt* p = static_cast<Dt*>(a.out) + o;
         *p = from_f<Dt>(to_f(*p) + rd<Dt>(acc[i][j]));
@@ -139,6 +142,7 @@ cudaError_t launch_epi(const LaunchCtx& c, const GemmArgs& a) {
   switch (a.epilogue) {
     case EPI_STORE: return launch_k(gemm_simt_kernel<Dt, WF, EPI_STORE>, grid, block, 0, c, a);
     case EPI_STORE_F32: return launch_k(gemm_simt_kernel<Dt, WF, EPI_STORE_F32>, grid, block, 0, c, a);
+    case EPI_STORE_RF32: return launch_k(gemm_simt_kernel<Dt, WF, EPI_STORE_RF32>, grid, block, 0, c, a);
     case EPI_RESIDUAL: return launch_k(gemm_simt_kernel<Dt, WF, EPI_RESIDUAL>, grid, block, 0, c, a);
     case EPI_SWIGLU: return launch_k(gemm_simt_kernel<Dt, WF, EPI_SWIGLU>, grid, block, 0, c, a);
     default: return cudaErrorInvalidValue;

@@ -443,13 +443,8 @@ __global__ void __launch_bounds__(W8_THREADS, 2) gemm_w8_kernel(SkinnyArgs a) {
 template <int MT, int EPI>
 cudaError_t w8_go(const LaunchCtx& c, const SkinnyArgs& a, dim3 grid) {
   constexpr size_t smem = w8_smem_bytes<MT>();
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gemm_w8_kernel<MT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e = set_max_smem((const void*)gemm_w8_kernel<MT, EPI>, (int)smem);
+  if (e != cudaSuccess) return e;
   return launch_k(gemm_w8_kernel<MT, EPI>, grid, dim3(W8_THREADS), smem, c, a);
 }
 

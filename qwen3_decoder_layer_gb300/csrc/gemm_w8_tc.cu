@@ -375,13 +375,8 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
 template <int EPI>
 cudaError_t wt_launch(const LaunchCtx& c, const CUtensorMap& mw, const CUtensorMap& ma, const SkinnyArgs& a,
                       dim3 grid) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gemm_w8_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)WT_SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e = set_max_smem((const void*)gemm_w8_tc_kernel<EPI>, (int)WT_SMEM);
+  if (e != cudaSuccess) return e;
   return launch_k(gemm_w8_tc_kernel<EPI>, grid, dim3(WT_THREADS), WT_SMEM, c, mw, ma, a);
 }
 

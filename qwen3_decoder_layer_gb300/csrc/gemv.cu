@@ -86,16 +86,14 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
   const int nvec = a.K / W::EPV;
   for (long long u = u0 + warp; u < u1; u += kWarps) {
     int b = 0, n = (int)u;
-    size_t row = (size_t)n;
-    const char* base = wb;
+    size_t row = (size_t)n;  // row of the weight (stacked experts: counted across all experts)
     if (gather) {
       b = (int)(u / a.N);
       n = (int)(u % a.N);
-      row = (size_t)n;
-      base = wb + (size_t)a.slot_expert[b] * (size_t)a.w_stride * W::BYTES;
+      row = (size_t)a.slot_expert[b] * (size_t)(a.w_stride / a.K) + (size_t)n;
     }
-    const char* r0 = base + row * row_bytes;
-    const char* r1 = base + (row + a.N) * row_bytes;
+    const char* r0 = wb + row * row_bytes;
+    const char* r1 = wb + (row + a.N) * row_bytes;
     const Dt* xrow = xs + (size_t)(gather ? b / a.slot_div : 0) * a.K;
     float acc[NT], acc2[NT];
 #pragma unroll
@@ -149,6 +147,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
         static_cast<Dt*>(a.out)[o] = from_f<Dt>(v);
       } else if (EPI == EPI_STORE_F32) {
         static_cast<float*>(a.out)[o] = v;
+      } else if (EPI == EPI_STORE_RF32) {
+        static_cast<float*>(a.out)[o] = rd<Dt>(v);
       } else if (EPI == EPI_RESIDUAL) {
         Dt* p = static_cast<Dt*>(a.out) + o;
         *p = from_f<Dt>(to_f(*p) + rd<Dt>(v));
@@ -164,12 +164,8 @@ template <typename Dt, int WF, int NT, int EPI>
 cudaError_t launch_one(const LaunchCtx& c, const GemvArgs& a) {
   auto kern = gemv_kernel<Dt, WF, NT, EPI>;
   const size_t smem = gemv_smem_bytes(a);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_max_smem((const void*)kern, 200 * 1024);
+  if (e != cudaSuccess) return e;
   const long long units = a.slot_expert ? (long long)a.T * a.N : (long long)a.N;
   long long grid = (units + kWarps - 1) / kWarps;
   const long long cap = (long long)c.num_sms * 4;
@@ -195,6 +191,7 @@ cudaError_t launch_epi(const LaunchCtx& c, const GemvArgs& a) {
   switch (a.epilogue) {
     case EPI_STORE: return launch_nt<Dt, WF, EPI_STORE>(c, a);
     case EPI_STORE_F32: return launch_nt<Dt, WF, EPI_STORE_F32>(c, a);
+    case EPI_STORE_RF32: return launch_nt<Dt, WF, EPI_STORE_RF32>(c, a);
     case EPI_RESIDUAL: return launch_nt<Dt, WF, EPI_RESIDUAL>(c, a);
     case EPI_SWIGLU: return launch_nt<Dt, WF, EPI_SWIGLU>(c, a);
     default: return cudaErrorInvalidValue;

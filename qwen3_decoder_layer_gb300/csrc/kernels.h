@@ -8,7 +8,8 @@ namespace q3 {
 
 enum DType { DT_F32 = 0, DT_BF16 = 1 };
 enum WFmt { W_DT = 0, W_U8 = 1 };  // weights in the model dtype, or affine int8 codes
-enum Epi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_RESIDUAL = 2, EPI_SWIGLU = 3 };
+enum Epi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_RESIDUAL = 2, EPI_SWIGLU = 3,
+           EPI_STORE_RF32 = 4 /* rounded to the model dtype, stored as fp32 (output head) */ };
 
 struct LaunchCtx {
   cudaStream_t stream;
@@ -336,6 +337,8 @@ struct AttnDecArgs {
   int grid_x;
   int nq;              // largest query-vector count (rows x G) of any query block, <= attn_decode2_nq_max()
   int runs;            // 1: blocks walk contiguous item ranges (more items than blocks); 0: one item per block
+  int cluster;         // > 1: one query block per cluster of this many CTAs (grid_x = cluster x query blocks),
+                       // partials merged through distributed shared memory; items and partial buffers unused
   int* err;
   const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
   size_t pf_bytes;
@@ -343,45 +346,35 @@ struct AttnDecArgs {
 cudaError_t launch_attn_decode2(const LaunchCtx& c, int dt, const AttnDecArgs& a);
 int attn_decode2_chunk(int dt);
 int attn_decode2_nq_max();
+// Cluster variant: keys a cluster of `cl` CTAs takes for nq query vectors, and
+// how many such clusters (grid cl * clusters_x by kv) can be resident at once.
+int attn_decode_cluster_keys(int dt, int nq, int cl);
+int attn_decode_cluster_capacity(int dt, int D, int nq, int cl, int kv, int clusters_x);
 
-// Whole decode step (T <= 4 rows, dense layers) in one persistent cooperative
-// kernel: per-layer weight pointers in a device table.
-struct FusedLayer {
-  const void *qkv, *qkv_s, *qkv_b, *o, *o_s, *o_b, *gu, *gu_s, *gu_b, *down, *down_s, *down_b;
-  const void *in_norm, *post_norm, *q_norm, *k_norm;
+
+// Embedding rows: out[t] = table[ids[t]] (dt rows of `hidden`); ids on the device.
+struct EmbedArgs {
+  const void* table;
+  const int* ids;
+  int n, hidden;
+  void* out;
 };
-struct FusedArgs {
-  const FusedLayer* layers;  // [L] device
-  const void* final_norm;
-  int L, T, hidden, H, KV, D, I, group;
-  float eps, scale;
-  int row_seq[4], row_pos[4];
-  void* kc;                  // cache base: layer 0, sequence 0
-  void* vc;
-  long long layer_stride, seq_stride;
-  int capacity;
-  const float* cos_t;
-  const float* sin_t;
-  const void* x;             // dt [T, hidden] input rows
-  void* h;                   // dt [T, hidden] residual stream
-  void* qkv;                 // dt [T, (H + 2 KV) D]
-  void* attn;                // dt [T, H D]
-  void* mbuf;                // dt [T, I]
-  void* out;                 // dt [T, hidden]
-  double* sumsq;             // [2 L + 1][T]
-  float* part_o;             // [parts][KV][8][D]
-  float* part_ml;            // [parts][KV][8][2]
-  int* counters;             // [4 KV], zero at launch
-  unsigned* sync;            // [2]: grid-barrier counter, abort flag; zero at launch
-  int* err;
-  int slot_bytes, n_slots, u_bytes;  // ring geometry (fused_decode_plan)
+cudaError_t launch_embed_gather(const LaunchCtx& c, int dt, const EmbedArgs& a);
+
+// L2 normalisation of one dt row of `hidden` into out, each step rounded to
+// the model dtype: sq = R(v v), ss = R(sum sq), n = R(sqrt ss), out = R(v / n).
+struct L2PoolArgs {
+  const void* row;
+  int hidden;
+  void* out;
 };
-// Fills the ring geometry and the dynamic shared memory size; false if this
-// shape is not supported by the fused kernel.
-bool fused_decode_plan(int dt, int wfmt, FusedArgs& a, size_t* smem);
-cudaError_t launch_fused_decode(const LaunchCtx& c, int dt, int wfmt, const FusedArgs& a, int grid, size_t smem);
-int fused_decode_nq_max();
-int fused_decode_chunk();
+cudaError_t launch_l2_pool(const LaunchCtx& c, int dt, const L2PoolArgs& a);
+
+// One CTA waits on an mbarrier that nothing completes, with the bounded wait
+// every kernel here uses (mbar_wait); it gives up after its limit, records
+// kWaitProbeCode in *err and returns.
+constexpr int kWaitProbeCode = 99;
+cudaError_t launch_wait_probe(cudaStream_t s, int* err);
 
 // out = RMSNorm(h) * gain with the sum of squares of each row precomputed.
 struct NormApplyArgs {

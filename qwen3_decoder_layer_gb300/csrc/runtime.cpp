@@ -74,13 +74,14 @@ struct qwen3_handle {
   std::vector<int32_t> lengths;
   std::string err;
   // options
-  bool use_graphs = true, profile = false, pdl = true, use_tc = true, l2_prefetch = true, fused = false;
-  bool coop = false;         // device supports cooperative launches
-  void* fused_layers = nullptr;  // device FusedLayer table (dense stacks)
+  bool use_graphs = true, profile = false, pdl = true, use_tc = true, l2_prefetch = true;
+  bool cluster_attn = true;   // decode attention on thread-block clusters where it fits
+  int64_t fail_alloc_in = 0;  // test hook: the n-th next workspace allocation fails (0 = off)
+  std::map<int64_t, int> cluster_cap;  // resident clusters of the decode-attention cluster kernel, by launch shape
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
-      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, fsync, skws,
-      skcnt, ysort;
+      cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, skws,
+      skcnt, ysort, ids, pool_rows;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -137,9 +138,11 @@ qwen3_status ensure(qwen3_handle* h, DevBuf& b, size_t bytes, bool zero = false)
   size_t nb = std::max(bytes, b.bytes + b.bytes / 2);
   nb = (nb + 255) & ~size_t(255);
   void* p = nullptr;
-  if (cudaMalloc(&p, nb) != cudaSuccess) {
+  const bool injected = h->fail_alloc_in > 0 && --h->fail_alloc_in == 0;
+  if (injected || cudaMalloc(&p, nb) != cudaSuccess) {
     cudaGetLastError();
-    return fail(h, QWEN3_E_OOM, "device allocation of " + std::to_string(nb) + " bytes failed");
+    return fail(h, QWEN3_E_OOM, std::string(injected ? "(injected) " : "") + "device allocation of " +
+                                    std::to_string(nb) + " bytes failed");
   }
   if (zero) cudaMemset(p, 0, nb);
   if (b.p) {
@@ -240,7 +243,7 @@ qwen3_status qwen3_check_config(const qwen3_config* c) {
     if (c->num_experts > 256 || c->top_k < 1 || c->top_k > c->num_experts || c->top_k > 32) return QWEN3_E_ARG;
     if (c->moe_intermediate < 64 || c->moe_intermediate % 64 || c->moe_intermediate > 8192) return QWEN3_E_ARG;
     if (c->decoder_sparse_step < 1) return QWEN3_E_ARG;
-    if (c->weight_format != QWEN3_WEIGHTS_DENSE) return QWEN3_E_UNSUPPORTED;
+    if (c->weight_format == QWEN3_WEIGHTS_INT8 && c->moe_intermediate % c->group_size) return QWEN3_E_ARG;
     if (c->n_mlp_only_layers < 0 || (c->n_mlp_only_layers > 0 && !c->mlp_only_layers)) return QWEN3_E_ARG;
   }
   const double cache_elems = 2.0 * c->max_seqs * c->num_layers * c->n_kv_heads * (double)c->capacity * c->head_dim;
@@ -282,8 +285,7 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
       s = bad("missing or misaligned norm gain", l);
     else if (!lin_ok(w.qkv) || !lin_ok(w.o)) s = bad("missing attention weights", l);
     else if (is_moe_layer(h, l)) {
-      if (!w.router || !w.exp_gate_up || !w.exp_down || !aligned16(w.router) || !aligned16(w.exp_gate_up) ||
-          !aligned16(w.exp_down))
+      if (!w.router || !aligned16(w.router) || !lin_ok(w.exp_gate_up) || !lin_ok(w.exp_down))
         s = bad("missing MoE weights", l);
     } else if (!lin_ok(w.gate_up) || !lin_ok(w.down)) {
       s = bad("missing MLP weights", l);
@@ -308,9 +310,6 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
     return QWEN3_E_DEVICE;
   }
   h->num_sms = prop.multiProcessorCount;
-  int coop = 0;
-  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
-  h->coop = coop != 0;
   const qwen3_config& c = h->cfg;
   h->layer_stride = (size_t)c.n_kv_heads * c.capacity * c.head_dim;
   h->seq_stride = h->layer_stride * c.num_layers;
@@ -345,21 +344,6 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
   cudaMemcpy(h->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
   cudaMemcpy(h->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
   h->lengths.assign(c.max_seqs, 0);
-  if (c.num_experts == 0) {  // per-layer weight table of the fused decode kernel
-    std::vector<FusedLayer> fl(c.num_layers);
-    for (int l = 0; l < c.num_layers; ++l) {
-      const qwen3_layer_weights& w = h->layers[l];
-      fl[l] = FusedLayer{w.qkv.w, w.qkv.scale, w.qkv.bias, w.o.w, w.o.scale, w.o.bias, w.gate_up.w,
-                         w.gate_up.scale, w.gate_up.bias, w.down.w, w.down.scale, w.down.bias,
-                         w.in_norm, w.post_norm, w.q_norm, w.k_norm};
-    }
-    if (cudaMalloc(&h->fused_layers, fl.size() * sizeof(FusedLayer)) != cudaSuccess) {
-      cudaGetLastError();
-      qwen3_destroy(h);
-      return QWEN3_E_OOM;
-    }
-    cudaMemcpy(h->fused_layers, fl.data(), fl.size() * sizeof(FusedLayer), cudaMemcpyHostToDevice);
-  }
   for (int i = 0; i < qwen3_handle::kRing; ++i) cudaEventCreateWithFlags(&h->pinned_ev[i], cudaEventDisableTiming);
   cudaStreamCreateWithFlags(&h->gstream, cudaStreamNonBlocking);
   cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming);
@@ -380,7 +364,7 @@ void qwen3_destroy(qwen3_handle* h) {
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                     &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err,
-                    &h->fsync, &h->skws, &h->skcnt, &h->ysort};
+                    &h->skws, &h->skcnt, &h->ysort, &h->ids, &h->pool_rows};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -399,7 +383,6 @@ void qwen3_destroy(qwen3_handle* h) {
   if (h->vcache) cudaFree(h->vcache);
   if (h->rope_cos) cudaFree(h->rope_cos);
   if (h->rope_sin) cudaFree(h->rope_sin);
-  if (h->fused_layers) cudaFree(h->fused_layers);
   delete h;
 }
 
@@ -451,7 +434,11 @@ qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value) {
     case QWEN3_OPT_PDL: h->pdl = value != 0; return QWEN3_OK;
     case QWEN3_OPT_TENSOR_CORES: h->use_tc = value != 0; return QWEN3_OK;
     case QWEN3_OPT_L2_PREFETCH: h->l2_prefetch = value != 0; return QWEN3_OK;
-    case QWEN3_OPT_FUSED_DECODE: h->fused = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_CLUSTER_ATTENTION: h->cluster_attn = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_FAIL_ALLOC:
+      if (value < 0) return fail(h, QWEN3_E_ARG, "QWEN3_OPT_FAIL_ALLOC takes a count >= 0");
+      h->fail_alloc_in = value;
+      return QWEN3_OK;
   }
   return fail(h, QWEN3_E_ARG, "unknown option");
 }
@@ -516,6 +503,8 @@ struct Plan {
   int chunk = 64;
   int nq_max = 16;
   int max_nq = 1;              // largest rows x G of any query block
+  int max_keys = 0;            // most keys any query block attends to
+  int cluster = 0;             // decode attention: CTAs per cluster (0 = the item / run kernels)
   int n_qblocks = 0, n_items = 0, n_parts = 0;
   std::vector<int32_t> blob;   // row_seq[T] row_pos[T] n_items qblocks items
   size_t off_rowseq = 0, off_rowpos = 0, off_nitems = 0, off_qb = 0, off_items = 0;
@@ -567,6 +556,7 @@ qwen3_status build_plan(qwen3_handle* h, int T, const int32_t* seq_ids, const in
       const int nr = std::min(P.rows_per_block, g.n - r);
       P.max_nq = std::max(P.max_nq, nr * G);
       const int last_pos = g.pos0 + r + nr - 1;
+      P.max_keys = std::max(P.max_keys, last_pos + 1);
       const int nch = P.attn == ATTN_TC ? 1 : (last_pos + 1 + P.chunk - 1) / P.chunk;
       qb.insert(qb.end(), {g.seq, g.row0 + r, nr, g.pos0 + r, nch, parts, g.row0, g.pos0, g.n, 0});
       for (int ch = 0; ch < nch; ++ch) items.insert(items.end(), {nqb, ch});
@@ -620,7 +610,6 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   ENS(mbuf, Tz * std::max(c.intermediate, 64) * e, false);
   ENS(sumsq, Tz * (2 * (size_t)c.num_layers + 1) * sizeof(double), true);
   ENS(dev_err, 64, true);
-  ENS(fsync, (size_t)(2 + 4 * c.n_kv_heads) * 4, true);
   if (!P.gemv && T <= 64) {  // skinny GEMM split-K workspace (kept zero by the kernel)
     const size_t nmax = std::max({(size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, (size_t)c.hidden,
                                   2 * (size_t)c.intermediate});
@@ -629,10 +618,7 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
   }
   // attention partials: sized for the worst case of this row count when graphs replay it
   size_t parts = (size_t)std::max(P.n_parts, 1);
-  if (P.gemv) {
-    const int ch = std::min(P.chunk, fused_decode_chunk());  // the fused kernel's items may be shorter
-    parts = std::max(parts, (size_t)std::max(P.n_qblocks, T) * ((c.capacity + ch - 1) / ch));
-  }
+  if (P.gemv) parts = std::max(parts, (size_t)std::max(P.n_qblocks, T) * ((c.capacity + P.chunk - 1) / P.chunk));
   ENS(part_o, parts * c.n_kv_heads * P.nq_max * c.head_dim * 4, false);
   ENS(part_ml, parts * c.n_kv_heads * P.nq_max * 2 * 4, false);
   ENS(counters, (size_t)std::max(P.n_qblocks, T) * c.n_kv_heads * 4, true);
@@ -704,6 +690,7 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
   const qwen3_layer_weights& W = h->layers[layer];
   const int E = c.num_experts, k = c.top_k, mI = c.moe_intermediate, hid = c.hidden;
   const int dt = h->dt;
+  const int xw = W.exp_gate_up.scale ? h->wfmt : W_DT;  // expert weight format
   cudaError_t e;
   // router logits, fp32, not rounded
   if (T <= 4) {
@@ -728,20 +715,22 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
   const int slots = T * k;
   if (unsorted) {
     GemvArgs g{};
-    g.T = slots; g.K = hid; g.N = mI; g.w = W.exp_gate_up; g.slot_expert = idx;
+    g.T = slots; g.K = hid; g.N = mI; g.w = W.exp_gate_up.w; g.scale = W.exp_gate_up.scale;
+    g.bias = W.exp_gate_up.bias; g.group = c.group_size; g.slot_expert = idx;
     g.w_stride = (long long)2 * mI * hid; g.slot_div = k; g.x_rows = T; g.x = y;
     g.epilogue = EPI_SWIGLU; g.out = B.mexp; g.ldo = mI;
-    e = launch(L, "gemv_expert_gate_up", [&] { return launch_gemv(L.ctx, dt, W_DT, g); });
+    e = launch(L, "gemv_expert_gate_up", [&] { return launch_gemv(L.ctx, dt, xw, g); });
     if (e != cudaSuccess) return e;
     GemvArgs d{};
-    d.T = slots; d.K = mI; d.N = hid; d.w = W.exp_down; d.slot_expert = idx; d.w_stride = (long long)hid * mI;
+    d.T = slots; d.K = mI; d.N = hid; d.w = W.exp_down.w; d.scale = W.exp_down.scale; d.bias = W.exp_down.bias;
+    d.group = c.group_size; d.slot_expert = idx; d.w_stride = (long long)hid * mI;
     d.slot_div = 1; d.x_rows = slots; d.x = B.mexp; d.epilogue = EPI_STORE; d.out = B.zexp;
     d.ldo = hid;
-    e = launch(L, "gemv_expert_down", [&] { return launch_gemv(L.ctx, dt, W_DT, d); });
+    e = launch(L, "gemv_expert_down", [&] { return launch_gemv(L.ctx, dt, xw, d); });
     if (e != cudaSuccess) return e;
   } else {
     // tensor-core grouped GEMMs (bf16 experts whose shapes fit the 128 x 256 tiles), else CUDA cores
-    const bool tc = h->use_tc && dt == DT_BF16 && B.ysort && mI % (128) == 0 && hid % 256 == 0 &&
+    const bool tc = h->use_tc && dt == DT_BF16 && xw == W_DT && B.ysort && mI % (128) == 0 && hid % 256 == 0 &&
                     gemm_tc_supported(slots, mI, hid, EPI_SWIGLU) && gemm_tc_supported(slots, hid, mI, EPI_STORE);
     const int BM = tc ? 128 : gemm_simt_tile_m();
     MoeScanArgs sc{};
@@ -761,14 +750,14 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
       e = launch(L, "moe_gather", [&] { return launch_moe_gather(L.ctx, dt, ga); });
       if (e != cudaSuccess) return e;
       GemmTcArgs t{};
-      t.M = slots; t.N = mI; t.K = hid; t.a = B.ysort; t.lda = hid; t.w = W.exp_gate_up; t.out = B.mexp;
+      t.M = slots; t.N = mI; t.K = hid; t.a = B.ysort; t.lda = hid; t.w = W.exp_gate_up.w; t.out = B.mexp;
       t.ldo = mI; t.epilogue = EPI_SWIGLU; t.err = B.err; t.tile_start = B.tile_start; t.row_off = B.row_off;
       t.row_cnt = B.row_cnt; t.n_groups = E; t.max_tiles_m = max_tiles; t.w_group_rows = 2LL * mI;
       t.w_rows_total = 2LL * mI * E;
       e = launch(L, "gemm_tc_expert_gate_up", [&] { return launch_gemm_tc(L.ctx, t); });
       if (e != cudaSuccess) return e;
       GemmTcArgs d{};
-      d.M = slots; d.N = hid; d.K = mI; d.a = B.mexp; d.lda = mI; d.w = W.exp_down; d.out = B.zexp; d.ldo = hid;
+      d.M = slots; d.N = hid; d.K = mI; d.a = B.mexp; d.lda = mI; d.w = W.exp_down.w; d.out = B.zexp; d.ldo = hid;
       d.epilogue = EPI_STORE; d.err = B.err; d.tile_start = B.tile_start; d.row_off = B.row_off;
       d.row_cnt = B.row_cnt; d.n_groups = E; d.max_tiles_m = max_tiles; d.w_group_rows = hid;
       d.w_rows_total = (long long)hid * E; d.c_rows = B.sorted_src;
@@ -776,23 +765,46 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
       if (e != cudaSuccess) return e;
     } else {
     GemmArgs g{};
-    g.M = slots; g.N = mI; g.K = hid; g.a = y; g.lda = hid; g.a_rows = B.sorted_tok; g.w = W.exp_gate_up;
+    g.M = slots; g.N = mI; g.K = hid; g.a = y; g.lda = hid; g.a_rows = B.sorted_tok; g.w = W.exp_gate_up.w;
+    g.scale = W.exp_gate_up.scale; g.bias = W.exp_gate_up.bias; g.group = c.group_size;
     g.w_stride = (long long)2 * mI * hid; g.tile_start = B.tile_start; g.row_off = B.row_off;
     g.row_cnt = B.row_cnt; g.n_groups = E; g.max_tiles = max_tiles; g.epilogue = EPI_SWIGLU; g.out = B.mexp;
     g.ldo = mI;
-    e = launch(L, "gemm_expert_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, g); });
+    e = launch(L, "gemm_expert_gate_up", [&] { return launch_gemm_simt(L.ctx, dt, xw, g); });
     if (e != cudaSuccess) return e;
     GemmArgs d{};
-    d.M = slots; d.N = hid; d.K = mI; d.a = B.mexp; d.lda = mI; d.w = W.exp_down; d.w_stride = (long long)hid * mI;
+    d.M = slots; d.N = hid; d.K = mI; d.a = B.mexp; d.lda = mI; d.w = W.exp_down.w; d.scale = W.exp_down.scale;
+    d.bias = W.exp_down.bias; d.group = c.group_size; d.w_stride = (long long)hid * mI;
     d.tile_start = B.tile_start; d.row_off = B.row_off; d.row_cnt = B.row_cnt; d.n_groups = E;
     d.max_tiles = max_tiles; d.epilogue = EPI_STORE; d.out = B.zexp; d.ldo = hid; d.c_rows = B.sorted_src;
-    e = launch(L, "gemm_expert_down", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, d); });
+    e = launch(L, "gemm_expert_down", [&] { return launch_gemm_simt(L.ctx, dt, xw, d); });
     if (e != cudaSuccess) return e;
     }
   }
   MoeCombineArgs cb{};
   cb.z = B.zexp; cb.w = w; cb.T = T; cb.k = k; cb.hidden = hid; cb.out = out; cb.h = h_res; cb.sumsq_out = sumsq_out;
   return launch(L, "moe_combine", [&] { return launch_moe_combine(L.ctx, dt, cb); });
+}
+
+// Decode attention with one query block per thread-block cluster when every
+// (query block, kv head) gets its own cluster, all of them resident at once,
+// and each query block's keys fit the cluster's shared memory: 16 CTAs per
+// cluster where the device allows it, else 8.
+int decode_cluster_size(qwen3_handle* h, const Plan& P) {
+  if (P.attn != ATTN_DECODE || P.n_qblocks < 1) return 0;
+  const qwen3_config& c = h->cfg;
+  for (int cl : {16, 8}) {
+    if ((int64_t)P.n_qblocks * c.n_kv_heads * cl > h->num_sms) continue;
+    if (P.max_keys > attn_decode_cluster_keys(h->dt, P.max_nq, cl)) continue;
+    const int nqb = P.max_nq <= 1 ? 1 : P.max_nq <= 2 ? 2 : P.max_nq <= 4 ? 4 : 8;
+    const int64_t key = ((int64_t)cl << 40) | ((int64_t)nqb << 32) | ((int64_t)P.n_qblocks << 16) | c.n_kv_heads;
+    auto it = h->cluster_cap.find(key);
+    if (it == h->cluster_cap.end())
+      it = h->cluster_cap.emplace(key, attn_decode_cluster_capacity(h->dt, c.head_dim, P.max_nq, cl, c.n_kv_heads,
+                                                                    P.n_qblocks)).first;
+    if (it->second >= P.n_qblocks * c.n_kv_heads) return cl;
+  }
+  return 0;
 }
 
 // Attention of layer l for the plan's kernel.
@@ -820,6 +832,11 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
     a.grid_x = std::max(1, (h->num_sms + KV - 1) / KV);
     a.nq = P.max_nq;
     a.runs = P.n_items > a.grid_x;
+    if (P.cluster > 1) {
+      a.cluster = P.cluster;
+      a.grid_x = P.cluster * P.n_qblocks;
+      a.runs = 0;
+    }
     a.pf = pf; a.pf_bytes = pf_bytes;
     return launch(L, "attn_decode", [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
@@ -932,16 +949,25 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
   return launch(L, "norm_apply", [&] { return launch_norm_apply(L.ctx, dt, n); });
 }
 
+// Kernel names of one linear under each GEMM it may run on (profiling keys).
+struct LinNames {
+  const char *tc, *w8tc, *skinny, *simt;
+};
+constexpr LinNames kQkv{"gemm_tc_qkv", "gemm_w8tc_qkv", "gemm_skinny_qkv", "gemm_qkv"};
+constexpr LinNames kO{"gemm_tc_o", "gemm_w8tc_o", "gemm_skinny_o", "gemm_o"};
+constexpr LinNames kGateUp{"gemm_tc_gate_up", "gemm_w8tc_gate_up", "gemm_skinny_gate_up", "gemm_gate_up"};
+constexpr LinNames kDown{"gemm_tc_down", "gemm_w8tc_down", "gemm_skinny_down", "gemm_down"};
+
 // A prefill linear: the tcgen05 GEMM for dense bf16 weights on shapes its
 // tile takes, the CUDA-core GEMM otherwise (fp32, int8, ragged N).
-cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const char* tc_name, const char* simt_name, int wfmt,
-                        const GemmArgs& g, const Bufs& B) {
+cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const LinNames& nm, int wfmt, const GemmArgs& g,
+                        const Bufs& B) {
   if (h->use_tc && h->dt == DT_BF16 && wfmt == W_DT && !g.a_rows && !g.c_rows && !g.tile_start &&
       gemm_tc_supported(g.M, g.N, g.K, g.epilogue)) {
     GemmTcArgs t{};
     t.M = g.M; t.N = g.N; t.K = g.K; t.a = g.a; t.lda = g.lda; t.w = g.w; t.out = g.out; t.ldo = g.ldo;
     t.epilogue = g.epilogue; t.err = B.err;
-    return launch(L, tc_name, [&] { return launch_gemm_tc(L.ctx, t); });
+    return launch(L, nm.tc, [&] { return launch_gemm_tc(L.ctx, t); });
   }
   if (g.M <= 64 && !g.a_rows && !g.c_rows && !g.tile_start && gemm_skinny_supported(g.M, g.N, g.K) && h->skws.p) {
     SkinnyArgs k{};
@@ -949,10 +975,10 @@ cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const char* tc_name, const
     k.group = g.group; k.epilogue = g.epilogue; k.out = g.out; k.ldo = g.ldo;
     k.ws = static_cast<float*>(h->skws.p); k.counters = static_cast<int*>(h->skcnt.p); k.err = B.err;
     if (h->use_tc && h->dt == DT_BF16 && wfmt == W_U8 && gemm_w8_tc_supported(g.M, g.N, g.K, g.group, g.epilogue))
-      return launch(L, tc_name, [&] { return launch_gemm_w8_tc(L.ctx, k); });
-    return launch(L, simt_name, [&] { return launch_gemm_skinny(L.ctx, h->dt, wfmt, k); });
+      return launch(L, nm.w8tc, [&] { return launch_gemm_w8_tc(L.ctx, k); });
+    return launch(L, nm.skinny, [&] { return launch_gemm_skinny(L.ctx, h->dt, wfmt, k); });
   }
-  return launch(L, simt_name, [&] { return launch_gemm_simt(L.ctx, h->dt, wfmt, g); });
+  return launch(L, nm.simt, [&] { return launch_gemm_simt(L.ctx, h->dt, wfmt, g); });
 }
 
 // Prefill plan (T > 4): add+RMSNorm kernels, tiled GEMMs, ping-pong residual.
@@ -976,14 +1002,14 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
     GemmArgs g{};
     g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
     g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
-    e = linear_gemm(h, L, "gemm_tc_qkv", "gemm_qkv", wfmt_of(W.qkv), g, B);
+    e = linear_gemm(h, L, kQkv, wfmt_of(W.qkv), g, B);
     if (e != cudaSuccess) return e;
     e = enqueue_attention(h, L, P, l, B);
     if (e != cudaSuccess) return e;
     GemmArgs go{};
     go.M = T; go.N = hid; go.K = H * D; go.a = B.attn; go.lda = H * D; go.w = W.o.w; go.scale = W.o.scale;
     go.bias = W.o.bias; go.group = c.group_size; go.epilogue = EPI_RESIDUAL; go.out = h_cur; go.ldo = hid;
-    e = linear_gemm(h, L, "gemm_tc_o", "gemm_o", wfmt_of(W.o), go, B);
+    e = linear_gemm(h, L, kO, wfmt_of(W.o), go, B);
     if (e != cudaSuccess) return e;
     NormArgs n2{};
     n2.h_in = h_cur; n2.pend = nullptr; n2.h_out = h_cur; n2.y = B.y; n2.gain = W.post_norm; n2.rows = T;
@@ -997,12 +1023,12 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
       GemmArgs gu{};
       gu.M = T; gu.N = I; gu.K = hid; gu.a = B.y; gu.lda = hid; gu.w = W.gate_up.w; gu.scale = W.gate_up.scale;
       gu.bias = W.gate_up.bias; gu.group = c.group_size; gu.epilogue = EPI_SWIGLU; gu.out = B.m; gu.ldo = I;
-      e = linear_gemm(h, L, "gemm_tc_gate_up", "gemm_gate_up", wfmt_of(W.gate_up), gu, B);
+      e = linear_gemm(h, L, kGateUp, wfmt_of(W.gate_up), gu, B);
       if (e != cudaSuccess) return e;
       GemmArgs d{};
       d.M = T; d.N = hid; d.K = I; d.a = B.m; d.lda = I; d.w = W.down.w; d.scale = W.down.scale;
       d.bias = W.down.bias; d.group = c.group_size; d.epilogue = EPI_STORE; d.out = B.pend; d.ldo = hid;
-      e = linear_gemm(h, L, "gemm_tc_down", "gemm_down", wfmt_of(W.down), d, B);
+      e = linear_gemm(h, L, kDown, wfmt_of(W.down), d, B);
       if (e != cudaSuccess) return e;
     }
     have_pend = true;
@@ -1014,39 +1040,6 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
   n.h_in = h_in; n.pend = B.pend; n.h_out = h_cur; n.y = out; n.gain = h->final_norm; n.rows = T; n.hidden = hid;
   n.eps = c.rms_eps;
   return launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
-}
-
-// The fused decode step (one cooperative kernel for the whole stack) applies
-// to dense stacks at decode row counts when the device and shape allow it.
-bool fused_args(qwen3_handle* h, const Plan& P, const void* x, void* out, FusedArgs& a, size_t* smem) {
-  const qwen3_config& c = h->cfg;
-  if (!h->fused || !h->coop || !h->fused_layers || !P.gemv || P.attn != ATTN_DECODE || c.num_experts != 0)
-    return false;
-  a = FusedArgs{};
-  a.layers = static_cast<const FusedLayer*>(h->fused_layers);
-  a.final_norm = h->final_norm;
-  a.L = c.num_layers; a.T = P.T; a.hidden = c.hidden; a.H = c.n_heads; a.KV = c.n_kv_heads; a.D = c.head_dim;
-  a.I = c.intermediate; a.group = c.group_size; a.eps = c.rms_eps;
-  a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
-  for (int t = 0; t < P.T; ++t) {
-    a.row_seq[t] = P.blob[P.off_rowseq + t];
-    a.row_pos[t] = P.blob[P.off_rowpos + t];
-  }
-  a.kc = h->kcache; a.vc = h->vcache;
-  a.layer_stride = (long long)h->layer_stride; a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity;
-  a.cos_t = h->rope_cos; a.sin_t = h->rope_sin;
-  a.x = x; a.out = out;
-  return fused_decode_plan(h->dt, h->wfmt, a, smem);
-}
-
-cudaError_t enqueue_fused(qwen3_handle* h, Launcher& L, FusedArgs& a, size_t smem, const Bufs& B) {
-  a.h = B.hA; a.qkv = B.qkv; a.attn = B.attn; a.mbuf = B.m; a.sumsq = B.sumsq;
-  a.part_o = B.part_o; a.part_ml = B.part_ml; a.err = B.err;
-  a.sync = static_cast<unsigned*>(h->fsync.p);
-  a.counters = static_cast<int*>(h->fsync.p) + 2;
-  cudaError_t e = cudaMemsetAsync(h->fsync.p, 0, h->fsync.bytes, L.ctx.stream);
-  if (e != cudaSuccess) return e;
-  return launch(L, "decode_fused", [&] { return launch_fused_decode(L.ctx, h->dt, h->wfmt, a, h->num_sms, smem); });
 }
 
 cudaError_t enqueue_forward(qwen3_handle* h, Launcher& L, const Plan& P, const void* x, void* out, const Bufs& B) {
@@ -1064,27 +1057,19 @@ extern "C" qwen3_status qwen3_forward(qwen3_handle* h, const void* x, int32_t T,
   Plan P;
   qwen3_status st = build_plan(h, T, seq_ids, positions, P);
   if (st != QWEN3_OK) return st;
+  if (h->cluster_attn) P.cluster = decode_cluster_size(h, P);
   st = ensure_workspace(h, P, T);
   if (st != QWEN3_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Bufs B = bufs_of(h);
   Launcher L{h, {s, h->pdl && !h->profile, h->num_sms}};
-  FusedArgs fa;
-  size_t fsmem = 0;
-  if (fused_args(h, P, x, out, fa, &fsmem)) {  // one kernel for the step; the rows travel as launch arguments
-    cudaError_t e = enqueue_fused(h, L, fa, fsmem, B);
-    if (e != cudaSuccess) return cuda_fail(h, e, "fused decode launch");
-    h->last_launches = L.count;
-    for (int t = 0; t < T; ++t) h->lengths[seq_ids[t]] = positions[t] + 1;
-    return QWEN3_OK;
-  }
   st = upload_plan(h, P, s);
   if (st != QWEN3_OK) return st;
   const bool graph = h->use_graphs && !h->profile && P.gemv;
   cudaError_t e;
   if (graph) {
     const int runs = P.attn == ATTN_DECODE && P.n_items > std::max(1, (h->num_sms + h->cfg.n_kv_heads - 1) / h->cfg.n_kv_heads);
-    const GraphKey key{T, P.attn * 64 + P.max_nq + (runs ? 32 : 0), x, out};
+    const GraphKey key{T, P.attn * 64 + P.max_nq + (runs ? 32 : 0) + (P.cluster > 1 ? 16 : 0), x, out};
     if (h->graphs.size() > 32) {  // callers cycling through buffers: start over
       for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
       h->graphs.clear();
@@ -1152,6 +1137,13 @@ extern "C" qwen3_status qwen3_moe_layer(qwen3_handle* h, int32_t layer, const vo
   return QWEN3_OK;
 }
 
+extern "C" qwen3_status qwen3_selftest_bounded_wait(qwen3_handle* h, void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  cudaError_t e = launch_wait_probe(static_cast<cudaStream_t>(stream), static_cast<int*>(h->dev_err.p));
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  return QWEN3_OK;
+}
+
 extern "C" qwen3_status qwen3_device_error(qwen3_handle* h, int32_t* code) {
   if (!h || !code) return QWEN3_E_ARG;
   *code = 0;
@@ -1165,6 +1157,130 @@ extern "C" qwen3_status qwen3_device_error(qwen3_handle* h, int32_t* code) {
     *code = v;
     return fail(h, QWEN3_E_DEVICE, "a kernel gave up waiting for its data (code " + std::to_string(v) + ")");
   }
+  return QWEN3_OK;
+}
+
+// ======================================================================
+// embedding rows, output head, pooled sentence vector
+// ======================================================================
+namespace {
+
+// Host ints -> device buffer through the pinned staging ring.
+qwen3_status upload_ints(qwen3_handle* h, const int32_t* v, int n, DevBuf& dst, cudaStream_t s) {
+  qwen3_status st = ensure(h, dst, (size_t)n * 4 + 64, false);
+  if (st != QWEN3_OK) return st;
+  const int i = h->ring_pos;
+  h->ring_pos = (h->ring_pos + 1) % qwen3_handle::kRing;
+  cudaEventSynchronize(h->pinned_ev[i]);
+  const size_t bytes = (size_t)n * 4;
+  if (h->pinned_bytes[i] < bytes) {
+    if (h->pinned[i]) cudaFreeHost(h->pinned[i]);
+    h->pinned[i] = nullptr;
+    const size_t nb = std::max(bytes, (size_t)4096) * 2;
+    if (cudaHostAlloc(&h->pinned[i], nb, cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      h->pinned_bytes[i] = 0;
+      return fail(h, QWEN3_E_OOM, "pinned host allocation failed");
+    }
+    h->pinned_bytes[i] = nb;
+  }
+  std::memcpy(h->pinned[i], v, bytes);
+  cudaError_t e = cudaMemcpyAsync(dst.p, h->pinned[i], bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "id upload");
+  cudaEventRecord(h->pinned_ev[i], s);
+  return QWEN3_OK;
+}
+
+}  // namespace
+
+extern "C" qwen3_status qwen3_embed(qwen3_handle* h, const void* table, int32_t vocab, const int32_t* ids, int32_t n,
+                                    void* out, void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  if (!table || !ids || !out) return fail(h, QWEN3_E_ARG, "null pointer argument");
+  if (vocab < 1 || n < 1 || n > (1 << 20)) return fail(h, QWEN3_E_ARG, "vocab or row count out of range");
+  if (!aligned16(table) || !aligned16(out)) return fail(h, QWEN3_E_ARG, "table and out must be 16-byte aligned");
+  for (int t = 0; t < n; ++t)
+    if (ids[t] < 0 || ids[t] >= vocab)
+      return fail(h, QWEN3_E_ARG, "token id " + std::to_string(ids[t]) + " at row " + std::to_string(t) +
+                                      " is outside [0, " + std::to_string(vocab) + ")");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  qwen3_status st = upload_ints(h, ids, n, h->ids, s);
+  if (st != QWEN3_OK) return st;
+  Launcher L{h, {s, h->pdl && !h->profile, h->num_sms}};
+  EmbedArgs a{table, static_cast<const int*>(h->ids.p), n, h->cfg.hidden, out};
+  cudaError_t e = launch(L, "embed_gather", [&] { return launch_embed_gather(L.ctx, h->dt, a); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  h->last_launches = L.count;
+  return QWEN3_OK;
+}
+
+extern "C" qwen3_status qwen3_head(qwen3_handle* h, const void* w, int32_t n_out, const void* x, int32_t T,
+                                   float* logits, void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  if (!w || !x || !logits) return fail(h, QWEN3_E_ARG, "null pointer argument");
+  if (n_out < 1 || T < 1 || T > (1 << 20)) return fail(h, QWEN3_E_ARG, "row or output count out of range");
+  if (!aligned16(w) || !aligned16(x)) return fail(h, QWEN3_E_ARG, "w and x must be 16-byte aligned");
+  const int hid = h->cfg.hidden;
+  Launcher L{h, {static_cast<cudaStream_t>(stream), h->pdl && !h->profile, h->num_sms}};
+  cudaError_t e;
+  if (T <= 4) {
+    GemvArgs g{};
+    g.T = T; g.K = hid; g.N = n_out; g.w = w; g.x_rows = T; g.x = x; g.epilogue = EPI_STORE_RF32;
+    g.out = logits; g.ldo = n_out;
+    e = launch(L, "gemv_head", [&] { return launch_gemv(L.ctx, h->dt, W_DT, g); });
+  } else {
+    GemmArgs g{};
+    g.M = T; g.N = n_out; g.K = hid; g.a = x; g.lda = hid; g.w = w; g.epilogue = EPI_STORE_RF32;
+    g.out = logits; g.ldo = n_out;
+    e = launch(L, "gemm_head", [&] { return launch_gemm_simt(L.ctx, h->dt, W_DT, g); });
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  h->last_launches = L.count;
+  return QWEN3_OK;
+}
+
+extern "C" qwen3_status qwen3_embed_pooled(qwen3_handle* h, const void* x, int32_t T, int32_t seq, void* out,
+                                           void* stream) {
+  if (!h) return QWEN3_E_ARG;
+  if (!x || !out) return fail(h, QWEN3_E_ARG, "null pointer argument");
+  if (seq < 0 || seq >= h->cfg.max_seqs) return fail(h, QWEN3_E_SEQ, "sequence id out of range");
+  if (T < 1 || T > h->cfg.capacity)
+    return fail(h, QWEN3_E_CAPACITY, "row count must be in [1, capacity] (the sequence restarts at position 0)");
+  if (!aligned16(x) || !aligned16(out)) return fail(h, QWEN3_E_ARG, "x and out must be 16-byte aligned");
+  const size_t row_bytes = (size_t)h->cfg.hidden * h->esz;
+  qwen3_status st = ensure(h, h->pool_rows, (size_t)T * row_bytes, false);
+  if (st != QWEN3_OK) return st;
+  std::vector<int32_t> sids(T, seq), pos(T);
+  for (int t = 0; t < T; ++t) pos[t] = t;
+  const int32_t saved = h->lengths[seq];
+  h->lengths[seq] = 0;  // positions 0..T-1 of a fresh sequence (the cache is cleared below)
+  Plan P;
+  st = build_plan(h, T, sids.data(), pos.data(), P);
+  h->lengths[seq] = saved;
+  if (st != QWEN3_OK) return st;
+  st = qwen3_reset(h, seq, stream);
+  if (st != QWEN3_OK) return st;
+  st = qwen3_forward(h, x, T, sids.data(), pos.data(), h->pool_rows.p, stream);
+  if (st != QWEN3_OK) return st;
+  const int64_t fwd_launches = h->last_launches;
+  Launcher L{h, {static_cast<cudaStream_t>(stream), h->pdl && !h->profile, h->num_sms}};
+  L2PoolArgs a{static_cast<const char*>(h->pool_rows.p) + (size_t)(T - 1) * row_bytes, h->cfg.hidden, out};
+  cudaError_t e = launch(L, "l2_pool", [&] { return launch_l2_pool(L.ctx, h->dt, a); });
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  h->last_launches = fwd_launches + L.count;
+  return QWEN3_OK;
+}
+
+extern "C" qwen3_status qwen3_workspace_bytes(const qwen3_handle* h, int64_t* bytes) {
+  if (!h || !bytes) return QWEN3_E_ARG;
+  const DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
+                          &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
+                          &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc,
+                          &h->sumsq, &h->dev_err, &h->skws, &h->skcnt, &h->ysort, &h->ids,
+                          &h->pool_rows};
+  int64_t n = 0;
+  for (const DevBuf* b : bufs) n += (int64_t)b->bytes;
+  *bytes = n;
   return QWEN3_OK;
 }
 
@@ -1253,6 +1369,13 @@ qwen3_status moe_layer_on_scratch(qwen3_handle* h, int32_t layer, const void* y,
   B.sorted_src = reinterpret_cast<int*>(base + S.sorted_src);
   B.mexp = base + S.mexp;
   B.zexp = base + S.zexp;
+  // The tensor-core path gathers the rows into expert order first (ysort,
+  // slots x hidden, the size of zexp).  ysort is read only by the gate|up GEMM
+  // and zexp is first written by the down GEMM, which starts after it (stream
+  // order; its stores follow its wait on the gate|up kernel), so the two share
+  // one region.
+  if (h->dt == DT_BF16 && T > 4) B.ysort = B.zexp;
+  B.err = static_cast<int*>(h->dev_err.p);
   Launcher L{h, {s, h->pdl, h->num_sms}};
   e = moe_block(h, L, layer, y, T, out, nullptr, nullptr, topk_idx, topk_w, B);
   if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");

@@ -217,22 +217,6 @@ def test_launch_options_do_not_change_results(cuda_ok, graphs, pdl):
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("cfg", [SMALL_D128, I.with_sizes(SMALL_D128, dtype="fp32"), SMALL_INT8],
-                         ids=["bf16", "fp32", "int8"])
-def test_fused_decode_step(cuda_ok, cfg):
-    """The whole-step persistent kernel (QWEN3_OPT_FUSED_DECODE): decode rows of
-    one to four sequences, 1-4 rows per call, against the oracle."""
-    cfg = I.with_sizes(cfg, max_seqs=3)
-    p = Parity(cfg, seed=2050)
-    Q.qwen3_set_option(p.stack.h, Q.QWEN3_OPT_FUSED_DECODE, 1)
-    p.step(I.make_rows(cfg, 37, seed=2051).cuda(), seq_ids=[0] * 37)        # prefill (not fused)
-    p.step(I.make_rows(cfg, 9, seed=2052).cuda(), seq_ids=[1] * 9)
-    for i, sids in enumerate([[0], [1], [0, 0], [0, 1], [2, 2, 2], [0, 1, 1, 2]]):
-        p.step(I.make_rows(cfg, len(sids), seed=2053 + i).cuda(), seq_ids=sids)
-    p.close()
-    p.check()
-
-
 def test_errors_leave_state_unchanged(cuda_ok):
     """Capacity overflow, a position gap, a bad or split sequence: each returns its
     status before any launch, the lengths stay put, the output is untouched, and
@@ -280,3 +264,23 @@ def test_reset_then_reuse(cuda_ok):
     assert Q.qwen3_get_length(stack.h, 0) == 0
     assert torch.equal(stack.forward(x), first)
     stack.close()
+
+
+@pytest.mark.parametrize("cfg", [SMALL_D128, I.with_sizes(SMALL_D128, dtype="fp32"), SMALL_MOE],
+                         ids=["bf16", "fp32", "moe_g8"])
+@pytest.mark.parametrize("cluster", [1, 0])
+def test_decode_attention_cluster_and_split_k(cuda_ok, cfg, cluster):
+    """Decode attention of few query blocks runs on thread-block clusters
+    (partials merged through distributed shared memory) unless switched off
+    (split-K with the global merge): both against the oracle, at contexts
+    from one key to a few hundred, one to four rows per sequence."""
+    cfg = I.with_sizes(cfg, max_seqs=3, capacity=400)
+    p = Parity(cfg, seed=2400 + cluster)
+    Q.qwen3_set_option(p.stack.h, Q.QWEN3_OPT_CLUSTER_ATTENTION, cluster)
+    p.step(I.make_rows(cfg, 1, seed=2401).cuda(), seq_ids=[0])                       # one key
+    p.fill_cache(1, 333, seed=2402)
+    p.fill_cache(2, 64, seed=2403)
+    for i, sids in enumerate([[1], [2], [0, 1], [1, 1, 1], [0, 1, 2], [2, 2, 2, 2], [1]]):
+        p.step(I.make_rows(cfg, len(sids), seed=2410 + i).cuda(), seq_ids=sids)
+    p.close()
+    p.check()

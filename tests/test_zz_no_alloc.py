@@ -5,17 +5,20 @@ The static variant keeps all of its scratch in one fixed array inside the
 library, so callers whose memory is fully reserved up front, or owned by
 another allocator, can still run the MoE block.  These tests call it through
 the C ABI twice in a row -- the second call finds the first call's leftovers
-in the shared array -- and compare each result with qwen3_moe_layer on the
-same rows: expert indices exactly, weights to 1e-6, outputs within the bf16
-bound the other parity tests use.  Rows past the array's limit must be
-refused before any work is enqueued.
+in the shared array -- and check that:
+
+* it runs the same kernels as qwen3_moe_layer (the same launch count, the
+  tensor-core grouped expert GEMMs included), so its results are bitwise
+  equal to qwen3_moe_layer's;
+* it allocates nothing: after a first call, further calls of other row counts
+  leave the device's free memory and the handle's workspace as they were;
+* rows past the array's limit are refused before any work is enqueued.
 
 The file is named to be collected last.
 """
 import pytest
 import torch
 
-from gpu_helpers import TOL, rel_err
 from qwen3_decoder_layer_gb300 import binding as Q
 from qwen3_decoder_layer_gb300 import inputs as I
 
@@ -32,7 +35,7 @@ def _run(fn, stack, cfg, y):
     idx = torch.empty(T, cfg.top_k, dtype=torch.int32, device="cuda")
     w = torch.empty(T, cfg.top_k, dtype=torch.float32, device="cuda")
     fn(stack.h, 0, y, out, idx, w)
-    return out, idx, w
+    return out, idx, w, Q.qwen3_last_launch_count(stack.h)
 
 
 def _two_calls_match(cfg, seed, rows):
@@ -42,10 +45,10 @@ def _two_calls_match(cfg, seed, rows):
         static = [_run(Q.qwen3_moe_layer_static, stack, cfg, y) for y in ys]  # back to back
         ref = [_run(Q.qwen3_moe_layer, stack, cfg, y) for y in ys]
         torch.cuda.synchronize()
-        for (o_s, i_s, w_s), (o_r, i_r, w_r) in zip(static, ref):
-            assert torch.equal(i_s, i_r)
-            assert torch.max(torch.abs(w_s - w_r)).item() <= 1e-6
-            assert rel_err(o_s, o_r) <= TOL[cfg.dtype]
+        for (o_s, i_s, w_s, n_s), (o_r, i_r, w_r, n_r) in zip(static, ref):
+            assert n_s == n_r, "the static variant launched other kernels"
+            assert torch.equal(i_s, i_r) and torch.equal(w_s, w_r)
+            assert torch.equal(o_s, o_r)
     finally:
         stack.close()
 
@@ -62,6 +65,24 @@ def test_static_scratch_full_size_moe(cuda_ok, rows):
     _two_calls_match(FULL_1L, 2200 + sum(rows), rows)
 
 
+def test_static_scratch_allocates_nothing(cuda_ok):
+    stack = Q.Qwen3Stack(FULL_1L, I.make_weights(FULL_1L, seed=2250, device="cuda"))
+    try:
+        ys = [I.make_rows(FULL_1L, T, seed=2252 + T).cuda() for T in (1, 5, 17, 64, 91)]
+        for y in ys:   # first use of each kernel (lazy module loading may take device memory once)
+            _run(Q.qwen3_moe_layer_static, stack, FULL_1L, y)
+        torch.cuda.synchronize()
+        free0, ws0 = torch.cuda.mem_get_info()[0], Q.qwen3_workspace_bytes(stack.h)
+        ys = ys[::-1] + ys
+        for y in ys:
+            _run(Q.qwen3_moe_layer_static, stack, FULL_1L, y)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert Q.qwen3_workspace_bytes(stack.h) == ws0
+    finally:
+        stack.close()
+
+
 def test_static_scratch_rejects_too_many_rows(cuda_ok):
     stack = Q.Qwen3Stack(FULL_1L, I.make_weights(FULL_1L, seed=2300, device="cuda"))
     try:
@@ -70,9 +91,9 @@ def test_static_scratch_rejects_too_many_rows(cuda_ok):
         assert Q.STATUS[ei.value.status] == "QWEN3_E_ARG" and "at most 91 rows" in str(ei.value)
         # the refused call enqueued nothing; the next one works
         y = I.make_rows(FULL_1L, 2, seed=2302).cuda()
-        o_s, i_s, _ = _run(Q.qwen3_moe_layer_static, stack, FULL_1L, y)
-        o_r, i_r, _ = _run(Q.qwen3_moe_layer, stack, FULL_1L, y)
+        o_s, i_s, _, _ = _run(Q.qwen3_moe_layer_static, stack, FULL_1L, y)
+        o_r, i_r, _, _ = _run(Q.qwen3_moe_layer, stack, FULL_1L, y)
         torch.cuda.synchronize()
-        assert torch.equal(i_s, i_r) and rel_err(o_s, o_r) <= TOL["bf16"]
+        assert torch.equal(i_s, i_r) and torch.equal(o_s, o_r)
     finally:
         stack.close()
