@@ -291,8 +291,9 @@ class Qwen3Oracle:
         length..length+T-1 and raises on overflow.  If ``trace`` is a list,
         each layer appends a dict of its intermediate tensors.  ``taps`` is a
         dict keyed by layer index: each listed layer stores there the residual
-        entering it ("h_in"), the residual after its attention ("h") and its MLP
-        output ("pend") -- the pieces a one-layer stack needs to reproduce it."""
+        entering it ("h_in"), the residual after its attention ("h"), the MLP's
+        input ("y2") and its output ("pend") -- the pieces a one-layer stack
+        needs to reproduce it."""
         cfg, R = self.cfg, (lambda a: rnd(a, self.prec))
         x = _f64(x)
         T = x.shape[0]
@@ -369,7 +370,7 @@ class Qwen3Oracle:
                     raise ValueError(f"layer {li} is a dense layer but its weights have no MLP")
                 pend = self.dense_mlp(L, y2)
             if taps is not None and li in taps:
-                taps[li].update(h=h, pend=pend)
+                taps[li].update(h=h, pend=pend, y2=y2)
             if trace is not None:
                 trace.append({"y": y, "qkv": qkv, "q": q, "k": k, "v": v, "a": a,
                               "h": h, "y2": y2, "pend": pend})
