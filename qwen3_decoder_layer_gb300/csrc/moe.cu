@@ -70,26 +70,33 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
   }
 }
 
-// Single block: offsets and row-tile prefix of the experts' sorted rows.
-__global__ void moe_scan_kernel(MoeScanArgs a) {
+// Single block, one thread per expert (E <= 256): exclusive prefix sums of
+// the experts' row counts (sorted row offsets) and of their row tiles, by a
+// warp-shuffle scan inside each warp and a scan of the warp totals.
+__global__ void __launch_bounds__(256) moe_scan_kernel(MoeScanArgs a) {
+  __shared__ int s_rows[8], s_tiles[8];
   pdl_wait();
   pdl_launch();
-  if (threadIdx.x == 0) {
-    int off = 0, tiles = 0;
-    for (int e = 0; e < a.E; ++e) {
-      const int c = a.counts[e];
-      a.row_off[e] = off;
-      a.row_cnt[e] = c;
-      a.tile_start[e] = tiles;
-      off += c;
-      tiles += (c + a.bm - 1) / a.bm;
-    }
-    a.tile_start[a.E] = tiles;
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const int c = e < a.E ? a.counts[e] : 0;
+  const int tl = (c + a.bm - 1) / a.bm;
+  int rows = c, tiles = tl;  // inclusive scans within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int r = __shfl_up_sync(0xffffffffu, rows, o), t = __shfl_up_sync(0xffffffffu, tiles, o);
+    if (lane >= o) { rows += r; tiles += t; }
   }
+  if (lane == 31) { s_rows[warp] = rows; s_tiles[warp] = tiles; }
   __syncthreads();
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+  int rbase = 0, tbase = 0;
+  for (int w = 0; w < warp; ++w) { rbase += s_rows[w]; tbase += s_tiles[w]; }
+  if (e < a.E) {
+    a.row_off[e] = rbase + rows - c;
+    a.row_cnt[e] = c;
+    a.tile_start[e] = tbase + tiles - tl;
     a.cursor[e] = 0;
     a.counts[e] = 0;
+    if (e == a.E - 1) a.tile_start[a.E] = tbase + tiles;
   }
 }
 
@@ -166,6 +173,7 @@ cudaError_t launch_moe_gather(const LaunchCtx& c, int dt, const MoeGatherArgs& a
 }
 
 cudaError_t launch_moe_scan(const LaunchCtx& c, const MoeScanArgs& a) {
+  if (a.E > 256) return cudaErrorInvalidValue;
   return launch_k(moe_scan_kernel, dim3(1), dim3(256), 0, c, a);
 }
 

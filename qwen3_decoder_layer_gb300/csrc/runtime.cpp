@@ -788,12 +788,13 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
 
 // Decode attention with one query block per thread-block cluster when every
 // (query block, kv head) gets its own cluster, all of them resident at once,
-// and each query block's keys fit the cluster's shared memory: 16 CTAs per
-// cluster where the device allows it, else 8.
+// and each query block's keys fit the cluster's shared memory: the largest of
+// 16, 12 or 8 CTAs per cluster that fits (on a 152-SM GB300, seven 16-CTA
+// clusters of this kernel are resident at once, eight of 12, fifteen of 8).
 int decode_cluster_size(qwen3_handle* h, const Plan& P) {
   if (P.attn != ATTN_DECODE || P.n_qblocks < 1) return 0;
   const qwen3_config& c = h->cfg;
-  for (int cl : {16, 8}) {
+  for (int cl : {16, 12, 8}) {
     if ((int64_t)P.n_qblocks * c.n_kv_heads * cl > h->num_sms) continue;
     if (P.max_keys > attn_decode_cluster_keys(h->dt, P.max_nq, cl)) continue;
     const int nqb = P.max_nq <= 1 ? 1 : P.max_nq <= 2 ? 2 : P.max_nq <= 4 ? 4 : 8;
@@ -838,7 +839,8 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
       a.runs = 0;
     }
     a.pf = pf; a.pf_bytes = pf_bytes;
-    return launch(L, "attn_decode", [&] { return launch_attn_decode2(L.ctx, dt, a); });
+    return launch(L, a.cluster > 1 ? "attn_decode_cluster" : "attn_decode",
+                  [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
   QkRopeArgs r{};
   r.qkv = B.qkv; r.T = P.T; r.H = c.n_heads; r.KV = KV; r.D = D; r.q_out = B.q; r.kcache = kc; r.vcache = vc;
