@@ -256,9 +256,13 @@ QWEN3_API qwen3_status qwen3_get_length(const qwen3_handle* h, int32_t seq, int3
 #define QWEN3_OPT_PROFILE 2       /* 1 = launch directly and time every kernel with CUDA events */
 #define QWEN3_OPT_PDL 3           /* 1 (default) = programmatic dependent launch between kernels */
 #define QWEN3_OPT_TENSOR_CORES 4  /* 1 (default) = tcgen05 for bf16 prefill linears and attention, MoE expert GEMMs, and int8 linears of 5..32 rows; 0 = CUDA cores */
-#define QWEN3_OPT_L2_PREFETCH 5   /* 1 (default) = decode kernels prefetch the next linear's weights into L2 */
+#define QWEN3_OPT_L2_PREFETCH 5   /* decode kernels prefetch weights into L2 ahead of their kernel: 0 (default) = off;
+                                     1 = each kernel the next one's; 2 = attention o_proj's and gate|up's, o_proj
+                                     down's, down the next qkv's */
 #define QWEN3_OPT_CLUSTER_ATTENTION 8 /* 1 (default) = decode attention of few sequences on thread-block clusters
                                          (partials merged in distributed shared memory); 0 = split-K with a global merge */
+#define QWEN3_OPT_GEMV_CORESIDENT 9 /* 1 = decode GEMV blocks take at most half an SM, so the next kernel's blocks
+                                       stream their weights while these finish; 0 (default) = one block per SM */
 #define QWEN3_OPT_FAIL_ALLOC 7    /* failure injection: n > 0 makes the n-th next workspace allocation fail as if
                                      cudaMalloc had (QWEN3_E_OOM, no state change); 0 (default) = off */
 QWEN3_API qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value);

@@ -24,6 +24,7 @@ QWEN3_OPT_CUDA_GRAPHS, QWEN3_OPT_PROFILE, QWEN3_OPT_PDL, QWEN3_OPT_TENSOR_CORES 
 QWEN3_OPT_L2_PREFETCH = 5
 QWEN3_OPT_FAIL_ALLOC = 7
 QWEN3_OPT_CLUSTER_ATTENTION = 8
+QWEN3_OPT_GEMV_CORESIDENT = 9
 
 
 class Qwen3Error(RuntimeError):

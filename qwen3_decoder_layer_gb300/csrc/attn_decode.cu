@@ -108,6 +108,15 @@ __device__ __forceinline__ float ld_cluster(uint32_t addr) {
   return v;
 }
 
+// L2 prefetch of this block's share of [p, p + bytes) over the whole grid.
+__device__ __forceinline__ void prefetch_grid_share(const void* p, size_t bytes) {
+  if (!p || !bytes) return;
+  const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
+  const size_t per = ((bytes + nb - 1) / nb + 15) & ~size_t(15);
+  for (size_t b0 = per * b, b1 = min(per * (b + 1), bytes); b0 < b1; b0 += 65536)
+    prefetch_l2(static_cast<const char*>(p) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
+}
+
 // Keys of an item: [key0, key0 + nkeys) in nsub sub-chunks.
 struct ItemKeys {
   int key0, nkeys, nsub;
@@ -417,13 +426,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           *(volatile int*)&s_issued[s] = g / LY::STAGES + 1;
         }
       }
-      // L2 prefetch of this block's share of the next kernel's operand
-      if (a.pf && a.pf_bytes) {
-        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
-        const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
-        for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
-          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
-      }
+      // L2 prefetch of this block's share of the next kernels' operands
+      prefetch_grid_share(a.pf, a.pf_bytes);
+      prefetch_grid_share(a.pf2, a.pf2_bytes);
     }
     return;
   }
@@ -690,13 +695,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
           tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
         }
       }
-      // L2 prefetch of this block's share of the next kernel's operand
-      if (a.pf && a.pf_bytes) {
-        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
-        const size_t per = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
-        for (size_t b0 = per * b, b1 = min(per * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
-          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
-      }
+      // L2 prefetch of this block's share of the next kernels' operands
+      prefetch_grid_share(a.pf, a.pf_bytes);
+      prefetch_grid_share(a.pf2, a.pf2_bytes);
     }
     return;
   }
@@ -914,12 +915,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
         tma_load_1d(tiles(sub), kc + off, bytes, &full[sub]);
         tma_load_1d(tiles(sub) + LY::TILE, vc + off, bytes, &full[sub]);
       }
-      if (a.pf && a.pf_bytes) {  // L2 prefetch of this CTA's share of the next kernel's operand
-        const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
-        const size_t pshare = ((a.pf_bytes + nb - 1) / nb + 15) & ~size_t(15);
-        for (size_t b0 = pshare * b, b1 = min(pshare * (b + 1), a.pf_bytes); b0 < b1; b0 += 65536)
-          prefetch_l2(static_cast<const char*>(a.pf) + b0, (uint32_t)min(b1 - b0, (size_t)65536));
-      }
+      // L2 prefetch of this CTA's share of the next kernels' operands
+      prefetch_grid_share(a.pf, a.pf_bytes);
+      prefetch_grid_share(a.pf2, a.pf2_bytes);
     }
   } else {
     // ---------------------------------------------------------- consumers

@@ -30,6 +30,7 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 
 constexpr int G2_MAX_WARPS = 16;
 constexpr size_t G2_SMEM_LIMIT = 220 * 1024;
+constexpr size_t G2_SMEM_CORES = 110 * 1024;  // two CTAs per SM
 
 struct G2Layout {
   size_t x_bytes, row_bytes, unit_bytes, ring_bytes, total;
@@ -368,20 +369,25 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
 
 }  // namespace
 
-int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps) {
+int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps, bool coresident) {
   (void)group;
   const int wbytes = wfmt == W_U8 ? 1 : (dt == DT_BF16 ? 2 : 4);
   const int xbytes = dt == DT_BF16 ? 2 : 4;
-  for (int nw = G2_MAX_WARPS; nw >= 4; nw /= 2)
+  // co-resident: at most half of an SM (shared memory, threads), so the next
+  // kernel's CTAs, launched early, start streaming their weights beside these
+  const size_t limit = coresident ? G2_SMEM_CORES : G2_SMEM_LIMIT;
+  const int max_warps = coresident ? G2_MAX_WARPS / 2 : G2_MAX_WARPS;
+  for (int nw = max_warps; nw >= 4; nw /= 2)
     for (int s = 4; s >= (nw == 4 ? 1 : 2); --s) {
       const G2Layout L = g2_layout(wbytes, xbytes, T, K, pair, s, nw);
-      if (L.total <= G2_SMEM_LIMIT) {
+      if (L.total <= limit) {
         if (nwarps) *nwarps = nw;
         return s;
       }
     }
   if (nwarps) *nwarps = 4;
-  return g2_layout(wbytes, xbytes, T, K, pair, 1, 4).total <= G2_SMEM_LIMIT ? 1 : 0;
+  if (g2_layout(wbytes, xbytes, T, K, pair, 1, 4).total <= limit) return 1;
+  return coresident ? gemv2_plan(dt, wfmt, T, K, group, pair, nwarps, false) : 0;
 }
 
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a) {

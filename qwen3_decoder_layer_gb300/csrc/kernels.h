@@ -306,8 +306,9 @@ struct Gemv2Args {
 };
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a);
 // Ring slots per warp (return value, 0 = does not fit) and warps per block
-// (*nwarps) for a linear of K inputs at T rows.
-int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps);
+// (*nwarps) for a linear of K inputs at T rows; `coresident` keeps a block to
+// half an SM so that two kernels' blocks share it.
+int gemv2_plan(int dt, int wfmt, int T, int K, int group, bool pair, int* nwarps, bool coresident);
 
 // Decode attention with the q/k RMSNorm, RoPE and cache append fused in:
 // items as in AttnArgs; K/V chunks stream into a shared-memory ring by TMA;
@@ -340,8 +341,10 @@ struct AttnDecArgs {
   int cluster;         // > 1: one query block per cluster of this many CTAs (grid_x = cluster x query blocks),
                        // partials merged through distributed shared memory; items and partial buffers unused
   int* err;
-  const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
+  const void* pf;      // L2 prefetches (before the wait) of the next kernels' operands
   size_t pf_bytes;
+  const void* pf2;
+  size_t pf2_bytes;
 };
 cudaError_t launch_attn_decode2(const LaunchCtx& c, int dt, const AttnDecArgs& a);
 int attn_decode2_chunk(int dt);

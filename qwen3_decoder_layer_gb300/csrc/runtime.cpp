@@ -74,8 +74,10 @@ struct qwen3_handle {
   std::vector<int32_t> lengths;
   std::string err;
   // options
-  bool use_graphs = true, profile = false, pdl = true, use_tc = true, l2_prefetch = true;
+  bool use_graphs = true, profile = false, pdl = true, use_tc = true;
+  int l2_prefetch = 0;  // off: measured faster on the batch-1 decode step (the prefetches compete with the loads)
   bool cluster_attn = true;   // decode attention on thread-block clusters where it fits
+  bool coresident = false;    // decode GEMVs sized for two blocks per SM
   int64_t fail_alloc_in = 0;  // test hook: the n-th next workspace allocation fails (0 = off)
   std::map<int64_t, int> cluster_cap;  // resident clusters of the decode-attention cluster kernel, by launch shape
   // workspace buffers (grow only)
@@ -428,13 +430,22 @@ qwen3_status qwen3_get_length(const qwen3_handle* h, int32_t seq, int32_t* lengt
 
 qwen3_status qwen3_set_option(qwen3_handle* h, int32_t option, int64_t value) {
   if (!h) return QWEN3_E_ARG;
+  if (option != QWEN3_OPT_FAIL_ALLOC && !h->graphs.empty()) {  // captured launches follow the old options
+    cudaDeviceSynchronize();
+    for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.first);
+    h->graphs.clear();
+  }
   switch (option) {
     case QWEN3_OPT_CUDA_GRAPHS: h->use_graphs = value != 0; return QWEN3_OK;
     case QWEN3_OPT_PROFILE: h->profile = value != 0; return QWEN3_OK;
     case QWEN3_OPT_PDL: h->pdl = value != 0; return QWEN3_OK;
     case QWEN3_OPT_TENSOR_CORES: h->use_tc = value != 0; return QWEN3_OK;
-    case QWEN3_OPT_L2_PREFETCH: h->l2_prefetch = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_L2_PREFETCH:
+      if (value < 0 || value > 2) return fail(h, QWEN3_E_ARG, "QWEN3_OPT_L2_PREFETCH takes 0, 1 or 2");
+      h->l2_prefetch = (int)value;
+      return QWEN3_OK;
     case QWEN3_OPT_CLUSTER_ATTENTION: h->cluster_attn = value != 0; return QWEN3_OK;
+    case QWEN3_OPT_GEMV_CORESIDENT: h->coresident = value != 0; return QWEN3_OK;
     case QWEN3_OPT_FAIL_ALLOC:
       if (value < 0) return fail(h, QWEN3_E_ARG, "QWEN3_OPT_FAIL_ALLOC takes a count >= 0");
       h->fail_alloc_in = value;
@@ -810,7 +821,8 @@ int decode_cluster_size(qwen3_handle* h, const Plan& P) {
 
 // Attention of layer l for the plan's kernel.
 cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l, const Bufs& B,
-                              const void* pf = nullptr, size_t pf_bytes = 0) {
+                              const void* pf = nullptr, size_t pf_bytes = 0, const void* pf2 = nullptr,
+                              size_t pf2_bytes = 0) {
   const qwen3_config& c = h->cfg;
   const qwen3_layer_weights& W = h->layers[l];
   const int dt = h->dt, KV = c.n_kv_heads, D = c.head_dim;
@@ -838,7 +850,7 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
       a.grid_x = P.cluster * P.n_qblocks;
       a.runs = 0;
     }
-    a.pf = pf; a.pf_bytes = pf_bytes;
+    a.pf = pf; a.pf_bytes = pf_bytes; a.pf2 = pf2; a.pf2_bytes = pf2_bytes;
     return launch(L, a.cluster > 1 ? "attn_decode_cluster" : "attn_decode",
                   [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
@@ -883,7 +895,11 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
   auto lin_bytes = [&](const qwen3_linear& lin, int rows, int K) {
     return (size_t)rows * K * (lin.scale ? 1 : h->esz);
   };
-  const bool pf_on = h->l2_prefetch;
+  // L2 prefetch of weights ahead of their kernels: 1 = each kernel asks for
+  // the next one's; 2 = the attention kernel (far below the HBM rate) asks
+  // for o_proj's and gate|up's, o_proj for down's, down for the next qkv's.
+  const int pf_mode = h->l2_prefetch;
+  const bool pf_on = pf_mode == 1;
   cudaError_t e;
   for (int l = 0; l < NL; ++l) {
     const qwen3_layer_weights& W = h->layers[l];
@@ -897,12 +913,16 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       } else {
         g.prologue = PRO_SUMSQ; g.sumsq_in = slot(2 * l);
       }
-      g.stages = gemv2_plan(dt, wfmt_of(W.qkv), T, hid, c.group_size, false, &g.nwarps);
+      g.stages = gemv2_plan(dt, wfmt_of(W.qkv), T, hid, c.group_size, false, &g.nwarps, h->coresident);
       e = launch(L, "gemv_qkv", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.qkv), g); });
       if (e != cudaSuccess) return e;
     }
     const bool moe = is_moe_layer(h, l);
-    e = enqueue_attention(h, L, P, l, B, pf_on ? W.o.w : nullptr, lin_bytes(W.o, hid, H * D));
+    if (pf_mode == 2 && !moe)
+      e = enqueue_attention(h, L, P, l, B, W.o.w, lin_bytes(W.o, hid, H * D), W.gate_up.w,
+                            lin_bytes(W.gate_up, 2 * I, hid));
+    else
+      e = enqueue_attention(h, L, P, l, B, pf_mode ? W.o.w : nullptr, lin_bytes(W.o, hid, H * D));
     if (e != cudaSuccess) return e;
     {
       Gemv2Args g{};
@@ -910,7 +930,8 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.prologue = PRO_X; g.x = B.attn; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
       g.sumsq_out = slot(2 * l + 1); g.err = B.err;
       if (pf_on && !moe) { g.pf = W.gate_up.w; g.pf_bytes = lin_bytes(W.gate_up, 2 * I, hid); }
-      g.stages = gemv2_plan(dt, wfmt_of(W.o), T, H * D, c.group_size, false, &g.nwarps);
+      if (pf_mode == 2 && !moe) { g.pf = W.down.w; g.pf_bytes = lin_bytes(W.down, hid, I); }
+      g.stages = gemv2_plan(dt, wfmt_of(W.o), T, H * D, c.group_size, false, &g.nwarps, h->coresident);
       e = launch(L, "gemv_o", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.o), g); });
       if (e != cudaSuccess) return e;
     }
@@ -930,7 +951,7 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.group = c.group_size; g.prologue = PRO_SUMSQ; g.h = hres; g.gain = W.post_norm; g.eps = c.rms_eps;
       g.sumsq_in = slot(2 * l + 1); g.epilogue = EPI_SWIGLU; g.out = B.m; g.ldo = I; g.err = B.err;
       if (pf_on) { g.pf = W.down.w; g.pf_bytes = lin_bytes(W.down, hid, I); }
-      g.stages = gemv2_plan(dt, wfmt_of(W.gate_up), T, hid, c.group_size, true, &g.nwarps);
+      g.stages = gemv2_plan(dt, wfmt_of(W.gate_up), T, hid, c.group_size, true, &g.nwarps, h->coresident);
       e = launch(L, "gemv_gate_up", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.gate_up), g); });
       if (e != cudaSuccess) return e;
     }
@@ -939,8 +960,8 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       g.T = T; g.K = I; g.N = hid; g.w = W.down.w; g.scale = W.down.scale; g.bias = W.down.bias;
       g.group = c.group_size; g.prologue = PRO_X; g.x = B.m; g.epilogue = EPI_RESIDUAL; g.out = hres; g.ldo = hid;
       g.sumsq_out = slot(2 * l + 2); g.err = B.err;
-      if (pf_on && l + 1 < NL) { g.pf = h->layers[l + 1].qkv.w; g.pf_bytes = lin_bytes(h->layers[l + 1].qkv, qkv_rows, hid); }
-      g.stages = gemv2_plan(dt, wfmt_of(W.down), T, I, c.group_size, false, &g.nwarps);
+      if (pf_mode && l + 1 < NL) { g.pf = h->layers[l + 1].qkv.w; g.pf_bytes = lin_bytes(h->layers[l + 1].qkv, qkv_rows, hid); }
+      g.stages = gemv2_plan(dt, wfmt_of(W.down), T, I, c.group_size, false, &g.nwarps, h->coresident);
       e = launch(L, "gemv_down", [&] { return launch_gemv2(L.ctx, dt, wfmt_of(W.down), g); });
       if (e != cudaSuccess) return e;
     }

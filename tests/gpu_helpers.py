@@ -18,7 +18,9 @@ Tolerances.
   row's RMS, a non-power-of-two scale, which can turn two ulps of the sum into
   up to four of the output; the count of elements that need more than 2e-2 is
   reported.  In MoE layers, rows whose expert choice is a near-tie are left
-  out of the element comparison (near_tie_rows), counted, and capped.
+  out of the element comparison (near_tie_rows), counted, and capped at 30%
+  (the block itself is held to bit-exact indices on identical inputs by the
+  MoE block tests).
 * bf16, whole stacks: 2e-2, or TWIN_FACTOR x the drift between the oracle and
   its float32 twin (oracle.Qwen3OracleF32Acc: the same rounding points, float32
   arithmetic between them) on the same inputs, whichever is larger, capped at
@@ -271,7 +273,7 @@ class LayerGate:
                 note += f"{'; ' if note else ''}{ties} of {n_rows} rows with a near-tie expert choice left out"
             report(f"{self.cfg.name} layer {l} ({len(rs)} steps)", worst, tol, note)
             assert crit <= 1.0, f"layer {l}: max-abs/RMS {worst:.4f}, per-element criterion {crit:.3f} > 1"
-            assert ties <= 0.15 * n_rows, f"layer {l}: {ties} of {n_rows} rows are expert near-ties"
+            assert ties <= 0.3 * n_rows, f"layer {l}: {ties} of {n_rows} rows are expert near-ties"
 
     def close(self):
         for one, st in self.stacks.values():

@@ -199,18 +199,24 @@ def test_int8_weights_cuda_cores(cuda_ok, n_prefill):
     p.check()
 
 
-@pytest.mark.parametrize("graphs,pdl", [(0, 0), (0, 1), (1, 0)])
-def test_launch_options_do_not_change_results(cuda_ok, graphs, pdl):
-    """CUDA-graph replay and programmatic dependent launch change scheduling only:
-    results are bitwise equal to the default (graphs + PDL)."""
+@pytest.mark.parametrize("opts", [{"CUDA_GRAPHS": 0, "PDL": 0}, {"CUDA_GRAPHS": 0}, {"PDL": 0},
+                                  {"L2_PREFETCH": 1}, {"L2_PREFETCH": 2}, {"GEMV_CORESIDENT": 1}],
+                         ids=["direct", "direct_pdl", "graph_no_pdl", "prefetch1", "prefetch2", "coresident"])
+def test_launch_options_do_not_change_results(cuda_ok, opts):
+    """CUDA-graph replay, programmatic dependent launch, L2 prefetch and the
+    GEMV block size change scheduling only: results are bitwise equal to the
+    default; options switched on a live handle take effect (its captured
+    graphs are dropped)."""
     cfg = SMALL_D128
     wd = to_device(I.make_weights(cfg, seed=2000))
     xs = [I.make_rows(cfg, n, seed=2001 + i).cuda() for i, n in enumerate([9, 1, 1, 2, 1])]
     outs = []
-    for opt in [(1, 1), (graphs, pdl)]:
+    for o in [{}, opts]:
         s = Q.Qwen3Stack(cfg, wd)
-        Q.qwen3_set_option(s.h, Q.QWEN3_OPT_CUDA_GRAPHS, opt[0])
-        Q.qwen3_set_option(s.h, Q.QWEN3_OPT_PDL, opt[1])
+        s.forward(xs[0])                       # a graph-free prefill, then switch on the live handle
+        Q.qwen3_reset(s.h, 0)
+        for k, v in o.items():
+            Q.qwen3_set_option(s.h, getattr(Q, "QWEN3_OPT_" + k), v)
         outs.append([s.forward(x).clone() for x in xs])
         s.close()
     for a, b in zip(*outs):
