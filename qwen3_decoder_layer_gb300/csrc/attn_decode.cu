@@ -29,6 +29,8 @@
 // model dtype.
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "kernels.h"
@@ -287,6 +289,228 @@ __device__ __forceinline__ void warp_scores_softmax(const Dt* Kt, const float* q
   }
 }
 
+// A warp's online-softmax state over its keys and its partial (m, l, o) for
+// the merge.  Two forms with the same interface:
+//  * WarpAttnSimt: CUDA cores (every dtype); scores as above, then P.V with
+//    lane l holding head elements l*D/32 .. +D/32 of every query.
+//  * WarpAttnMma: bf16 with 4 or 8 query vectors (GQA groups of 4-8 heads, or
+//    several rows of a sequence), where the per-key work is a small dense
+//    product: S^T[16 keys x 8 queries] = K Q^T and O^T[D x 8] += V^T P^T on
+//    warp-level tensor-core MMAs (mma.sync m16n8k16, bf16 in, fp32
+//    accumulate; bf16 products are exact in fp32).  P enters the MMA as three
+//    bf16 parts hi + mid + lo, which hold all 24 bits of the fp32
+//    probability, so P.V keeps the accuracy of the CUDA-core form.  Lane L holds
+//    queries 2(L%4), 2(L%4)+1: its scores for keys L/4 and L/4+8, and its
+//    output columns t*16 + L/4 (+8) of every 16-dim tile t.
+template <typename Dt, int D, int NQ, int KW>
+struct WarpAttnSimt {
+  static constexpr int DPL = D / 32;
+  float m[NQ], l[NQ], o[NQ][DPL];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      m[i] = -CUDART_INF_F;
+      l[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+    }
+  }
+  __device__ __forceinline__ void load_q(const float*, int) {}
+  __device__ __forceinline__ void attend(Dt* Kt, Dt* Vt, const float* qs, float* ps, int nk, int nq, int kb,
+                                         int pos0, int G, float scale) {
+    const int lane = threadIdx.x & 31;
+    warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, pos0, G, scale, m, l, o);
+#pragma unroll 4
+    for (int u = 0; u < nk; ++u) {
+      float v[DPL];
+      load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        const float p = ps[i * KW + u];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(p, v[e], o[i][e]);
+      }
+    }
+  }
+  // partial of this warp -> mine[i * pitch + d] (o), [D] (m), [D + 1] (l)
+  __device__ __forceinline__ void store(float* mine, int pitch) const {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      store_lane_vec<DPL>(mine + i * pitch + lane * DPL, o[i]);
+      if (lane == 0) { mine[i * pitch + D] = m[i]; mine[i * pitch + D + 1] = l[i]; }
+    }
+  }
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+// two fp32 values that are bf16 values -> one bf16x2 word (first in the low half)
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
+
+template <int D, int NQ>
+struct WarpAttnMma {
+  static constexpr int NT = D / 16;  // 16-dim tiles (k-steps of the scores, m-tiles of the output)
+  float m[2], l[2];
+  float o[NT][4];
+  uint32_t qf[NT][2];                // B fragments of Q^T, per 16-dim k-step
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) { m[j] = -CUDART_INF_F; l[j] = 0.f; }
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[t][e] = 0.f;
+  }
+  // Q^T fragments from the staged queries (fp32 values of bf16 numbers: exact)
+  __device__ __forceinline__ void load_q(const float* qs, int nq) {
+    const int lane = threadIdx.x & 31, n = lane >> 2, c = (lane & 3) * 2;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (n < nq) {
+        const float* q = qs + n * D + t * 16 + c;
+        qf[t][0] = pack_bf16x2(q[0], q[1]);
+        qf[t][1] = pack_bf16x2(q[8], q[9]);
+      } else {
+        qf[t][0] = qf[t][1] = 0u;
+      }
+    }
+  }
+  __device__ __forceinline__ void attend(__nv_bfloat16* Kt, __nv_bfloat16* Vt, const float*, float*, int nk, int nq,
+                                         int kb, int pos0, int G, float scale) {
+    const int lane = threadIdx.x & 31, r0 = lane >> 2, q0 = (lane & 3) * 2;
+    // value rows past this warp's keys hold whatever the stage held: zero them
+    // (their probabilities are 0, but 0 * a non-finite value is not)
+    if (nk < 16) {
+      for (int c = lane; c < (16 - nk) * (D / 8); c += 32)
+        reinterpret_cast<uint4*>(Vt + (size_t)(nk + c / (D / 8)) * D)[c % (D / 8)] = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+    }
+    // S^T = K Q^T: rows = keys r0, r0 + 8; columns = queries q0, q0 + 1
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;  // ldmatrix row of this lane
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      uint32_t a[4];
+      ldsm_x4(a, Kt + (size_t)mrow * D + t * 16 + mcol);
+      mma_bf16_16816(s, a, qf[t][0], qf[t][1]);
+    }
+    float mx[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int q = q0 + j;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int k = r0 + 8 * h;
+        const bool ok = k < nk && q < nq && kb + k <= pos0 + q / G;
+        s[2 * h + j] = ok ? s[2 * h + j] * scale : -CUDART_INF_F;
+      }
+      float v = fmaxf(s[j], s[2 + j]);
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      mx[j] = v;
+    }
+    // probabilities (fp32)
+    float p[4], alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float m_new = fmaxf(m[j], mx[j]);
+      alpha[j] = (m[j] == -CUDART_INF_F) ? 0.f : expf(m[j] - m_new);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        p[2 * h + j] = (s[2 * h + j] == -CUDART_INF_F) ? 0.f : expf(s[2 * h + j] - m_new);
+      float sum = p[j] + p[2 + j];
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      if (m_new != -CUDART_INF_F) {
+        l[j] = fmaf(l[j], alpha[j], sum);
+        m[j] = m_new;
+      } else {
+        alpha[j] = 1.f;
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      o[t][0] *= alpha[0]; o[t][2] *= alpha[0];
+      o[t][1] *= alpha[1]; o[t][3] *= alpha[1];
+    }
+    // P^T as the B operand: lane L needs P[query L/4][keys 2(L%4), +1, +8, +9],
+    // held by lanes 8(L%4) + (L/4)/2 (keys 2(L%4), +8) and that + 4 (the odd keys)
+    const int src = (lane & 3) * 8 + (lane >> 3);
+    const int par = (lane >> 2) & 1;  // which of the source's two queries
+    float g[2][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      g[0][e] = __shfl_sync(0xffffffffu, p[e], src);
+      g[1][e] = __shfl_sync(0xffffffffu, p[e], src + 4);
+    }
+    const float pk0 = par ? g[0][1] : g[0][0], pk1 = par ? g[1][1] : g[1][0];
+    const float pk8 = par ? g[0][3] : g[0][2], pk9 = par ? g[1][3] : g[1][2];
+    // p = hi + mid + lo exactly: each part the top 8 significant bits of what
+    // is left (the differences are exact in fp32)
+    auto top = [](float v) { return __uint_as_float(__float_as_uint(v) & 0xffff0000u); };
+    const float h0 = top(pk0), h1 = top(pk1), h8 = top(pk8), h9 = top(pk9);
+    const float m0 = top(pk0 - h0), m1 = top(pk1 - h1), m8 = top(pk8 - h8), m9 = top(pk9 - h9);
+    const uint32_t bh0 = pack_bf16x2(h0, h1), bh1 = pack_bf16x2(h8, h9);
+    const uint32_t bm0 = pack_bf16x2(m0, m1), bm1 = pack_bf16x2(m8, m9);
+    const uint32_t bl0 = pack_bf16x2(pk0 - h0 - m0, pk1 - h1 - m1);
+    const uint32_t bl1 = pack_bf16x2(pk8 - h8 - m8, pk9 - h9 - m9);
+    // O^T += V^T P^T: A = V^T tile (16 dims x 16 keys) by a transposing ldmatrix
+    const int vrow = (lane & 7) + (lane >> 4) * 8, vcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      uint32_t a[4];
+      ldsm_x4_t(a, Vt + (size_t)vrow * D + t * 16 + vcol);
+      mma_bf16_16816(o[t], a, bh0, bh1);
+      mma_bf16_16816(o[t], a, bm0, bm1);
+      mma_bf16_16816(o[t], a, bl0, bl1);
+    }
+  }
+  __device__ __forceinline__ void store(float* mine, int pitch) const {
+    const int lane = threadIdx.x & 31, r0 = lane >> 2, q0 = (lane & 3) * 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int q = q0 + j;
+      if (q >= NQ) continue;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        mine[q * pitch + t * 16 + r0] = o[t][j];
+        mine[q * pitch + t * 16 + r0 + 8] = o[t][2 + j];
+      }
+      if (r0 == 0) { mine[q * pitch + D] = m[j]; mine[q * pitch + D + 1] = l[j]; }
+    }
+  }
+};
+
+// The warp state a kernel instance uses.
+template <typename Dt, int D, int NQ, int KW>
+struct WarpAttnOf {
+  using type = WarpAttnSimt<Dt, D, NQ, KW>;
+};
+template <int D, int NQ>
+struct WarpAttnOf<__nv_bfloat16, D, NQ, 16> {
+  using type = typename std::conditional<(NQ >= 4), WarpAttnMma<D, NQ>, WarpAttnSimt<__nv_bfloat16, D, NQ, 16>>::type;
+};
+
 // The last block to finish a (query block, kv head) combines its nc chunk
 // partials: M = max m_c, out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c,
 // rounded once to the model dtype.  Every partial is first loaded into
@@ -451,16 +675,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   // (with at most one item per block, block x takes item x)
   const int it_lo = n_items <= gx ? (int)blockIdx.x : lo_of(blockIdx.x);
   const int it_hi = n_items <= gx ? min((int)blockIdx.x + 1, n_items) : lo_of(blockIdx.x + 1);
-  float m_w[NQ], l_w[NQ], o_w[NQ][DPL];
-  auto reset_state = [&]() {
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      m_w[i] = -CUDART_INF_F;
-      l_w[i] = 0.f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
-    }
-  };
+  typename WarpAttnOf<Dt, D, NQ, KW>::type ws;  // this warp's online-softmax state
+  auto reset_state = [&]() { ws.reset(); };
   reset_state();
   __shared__ int s_run[2];  // this block's run index within the query block, number of runs
 
@@ -469,12 +685,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   auto flush = [&](int b, bool last) {
     const AttnQBlock qb = a.qblocks[b];
     const int nq = qb.nrows * G;
-    float* mine = wp + (size_t)warp * NQ * WP;
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      store_lane_vec<DPL>(mine + i * WP + lane * DPL, o_w[i]);
-      if (lane == 0) { mine[i * WP + D] = m_w[i]; mine[i * WP + D + 1] = l_w[i]; }
-    }
+    ws.store(wp + (size_t)warp * NQ * WP, WP);
     if (tid == 0) {  // runs of b: blocks with a non-empty range meeting b's items [part_base, part_base + n_chunks)
       const int s0 = qb.part_base, s1 = qb.part_base + qb.n_chunks;
       if (n_items <= gx) {  // one item per block: the run index is the item's chunk
@@ -557,6 +768,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
         store_lane_vec<DPL>(qs + i * D + lane * DPL, x);
       }
       csync();
+      ws.load_q(qs, nq);
     }
 
     // ---- this warp's keys of the item, folded into its running state
@@ -611,22 +823,12 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           }
         }
         __syncwarp();
-        warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale, m_w, l_w, o_w);
-        // P.V: lane holds head elements lane*DPL .. +DPL
-#pragma unroll 4
-        for (int u = 0; u < nk; ++u) {
-          float v[DPL];
-          load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) {
-            const float p = ps[i * KW + u];
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o_w[i][e] = fmaf(p, v[e], o_w[i][e]);
-          }
-        }
+        ws.attend(Kt, Vt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale);
       }
-      // this warp is done with its part of the stage
+      // this warp is done with its part of the stage (its smem writes ordered
+      // before the producer's next copy into it)
       __syncwarp();
+      fence_proxy_async();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     g += ik.nsub;
@@ -735,14 +937,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
     csync();
 
     // ---- this warp's keys, end to end
-    float m_w[NQ], l_w[NQ], o_w[NQ][DPL];
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      m_w[i] = -CUDART_INF_F;
-      l_w[i] = 0.f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
-    }
+    typename WarpAttnOf<Dt, D, NQ, KW>::type ws;
+    ws.reset();
+    ws.load_q(qs, nq);
     if (wsub < ik.nsub) {
       const int s = (g + wsub) % LY::STAGES;
       const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
@@ -779,31 +976,16 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
           }
         }
         __syncwarp();
-        warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale, m_w, l_w, o_w);
-        // P.V: lane holds head elements lane*DPL .. +DPL
-#pragma unroll 4
-        for (int u = 0; u < nk; ++u) {
-          float v[DPL];
-          load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) {
-            const float p = ps[i * KW + u];
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o_w[i][e] = fmaf(p, v[e], o_w[i][e]);
-          }
-        }
+        ws.attend(Kt, Vt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale);
       }
-      // this warp is done with its part of the stage
+      // this warp is done with its part of the stage (its smem writes ordered
+      // before the producer's next copy into it)
       __syncwarp();
+      fence_proxy_async();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     // warp partial -> shared memory
-    float* mine = wp + (size_t)warp * NQ * WP;
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      store_lane_vec<DPL>(mine + i * WP + lane * DPL, o_w[i]);
-      if (lane == 0) { mine[i * WP + D] = m_w[i]; mine[i * WP + D + 1] = l_w[i]; }
-    }
+    ws.store(wp + (size_t)warp * NQ * WP, WP);
     g += ik.nsub;
     csync();
     if (s_fail) break;
@@ -943,14 +1125,9 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
       store_lane_vec<DPL>(qs + i * D + lane * DPL, x);
     }
     csync();
-    float m_w[NQ], l_w[NQ], o_w[NQ][DPL];
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      m_w[i] = -CUDART_INF_F;
-      l_w[i] = 0.f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o_w[i][e] = 0.f;
-    }
+    typename WarpAttnOf<Dt, D, NQ, KW>::type ws;
+    ws.reset();
+    ws.load_q(qs, nq);
     for (int sub = wsub; sub < nsub; sub += AD_SUBS) {
       const int key0 = k_lo + sub * CK;
       const int nk = min(KW, k_hi - key0 - wk0);
@@ -987,26 +1164,10 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
         }
       }
       __syncwarp();
-      warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale, m_w, l_w, o_w);
-#pragma unroll 4
-      for (int u = 0; u < nk; ++u) {
-        float v[DPL];
-        load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-          const float p = ps[i * KW + u];
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) o_w[i][e] = fmaf(p, v[e], o_w[i][e]);
-        }
-      }
+      ws.attend(Kt, Vt, qs, ps, nk, nq, kb, qb.pos0, G, a.scale);
     }
     // warp partials -> the CTA's partial cp[i] = (sum_w f_w o_w, M, sum_w f_w l_w)
-    float* mine = wp + (size_t)warp * NQ * WP;
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      store_lane_vec<DPL>(mine + i * WP + lane * DPL, o_w[i]);
-      if (lane == 0) { mine[i * WP + D] = m_w[i]; mine[i * WP + D + 1] = l_w[i]; }
-    }
+    ws.store(wp + (size_t)warp * NQ * WP, WP);
     csync();
     if (warp < NQ) {
       const int i = warp;
