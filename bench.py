@@ -17,6 +17,7 @@ speculative verify windows (32 sequences x 4 rows).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
     python bench.py --workloads decode            # the headline line only
+    python bench.py --layers 2 ...                # a reduced case for profiler captures
 
 Multi-GPU runs are independent replicas (one stack per GPU, no collective on
 the data path); the value is all ranks' tokens over the slowest rank's time.
@@ -481,7 +482,7 @@ def prefill_workload(C, cfg, T, K, W, chunks=None):
 # ---------------------------------------------------------------- the workloads
 def wl_decode(C, K, W, cpu=True):
     I = C.I
-    cfg = I.DENSE_1P7B_DECODE
+    cfg = _sized(I.DENSE_1P7B_DECODE)
     assert CTX0 + W + K <= cfg.capacity, "steps + warmup exceed the cache capacity"
     res, stack, _ = decode_workload(C, cfg, [CTX0], K, W)
     stack.close()
@@ -494,7 +495,7 @@ def wl_decode(C, K, W, cpu=True):
 
 def wl_prefill(C, K, W, cpu=True):
     I = C.I
-    cfg = I.DENSE_1P7B_PREFILL
+    cfg = _sized(I.DENSE_1P7B_PREFILL)
     T = 2048
     res, stack, prof = prefill_workload(C, cfg, T, K, W, chunks=4)
     stack.close()
@@ -523,7 +524,7 @@ def wl_prefill(C, K, W, cpu=True):
 
 def wl_moe_decode(C, K, W, cpu=True):
     I = C.I
-    cfg = I.MOE_A3B_4LAYER
+    cfg = _sized(I.MOE_A3B_4LAYER)
     res, stack, _ = decode_workload(C, cfg, [2048], K, W)
     stack.close()
     res["config"] = {"workload": "Qwen3-MoE-shaped decode, bf16, 4 layers, 128 experts top-8, batch 1, "
@@ -535,7 +536,7 @@ def wl_moe_decode(C, K, W, cpu=True):
 
 def wl_moe_prefill(C, K, W, cpu=True):
     I = C.I
-    cfg = I.MOE_A3B_4LAYER
+    cfg = _sized(I.MOE_A3B_4LAYER)
     T = 1024
     res, stack, prof = prefill_workload(C, cfg, T, K, W)
     stack.close()
@@ -561,7 +562,7 @@ def wl_moe_prefill(C, K, W, cpu=True):
 
 def wl_batched_int8(C, K, W, cpu=True):
     I = C.I
-    cfg = I.DENSE_1P7B_INT8_B32
+    cfg = _sized(I.DENSE_1P7B_INT8_B32)
     ctxs = I.batch_context_lengths(32, 1024, 16384, seed=3600)
     assert max(ctxs) + W + K <= cfg.capacity
     res, stack, _ = decode_workload(C, cfg, ctxs, K, W)
@@ -578,7 +579,8 @@ def wl_batched_int8(C, K, W, cpu=True):
 def wl_verify(C, K, W, cpu=True):
     """Speculative verify windows: depth + 1 = 4 rows for each of 32 sequences."""
     I = C.I
-    cfg = I.with_sizes(I.DENSE_1P7B_DECODE, name="dense_1p7b_decode", max_seqs=32, capacity=4096 + 4 * (W + K) + 8)
+    cfg = _sized(I.with_sizes(I.DENSE_1P7B_DECODE, name="dense_1p7b_decode", max_seqs=32,
+                              capacity=4096 + 4 * (W + K) + 8))
     ctxs = I.batch_context_lengths(32, 1024, 4096, seed=3800)
     res, stack, _ = decode_workload(C, cfg, ctxs, K, W, rows_per_seq=4)
     stack.close()
@@ -596,6 +598,14 @@ WL_FN = {"decode": wl_decode, "prefill": wl_prefill, "moe_decode": wl_moe_decode
 WL_STEPS = {"prefill": 10, "moe_prefill": 10, "moe_decode": 32, "batched_int8": 16, "verify": 16}
 
 
+LAYERS = 0  # --layers: a reduced profiling case (fewer layers); 0 = the workloads as stated
+
+
+def _sized(cfg):
+    from qwen3_decoder_layer_gb300 import inputs as I
+    return I.with_sizes(cfg, num_layers=LAYERS) if LAYERS else cfg
+
+
 def run_gpu(args):
     import torch
     from qwen3_decoder_layer_gb300 import binding as Q
@@ -610,9 +620,11 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     B.build()
     Q.lib()
+    global LAYERS
+    LAYERS = args.layers
     C = Ctx()
     K, W = args.steps, args.warmup
-    cfg = C.I.DENSE_1P7B_DECODE
+    cfg = _sized(C.I.DENSE_1P7B_DECODE)
     assert CTX0 + W + K <= cfg.capacity, "steps + warmup exceed the cache capacity"
 
     # ---- headline: batch-1 decode, replicated on every rank
@@ -656,6 +668,8 @@ def run_gpu(args):
         "gpu_launches": res["gpu_launches"],
         "clocks": clocks.summary(),
     }
+    if LAYERS:
+        line["reduced"] = f"profiling case: {LAYERS} layers per stack, not a measurement of the workloads"
     gc.collect()
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
@@ -697,6 +711,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: every stack with this many layers (the line is marked reduced)")
     ap.add_argument("--workloads", default=",".join(WORKLOADS),
                     help="comma-separated subset of " + ",".join(WORKLOADS) + " (decode is always the headline)")
     args = ap.parse_args()
