@@ -331,7 +331,27 @@ def kernels_table(prof):
             for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])}
 
 
-def hbm_roofline(C, prof, cfg, rows, ctx_sum, step_bytes, step_ms):
+def _sha(path):
+    import hashlib
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_of(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt),
+    if the kernel's source is unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 5 and not line.startswith("#") and f[0] == f"{workload}:{kernel}":
+            src = os.path.join(ROOT, "qwen3_decoder_layer_gb300", "csrc", f[3])
+            if os.path.exists(src) and _sha(src) == f[4]:
+                return float(f[1])
+    return None
+
+
+def hbm_roofline(C, prof, cfg, rows, ctx_sum, step_bytes, step_ms, workload=None):
     """Roofline of the dominant kernel with known algorithmic bytes, and of the step."""
     total = sum(v[1] for v in prof.values()) or 1.0
     cands = [(k, v) for k, v in prof.items() if kernel_bytes(cfg, k, rows, ctx_sum)]
@@ -340,7 +360,8 @@ def hbm_roofline(C, prof, cfg, rows, ctx_sum, step_bytes, step_ms):
     avg = ms / n
     ach = b / (avg * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": k, "achieved": ach, "peak": C.hbm, "unit": "GB/s", "frac": ach / C.hbm,
-            "traffic": None, "algorithmic_bytes_per_launch": b, "avg_launch_ms": avg,
+            "traffic": traffic_of(workload, k) if workload else None,
+            "algorithmic_bytes_per_launch": b, "avg_launch_ms": avg,
             "kernel_share": ms / total, "timing": SERIAL, "peak_source": f"{C.peak_src} hbm_gbs (burst copy)",
             "step": {"bytes": step_bytes, "achieved_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
                      "frac": step_bytes / (step_ms * 1e-3) / 1e9 / C.hbm}}
@@ -363,6 +384,7 @@ def fill_cache_fast(C, stack, cfg, seq, n, gen):
 
 
 def decode_workload(C, cfg, ctxs, K, W, rows_per_seq=1, name="decode"):
+    """(name: the workload's key in profiles/traffic.txt)"""
     """Steps of `rows_per_seq` rows for each sequence (contexts ctxs, one
     sequence each) through the whole stack: device-timed, end to end, and
     per kernel.  Returns (result dict, stack, timing extras)."""
@@ -422,7 +444,7 @@ def decode_workload(C, cfg, ctxs, K, W, rows_per_seq=1, name="decode"):
            "kernels": kernels_table(prof), "kernel_timing": SERIAL}
     ctx_avg_sum = sum(n + (K - 1) / 2.0 * rows_per_seq + (rows_per_seq + 1) / 2.0 for n in ctxs)
     step_bytes = step_weight_bytes(cfg, R) + cfg.num_layers * kv_bytes_per_pos(cfg) * ctx_avg_sum * 1.0
-    res["roofline"] = hbm_roofline(C, prof, cfg, R, ctx_avg_sum, step_bytes, ms / K)
+    res["roofline"] = hbm_roofline(C, prof, cfg, R, ctx_avg_sum, step_bytes, ms / K, workload=name)
     res["roofline"]["step"]["note"] = "weights once per step + every sequence's cached K/V once per layer"
     return res, stack, (step, reset)
 
@@ -525,7 +547,7 @@ def wl_prefill(C, K, W, cpu=True):
 def wl_moe_decode(C, K, W, cpu=True):
     I = C.I
     cfg = _sized(I.MOE_A3B_4LAYER)
-    res, stack, _ = decode_workload(C, cfg, [2048], K, W)
+    res, stack, _ = decode_workload(C, cfg, [2048], K, W, name="moe_decode")
     stack.close()
     res["config"] = {"workload": "Qwen3-MoE-shaped decode, bf16, 4 layers, 128 experts top-8, batch 1, "
                                  "context 2048..2048+K-1", "layers": 4}
@@ -565,7 +587,7 @@ def wl_batched_int8(C, K, W, cpu=True):
     cfg = _sized(I.DENSE_1P7B_INT8_B32)
     ctxs = I.batch_context_lengths(32, 1024, 16384, seed=3600)
     assert max(ctxs) + W + K <= cfg.capacity
-    res, stack, _ = decode_workload(C, cfg, ctxs, K, W)
+    res, stack, _ = decode_workload(C, cfg, ctxs, K, W, name="batched_int8")
     stack.close()
     res["config"] = {"workload": "Qwen3-1.7B-shaped batched decode, int8 affine group-64 weights, bf16 "
                                  "activations and KV, 32 sequences at contexts uniform in [1024, 16384]",
@@ -582,7 +604,7 @@ def wl_verify(C, K, W, cpu=True):
     cfg = _sized(I.with_sizes(I.DENSE_1P7B_DECODE, name="dense_1p7b_decode", max_seqs=32,
                               capacity=4096 + 4 * (W + K) + 8))
     ctxs = I.batch_context_lengths(32, 1024, 4096, seed=3800)
-    res, stack, _ = decode_workload(C, cfg, ctxs, K, W, rows_per_seq=4)
+    res, stack, _ = decode_workload(C, cfg, ctxs, K, W, rows_per_seq=4, name="verify")
     stack.close()
     res["config"] = {"workload": "speculative verify windows on the Qwen3-1.7B-shaped stack, bf16: 32 sequences "
                                  "x 4 rows (depth 3) per call at contexts uniform in [1024, 4096]",
