@@ -296,6 +296,8 @@ __device__ __forceinline__ float rms_apply2(float h, F2 rs, float g) {
   return rd<Dt>(mul_round<Dt>(h, rs) * g);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// g * sigmoid(g) with the fast division (the result is rounded to the model
+// dtype by every caller; the IEEE division's slow path is avoided for 0).
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + expf(-g)); }
 
 }  // namespace q3

@@ -12,7 +12,11 @@
 // from the TMA warp to the MMA warp (full) and back (empty, signalled by
 // tcgen05.commit).  Four epilogue warps read the accumulator with
 // tcgen05.ld (warp q owns TMEM lanes 32q..32q+31, i.e. rows of the tile),
-// apply the fused epilogue (rounding / residual add / SiLU * up) and store.
+// apply the fused epilogue (rounding / residual add / SiLU * up) and store:
+// each warp writes 64 output columns of its 32 rows into a swizzled
+// shared-memory slab (lane = row) and reads it back transposed (8 lanes per
+// row), so that every global load of the residual and every store covers
+// whole 128-byte lines.
 // For SiLU * up the B tile is two 128-row boxes: gate rows n0.. and up rows
 // N + n0.., so TMEM columns 0..127 hold g and 128..255 hold u of the same
 // output columns.
@@ -31,7 +35,9 @@ constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column accumulators
 constexpr size_t TC_A_BYTES = (size_t)TC_BM * TC_BK * 2;   // 16 KB
 constexpr size_t TC_B_BYTES = (size_t)TC_BN * TC_BK * 2;   // 32 KB
 constexpr size_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
-constexpr size_t TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 1024 /* align */ + 256 /* barriers */;
+// epilogue staging: per epilogue warp 32 rows x 64 output columns (128 B per row)
+constexpr size_t TC_STG_WARP = 32 * 128;
+constexpr size_t TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 256 /* barriers */ + 4 * TC_STG_WARP + 1024 /* align */;
 
 using namespace tc;
 
@@ -154,60 +160,76 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {  // epilogue: warp q reads TMEM lanes 32q .. 32q + 31 = tile rows
+    // staging slab of this warp: row r's 16-byte chunk j sits at chunk j ^ (r & 7)
+    uint4* stg = reinterpret_cast<uint4*>(smem + TC_STAGES * TC_STAGE_BYTES + 256 + warp * TC_STG_WARP);
     int i = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int b = i & 1, use = i >> 1;
       const TileInfo ti = tile_of<GROUPED>(a, t, tiles_m, ncol);
-      const int n0 = ti.n0;
       int okl = 1;  // lane 0 waits for the accumulator; the other lanes wait at the warp barrier
       if (lane == 0) okl = mbar_wait(&acc_full[b], (uint32_t)(use & 1), a.err, 5);
       __syncwarp();
       if (!__shfl_sync(0xffffffffu, okl, 0)) break;
       fence_after();
-      const int row = ti.m0 + warp * 32 + lane;
-      const bool live = row < ti.mlim;
-      const size_t orow = !live ? 0 : (GROUPED && a.c_rows) ? (size_t)a.c_rows[row] : (size_t)row;
       const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * TC_BN);
-      if (EPI == EPI_SWIGLU) {
-        for (int c = 0; c < TC_BN / 2; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(tl + c, g);
-          tmem_ld32(tl + TC_BN / 2 + c, u);
-          if (live) {
-            float o[32];
+      // the 8 rows this lane stores per 64-column slab: r = 4k + lane / 8, chunk lane % 8
+      const int jr = lane & 7, r0 = lane >> 3;
+      const int rbase = ti.m0 + warp * 32;
+      for (int c = 0; c < ncol; c += 64) {
+        // 1. this lane's row: 64 columns from tensor memory, rounded to bf16, into the slab
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float o[32];
+          if (EPI == EPI_SWIGLU) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tl + c + 32 * h, g);
+            tmem_ld32(tl + TC_BN / 2 + c + 32 * h, u);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const float gv = rd<bf16>(__uint_as_float(g[e])), uv = rd<bf16>(__uint_as_float(u[e]));
               o[e] = rd<bf16>(silu_f(gv)) * uv;
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(a.out) + orow * a.ldo + n0 + c);
+          } else {
+            uint32_t r[32];
+            tmem_ld32(tl + c + 32 * h, r);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = Vec16<bf16>::pack(o + 8 * v);
+            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]);
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) stg[lane * 8 + ((4 * h + v) ^ (lane & 7))] = Vec16<bf16>::pack(o + 8 * v);
+        }
+        __syncwarp();
+        // 2. transposed: 8 lanes per row, whole 128-byte lines to global memory
+        uint4 x[8];
+        size_t orow[8];
+        bool live[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = 4 * k + r0, row = rbase + r;
+          live[k] = row < ti.mlim;
+          orow[k] = !live[k] ? 0 : (GROUPED && a.c_rows) ? (size_t)a.c_rows[row] : (size_t)row;
+          x[k] = stg[r * 8 + (jr ^ (r & 7))];
+        }
+        bf16* base = static_cast<bf16*>(a.out) + ti.n0 + c + 8 * jr;
+        if (EPI == EPI_RESIDUAL) {
+          uint4 hres[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (live[k]) hres[k] = *reinterpret_cast<const uint4*>(base + orow[k] * a.ldo);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float hv[8], av[8];
+            Vec16<bf16>::unpack(hres[k], hv);
+            Vec16<bf16>::unpack(x[k], av);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hv[e] += av[e];
+            x[k] = Vec16<bf16>::pack(hv);
           }
         }
-      } else {
-        for (int c = 0; c < TC_BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(tl + c, r);
-          if (live) {
-            bf16* p = static_cast<bf16*>(a.out) + orow * a.ldo + n0 + c;
-            float o[32];
-            if (EPI == EPI_RESIDUAL) {
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                float hv[8];
-                Vec16<bf16>::unpack(reinterpret_cast<const uint4*>(p)[v], hv);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[8 * v + e] = hv[e] + rd<bf16>(__uint_as_float(r[8 * v + e]));
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]);
-            }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(p)[v] = Vec16<bf16>::pack(o + 8 * v);
-          }
-        }
+        for (int k = 0; k < 8; ++k)
+          if (live[k]) *reinterpret_cast<uint4*>(base + orow[k] * a.ldo) = x[k];
+        __syncwarp();  // the slab is rewritten by the next 64 columns
       }
       // accumulator b may be overwritten by the tile after next
       fence_before();
