@@ -102,7 +102,9 @@ typedef struct {
   const void* bias;
 } qwen3_linear;
 
-/* Borrowed device pointers of one decoder layer. */
+/* Borrowed device pointers of one decoder layer.  The norm gains, the router
+ * and every linear's w must be 16-byte aligned (a misaligned or missing one
+ * makes qwen3_create return QWEN3_E_ARG). */
 typedef struct {
   const void* in_norm;       /* dt [hidden]  input_layernorm gain */
   const void* post_norm;     /* dt [hidden]  post_attention_layernorm gain */

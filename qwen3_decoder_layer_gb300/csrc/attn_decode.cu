@@ -1190,26 +1190,54 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
   // every CTA's partial is in its shared memory
   __syncwarp();
   cluster_sync_all();
-  if (warp < AD_CWARPS && !s_fail) {
-    // this CTA's slice of the nq x D outputs, combined over the cluster
+  {
+    // This CTA's slice of the nq x D outputs, combined over the cluster with
+    // one round of independent distributed loads: every CTA's (m, l) of each
+    // query and one (output, CTA) value per thread; then the maxima and sums,
+    // then the weighted sums in CTA order.  Scratch: this CTA's warp
+    // partials, which nobody reads any more.
+    float* cm = wp;                        // [16][NQ] m of CTA c
+    float* cl = cm + 16 * NQ;              // [16][NQ] l of CTA c
+    float* sM = cl + 16 * NQ;              // [NQ] max over CTAs, then [NQ] the sum
+    float* red = sM + 2 * NQ;              // [outputs of the slice][ncl]
+    const uint32_t cp_addr = smem_u32(cp);
     const int total = nq * D;
     const int share = (total + (int)ncl - 1) / (int)ncl;
-    const uint32_t cp_addr = smem_u32(cp);
-    for (int idx = (int)rank * share + tid; idx < min(total, ((int)rank + 1) * share); idx += AD_CTHREADS) {
-      const int i = idx / D, d = idx % D;
+    const int o0 = min(total, (int)rank * share), n_out = min(total, o0 + share) - o0;
+    for (int t = tid; t < (int)ncl * nq; t += AD_THREADS) {
+      const int c = t / nq, i = t % nq;
+      const uint32_t base = cluster_map(cp_addr + (uint32_t)(i * CP + D) * 4u, (uint32_t)c);
+      cm[c * NQ + i] = ld_cluster(base);
+      cl[c * NQ + i] = ld_cluster(base + 4u);
+    }
+    for (int t = tid; t < n_out * (int)ncl; t += AD_THREADS) {
+      const int c = t % (int)ncl, idx = o0 + t / (int)ncl;
+      red[t] = ld_cluster(cluster_map(cp_addr + (uint32_t)((idx / D) * CP + idx % D) * 4u, (uint32_t)c));
+    }
+    __syncthreads();
+    if (tid < nq) {
       float M = -CUDART_INF_F;
-      for (uint32_t c = 0; c < ncl; ++c)
-        M = fmaxf(M, ld_cluster(cluster_map(cp_addr + (uint32_t)(i * CP + D) * 4u, c)));
-      float L = 0.f, v = 0.f;
+      for (uint32_t c = 0; c < ncl; ++c) M = fmaxf(M, cm[c * NQ + tid]);
+      float L = 0.f;
       for (uint32_t c = 0; c < ncl; ++c) {
-        const uint32_t base = cluster_map(cp_addr + (uint32_t)(i * CP) * 4u, c);
-        const float m = ld_cluster(base + (uint32_t)D * 4u);
-        const float f = (m == -CUDART_INF_F) ? 0.f : expf(m - M);
-        L = fmaf(ld_cluster(base + (uint32_t)(D + 1) * 4u), f, L);
-        v = fmaf(ld_cluster(base + (uint32_t)d * 4u), f, v);
+        const float m = cm[c * NQ + tid];
+        L = fmaf(cl[c * NQ + tid], (m == -CUDART_INF_F) ? 0.f : expf(m - M), L);
       }
-      const int row = qb.row0 + i / G, head = j * G + i % G;
-      static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / L);
+      sM[tid] = M;
+      sM[NQ + tid] = L;
+    }
+    __syncthreads();
+    if (!s_fail) {
+      for (int t = tid; t < n_out; t += AD_THREADS) {
+        const int idx = o0 + t, i = idx / D, d = idx % D;
+        float v = 0.f;
+        for (uint32_t c = 0; c < ncl; ++c) {
+          const float m = cm[c * NQ + i];
+          v = fmaf(red[t * (int)ncl + (int)c], (m == -CUDART_INF_F) ? 0.f : expf(m - sM[i]), v);
+        }
+        const int row = qb.row0 + i / G, head = j * G + i % G;
+        static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / sM[NQ + i]);
+      }
     }
   }
   // no CTA leaves (freeing its shared memory) while another may still read it

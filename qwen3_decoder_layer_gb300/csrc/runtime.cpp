@@ -283,7 +283,8 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
       if (int8 && (!L.scale || !L.bias)) return false;
       return true;
     };
-    if (!w.in_norm || !w.post_norm || !w.q_norm || !w.k_norm || !aligned16(w.in_norm) || !aligned16(w.post_norm))
+    if (!w.in_norm || !w.post_norm || !w.q_norm || !w.k_norm || !aligned16(w.in_norm) || !aligned16(w.post_norm) ||
+        !aligned16(w.q_norm) || !aligned16(w.k_norm))
       s = bad("missing or misaligned norm gain", l);
     else if (!lin_ok(w.qkv) || !lin_ok(w.o)) s = bad("missing attention weights", l);
     else if (is_moe_layer(h, l)) {
