@@ -34,6 +34,7 @@
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace q3 {
 
@@ -69,13 +70,55 @@ template <typename Dt, int D, int NQ> struct ADLayout {
   static constexpr int MPITCH = AD_CWARPS + 2;                                    // weights of the warps, M, L
   static constexpr size_t OFF_MRG = OFF_WP + WP_FLOATS * 4;                       // [NQ][MPITCH] merge scratch
   static constexpr size_t OFF_BAR = (OFF_MRG + (size_t)NQ * MPITCH * 4 + 15) & ~size_t(15);
-  static constexpr size_t TOTAL = OFF_BAR + 2 * STAGES * 8 + 16;
+  static constexpr size_t TOTAL = OFF_BAR + 2 * STAGES * 8 + 16 + 1024;  // + slack to align the base to 1024
   // cluster variant: this CTA's merged partial [NQ][D + 2] (o, then m and l),
   // read by the other CTAs of the cluster
   static constexpr int CPITCH = D + 2;
   static constexpr size_t OFF_CP = (TOTAL + 15) & ~size_t(15);
-  static constexpr size_t TOTAL_CL = OFF_CP + (size_t)NQ * CPITCH * 4;
+  static constexpr size_t TOTAL_CL = OFF_CP + (size_t)NQ * CPITCH * 4 + 1024;
 };
+
+// A K or V tile in shared memory as the TMA writes it: each cached position's
+// row of D elements is R = D * sizeof(Dt) / 128 consecutive 128-byte lines
+// (the tile is one contiguous piece of the cache, one copy), and the 16-byte
+// chunk c of line L sits at chunk c ^ (L & 7) of that line (128-byte
+// swizzle: row-wise 16-byte accesses of a warp, e.g. ldmatrix over 8 rows,
+// spread over the bank groups).  p: the warp's first row (a multiple of 8
+// lines into the 1024-byte aligned tile).
+// (SWZ = false: the rows as they lie in the cache, unswizzled, filled by bulk
+// copies of the valid keys only; the CUDA-core warp form reads whole rows of
+// consecutive lanes and has no bank conflicts there.)
+template <typename Dt, int D, bool SWZ>
+struct KVT {
+  static constexpr int R = D * (int)sizeof(Dt) / 128;
+  uint8_t* p;
+  __device__ __forceinline__ uint8_t* chunk(int r, int c) const {
+    if (!SWZ) return p + r * (D * (int)sizeof(Dt)) + c * 16;
+    const int line = r * R + (c >> 3);
+    return p + line * 128 + (((c & 7) ^ (line & 7)) << 4);
+  }
+  // element e of row r; the elements after it up to the end of its 16-byte chunk follow it
+  __device__ __forceinline__ Dt* elem(int r, int e) const {
+    const int off = e * (int)sizeof(Dt);
+    return reinterpret_cast<Dt*>(chunk(r, off >> 4) + (off & 15));
+  }
+};
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+// The K and V tiles of CK cached positions from row `row` (kv head x capacity
+// + position) of sequence `seq`, one tensor load each, completing on `bar`.
+// The box is always whole: lines past the valid keys hold other cache
+// contents or zeros, and are masked.
+template <typename Dt, int D>
+__device__ __forceinline__ void load_kv_tiles(uint8_t* stage, const CUtensorMap* mk, const CUtensorMap* mv, int row,
+                                              int seq, uint64_t* bar) {
+  constexpr int CK = ADT<Dt>::CK, R = D * (int)sizeof(Dt) / 128;
+  constexpr uint32_t TILE = (uint32_t)CK * D * sizeof(Dt);
+  mbar_expect_tx(bar, 2 * TILE);
+  tc::tma_load_3d(stage, mk, 0, row * R, seq, bar);
+  tc::tma_load_3d(stage + TILE, mv, 0, row * R, seq, bar);
+}
 
 // Named barrier over the consumer warps only.
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(AD_CTHREADS) : "memory"); }
@@ -166,7 +209,7 @@ __device__ __forceinline__ float rs_sum(float (&v)[NS], int sub_l) {
 // in registers when there are at most two.  Eight queries: one butterfly per
 // (step, query), the registers being needed for the state.
 template <typename Dt, int D, int NQ, int KW>
-__device__ __forceinline__ void warp_scores_softmax(const Dt* Kt, const float* qs, float* ps, int nk, int nq, int kb,
+__device__ __forceinline__ void warp_scores_softmax(KVT<Dt, D, false> Kt, const float* qs, float* ps, int nk, int nq, int kb,
                                                     int pos0, int G, float scale, float (&m_w)[NQ], float (&l_w)[NQ],
                                                     float (&o_w)[NQ][D / 32]) {
   constexpr int EPV = 16 / sizeof(Dt);
@@ -194,7 +237,7 @@ __device__ __forceinline__ void warp_scores_softmax(const Dt* Kt, const float* q
       const int u = st * KPS + kq;
       float kv[EPV];
       if (u < nk) {
-        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
+        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt.chunk(u, sub_l)), kv);
       } else {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
@@ -244,7 +287,7 @@ __device__ __forceinline__ void warp_scores_softmax(const Dt* Kt, const float* q
       const int u = st * KPS + kq;
       float kv[EPV];
       if (u < nk) {
-        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt + (size_t)u * D + sub_l * EPV), kv);
+        Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(Kt.chunk(u, sub_l)), kv);
       } else {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) kv[e] = 0.f;
@@ -304,6 +347,7 @@ __device__ __forceinline__ void warp_scores_softmax(const Dt* Kt, const float* q
 //    output columns t*16 + L/4 (+8) of every 16-dim tile t.
 template <typename Dt, int D, int NQ, int KW>
 struct WarpAttnSimt {
+  static constexpr bool kSwizzled = false;  // reads K / V tiles as the cache lays them out
   static constexpr int DPL = D / 32;
   float m[NQ], l[NQ], o[NQ][DPL];
   __device__ __forceinline__ void reset() {
@@ -316,14 +360,14 @@ struct WarpAttnSimt {
     }
   }
   __device__ __forceinline__ void load_q(const float*, int) {}
-  __device__ __forceinline__ void attend(Dt* Kt, Dt* Vt, const float* qs, float* ps, int nk, int nq, int kb,
+  __device__ __forceinline__ void attend(KVT<Dt, D, false> Kt, KVT<Dt, D, false> Vt, const float* qs, float* ps, int nk, int nq, int kb,
                                          int pos0, int G, float scale) {
     const int lane = threadIdx.x & 31;
     warp_scores_softmax<Dt, D, NQ, KW>(Kt, qs, ps, nk, nq, kb, pos0, G, scale, m, l, o);
 #pragma unroll 4
     for (int u = 0; u < nk; ++u) {
       float v[DPL];
-      load_lane_vec<Dt, DPL>(Vt + (size_t)u * D + lane * DPL, v);
+      load_lane_vec<Dt, DPL>(Vt.elem(u, lane * DPL), v);
 #pragma unroll
       for (int i = 0; i < NQ; ++i) {
         const float p = ps[i * KW + u];
@@ -367,6 +411,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <int D, int NQ>
 struct WarpAttnMma {
+  static constexpr bool kSwizzled = true;  // reads K / V tiles 128-byte swizzled (ldmatrix over 8 rows)
   static constexpr int NT = D / 16;  // 16-dim tiles (k-steps of the scores, m-tiles of the output)
   float m[2], l[2];
   float o[NT][4];
@@ -393,14 +438,14 @@ struct WarpAttnMma {
       }
     }
   }
-  __device__ __forceinline__ void attend(__nv_bfloat16* Kt, __nv_bfloat16* Vt, const float*, float*, int nk, int nq,
+  __device__ __forceinline__ void attend(KVT<__nv_bfloat16, D, true> Kt, KVT<__nv_bfloat16, D, true> Vt, const float*, float*, int nk, int nq,
                                          int kb, int pos0, int G, float scale) {
     const int lane = threadIdx.x & 31, r0 = lane >> 2, q0 = (lane & 3) * 2;
     // value rows past this warp's keys hold whatever the stage held: zero them
     // (their probabilities are 0, but 0 * a non-finite value is not)
     if (nk < 16) {
       for (int c = lane; c < (16 - nk) * (D / 8); c += 32)
-        reinterpret_cast<uint4*>(Vt + (size_t)(nk + c / (D / 8)) * D)[c % (D / 8)] = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(Vt.chunk(nk + c / (D / 8), c % (D / 8))) = make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
     }
     // S^T = K Q^T: rows = keys r0, r0 + 8; columns = queries q0, q0 + 1
@@ -409,7 +454,7 @@ struct WarpAttnMma {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       uint32_t a[4];
-      ldsm_x4(a, Kt + (size_t)mrow * D + t * 16 + mcol);
+      ldsm_x4(a, Kt.chunk(mrow, t * 2 + mcol / 8));
       mma_bf16_16816(s, a, qf[t][0], qf[t][1]);
     }
     float mx[2];
@@ -479,7 +524,7 @@ struct WarpAttnMma {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       uint32_t a[4];
-      ldsm_x4_t(a, Vt + (size_t)vrow * D + t * 16 + vcol);
+      ldsm_x4_t(a, Vt.chunk(vrow, t * 2 + vcol / 8));
       mma_bf16_16816(o[t], a, bh0, bh1);
       mma_bf16_16816(o[t], a, bm0, bm1);
       mma_bf16_16816(o[t], a, bl0, bl1);
@@ -585,11 +630,14 @@ __device__ void combine_parts(const AttnDecArgs& a, const AttnQBlock& qb, int j,
 }
 
 template <typename Dt, int D, int NQ>
-__global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs a) {
-  extern __shared__ __align__(128) uint8_t ad_smem[];
+__global__ void __launch_bounds__(AD_THREADS, 1)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, AttnDecArgs a) {
+  extern __shared__ __align__(128) uint8_t ad_smem_raw[];
+  uint8_t* ad_smem = align1024(ad_smem_raw);  // the K/V tiles' swizzle is relative to 1024-byte blocks
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
-  constexpr int KW = LY::KW;            // keys per warp
+  constexpr int KW = LY::KW;
+  constexpr bool SWZ = WarpAttnOf<Dt, D, NQ, KW>::type::kSwizzled;  // K / V tiles swizzled (tensor loads)            // keys per warp
   constexpr int DPL = D / 32;           // head elements per lane
   constexpr int WP = LY::WPITCH;
   constexpr int MP = LY::MPITCH;
@@ -622,8 +670,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
   if (warp == AD_CWARPS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const Dt* kc = static_cast<const Dt*>(a.kc);
-      const Dt* vc = static_cast<const Dt*>(a.vc);
       int g = 0;
       // at most one item per block: item x; else the contiguous range (as the consumers)
       const int it_lo = n_items <= (int)gridDim.x ? (int)blockIdx.x
@@ -641,12 +687,16 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
             return;
           }
           const int k0 = ik.key0 + sub * CK;
-          const int nk = min(CK, ik.key0 + ik.nkeys - k0);
-          const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
-          const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
-          mbar_expect_tx(&full[s], 2 * bytes);
-          tma_load_1d(tiles(s), kc + off, bytes, &full[s]);
-          tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
+          if constexpr (SWZ) {
+            load_kv_tiles<Dt, D>(tiles(s), &map_k, &map_v, j * a.capacity + k0, qb.seq, &full[s]);
+          } else {
+            const int nk = min(CK, ik.key0 + ik.nkeys - k0);
+            const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
+            const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
+            mbar_expect_tx(&full[s], 2 * bytes);
+            tma_load_1d(tiles(s), static_cast<const Dt*>(a.kc) + off, bytes, &full[s]);
+            tma_load_1d(tiles(s) + LY::TILE, static_cast<const Dt*>(a.vc) + off, bytes, &full[s]);
+          }
           *(volatile int*)&s_issued[s] = g / LY::STAGES + 1;
         }
       }
@@ -776,8 +826,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
       const int s = (g + wsub) % LY::STAGES;
       const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
       const int nk = min(KW, ik.key0 + ik.nkeys - key0 - wk0);  // this warp's keys (may be <= 0)
-      Dt* Kt = reinterpret_cast<Dt*>(tiles(s)) + (size_t)wk0 * D;
-      Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE) + (size_t)wk0 * D;
+      const KVT<Dt, D, SWZ> Kt{tiles(s) + (size_t)wk0 * D * sizeof(Dt)};
+      const KVT<Dt, D, SWZ> Vt{tiles(s) + LY::TILE + (size_t)wk0 * D * sizeof(Dt)};
       // A warp may reach a stage before the previous use of it has landed
       // (it skips the sub-chunks a shorter item does not have): wait until the
       // producer has issued this use, so that the parity wait below cannot
@@ -814,8 +864,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
           const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
 #pragma unroll
           for (int e = 0; e < DPL; ++e) {
-            Kt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(x[e]);
-            Vt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+            Kt.elem(u - kb, lane * DPL)[e] = from_f<Dt>(x[e]);
+            Vt.elem(u - kb, lane * DPL)[e] = from_f<Dt>(v[e]);
             if (owner) {
               static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
               static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
@@ -840,11 +890,14 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_kernel(AttnDecArgs 
 // at least as many blocks as items, e.g. batch-1 decode): the queries are
 // staged and the warp partials merged for every item.
 template <typename Dt, int D, int NQ>
-__global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDecArgs a) {
-  extern __shared__ __align__(128) uint8_t ad_smem[];
+__global__ void __launch_bounds__(AD_THREADS, 1)
+    attn_decode_item_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, AttnDecArgs a) {
+  extern __shared__ __align__(128) uint8_t ad_smem_raw[];
+  uint8_t* ad_smem = align1024(ad_smem_raw);  // the K/V tiles' swizzle is relative to 1024-byte blocks
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
-  constexpr int KW = LY::KW;            // keys per warp
+  constexpr int KW = LY::KW;
+  constexpr bool SWZ = WarpAttnOf<Dt, D, NQ, KW>::type::kSwizzled;  // K / V tiles swizzled (tensor loads)            // keys per warp
   constexpr int DPL = D / 32;           // head elements per lane
   constexpr int WP = LY::WPITCH;
   constexpr int MP = LY::MPITCH;
@@ -875,8 +928,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
   if (warp == AD_CWARPS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const Dt* kc = static_cast<const Dt*>(a.kc);
-      const Dt* vc = static_cast<const Dt*>(a.vc);
       int g = 0;
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const AttnItem item = a.items[it];
@@ -889,12 +940,16 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
             return;
           }
           const int k0 = ik.key0 + sub * CK;
-          const int nk = min(CK, ik.key0 + ik.nkeys - k0);
-          const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
-          const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
-          mbar_expect_tx(&full[s], 2 * bytes);
-          tma_load_1d(tiles(s), kc + off, bytes, &full[s]);
-          tma_load_1d(tiles(s) + LY::TILE, vc + off, bytes, &full[s]);
+          if constexpr (SWZ) {
+            load_kv_tiles<Dt, D>(tiles(s), &map_k, &map_v, j * a.capacity + k0, qb.seq, &full[s]);
+          } else {
+            const int nk = min(CK, ik.key0 + ik.nkeys - k0);
+            const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
+            const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
+            mbar_expect_tx(&full[s], 2 * bytes);
+            tma_load_1d(tiles(s), static_cast<const Dt*>(a.kc) + off, bytes, &full[s]);
+            tma_load_1d(tiles(s) + LY::TILE, static_cast<const Dt*>(a.vc) + off, bytes, &full[s]);
+          }
         }
       }
       // L2 prefetch of this block's share of the next kernels' operands
@@ -944,8 +999,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
       const int s = (g + wsub) % LY::STAGES;
       const int key0 = ik.key0 + wsub * CK;                     // sub-chunk's first key
       const int nk = min(KW, ik.key0 + ik.nkeys - key0 - wk0);  // this warp's keys (may be <= 0)
-      Dt* Kt = reinterpret_cast<Dt*>(tiles(s)) + (size_t)wk0 * D;
-      Dt* Vt = reinterpret_cast<Dt*>(tiles(s) + LY::TILE) + (size_t)wk0 * D;
+      const KVT<Dt, D, SWZ> Kt{tiles(s) + (size_t)wk0 * D * sizeof(Dt)};
+      const KVT<Dt, D, SWZ> Vt{tiles(s) + LY::TILE + (size_t)wk0 * D * sizeof(Dt)};
       int landed = 1;
       if (lane == 0) landed = mbar_wait(&full[s], (uint32_t)(((g + wsub) / LY::STAGES) & 1), a.err, 2);
       __syncwarp();
@@ -967,8 +1022,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
           const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
 #pragma unroll
           for (int e = 0; e < DPL; ++e) {
-            Kt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(x[e]);
-            Vt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+            Kt.elem(u - kb, lane * DPL)[e] = from_f<Dt>(x[e]);
+            Vt.elem(u - kb, lane * DPL)[e] = from_f<Dt>(v[e]);
             if (owner) {
               static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
               static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
@@ -1041,11 +1096,14 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_item_kernel(AttnDec
 // out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c, rounded once.  No
 // partial goes through global memory and no CTA waits on another's atomic.
 template <typename Dt, int D, int NQ>
-__global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(AttnDecArgs a) {
-  extern __shared__ __align__(128) uint8_t ad_smem[];
+__global__ void __launch_bounds__(AD_THREADS, 1)
+    attn_decode_cluster_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, AttnDecArgs a) {
+  extern __shared__ __align__(128) uint8_t ad_smem_raw[];
+  uint8_t* ad_smem = align1024(ad_smem_raw);  // the K/V tiles' swizzle is relative to 1024-byte blocks
   using LY = ADLayout<Dt, D, NQ>;
   constexpr int CK = LY::CK;
   constexpr int KW = LY::KW;
+  constexpr bool SWZ = WarpAttnOf<Dt, D, NQ, KW>::type::kSwizzled;  // K / V tiles swizzled (tensor loads)
   constexpr int DPL = D / 32;
   constexpr int WP = LY::WPITCH;
   constexpr int MP = LY::MPITCH;
@@ -1086,16 +1144,18 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
   if (warp == AD_CWARPS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const Dt* kc = static_cast<const Dt*>(a.kc);
-      const Dt* vc = static_cast<const Dt*>(a.vc);
       for (int sub = 0; sub < nsub && sub < LY::STAGES; ++sub) {
         const int k0 = k_lo + sub * CK;
-        const int nk = min(CK, k_hi - k0);
-        const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
-        const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
-        mbar_expect_tx(&full[sub], 2 * bytes);
-        tma_load_1d(tiles(sub), kc + off, bytes, &full[sub]);
-        tma_load_1d(tiles(sub) + LY::TILE, vc + off, bytes, &full[sub]);
+        if constexpr (SWZ) {
+          load_kv_tiles<Dt, D>(tiles(sub), &map_k, &map_v, j * a.capacity + k0, qb.seq, &full[sub]);
+        } else {
+          const int nk = min(CK, k_hi - k0);
+          const size_t off = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + k0) * D;
+          const uint32_t bytes = (uint32_t)(nk * D * sizeof(Dt));
+          mbar_expect_tx(&full[sub], 2 * bytes);
+          tma_load_1d(tiles(sub), static_cast<const Dt*>(a.kc) + off, bytes, &full[sub]);
+          tma_load_1d(tiles(sub) + LY::TILE, static_cast<const Dt*>(a.vc) + off, bytes, &full[sub]);
+        }
       }
       // L2 prefetch of this CTA's share of the next kernels' operands
       prefetch_grid_share(a.pf, a.pf_bytes);
@@ -1131,8 +1191,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
     for (int sub = wsub; sub < nsub; sub += AD_SUBS) {
       const int key0 = k_lo + sub * CK;
       const int nk = min(KW, k_hi - key0 - wk0);
-      Dt* Kt = reinterpret_cast<Dt*>(tiles(sub)) + (size_t)wk0 * D;
-      Dt* Vt = reinterpret_cast<Dt*>(tiles(sub) + LY::TILE) + (size_t)wk0 * D;
+      const KVT<Dt, D, SWZ> Kt{tiles(sub) + (size_t)wk0 * D * sizeof(Dt)};
+      const KVT<Dt, D, SWZ> Vt{tiles(sub) + LY::TILE + (size_t)wk0 * D * sizeof(Dt)};
       int landed = 1;
       if (lane == 0) landed = mbar_wait(&full[sub], 0u, a.err, 2);
       __syncwarp();
@@ -1155,8 +1215,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
         const size_t goff = (size_t)qb.seq * a.seq_stride + ((size_t)j * a.capacity + u) * D + lane * DPL;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) {
-          Kt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(x[e]);
-          Vt[(u - kb) * D + lane * DPL + e] = from_f<Dt>(v[e]);
+          Kt.elem(u - kb, lane * DPL)[e] = from_f<Dt>(x[e]);
+          Vt.elem(u - kb, lane * DPL)[e] = from_f<Dt>(v[e]);
           if (owner) {
             static_cast<Dt*>(a.kc)[goff + e] = from_f<Dt>(x[e]);
             static_cast<Dt*>(a.vc)[goff + e] = from_f<Dt>(v[e]);
@@ -1244,9 +1304,31 @@ __global__ void __launch_bounds__(AD_THREADS, 1) attn_decode_cluster_kernel(Attn
   cluster_sync_all();
 }
 
+// 3-D map over one layer's K or V cache [sequence][kv head x capacity][D],
+// each position's row seen as D * sizeof(Dt) / 128 lines of 128 bytes: boxes
+// of CK positions' lines (one contiguous piece of the cache), 128-byte
+// swizzle, zeros out of bounds.
+template <typename Dt>
+bool make_kv_map(CUtensorMap* m, const void* base, int D, const AttnDecArgs& a) {
+  tc::EncodeTiledFn fn = tc::encode_fn();
+  const int R = D * (int)sizeof(Dt) / 128;
+  if (!fn || a.n_seqs < 1 || R < 1) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(128 / sizeof(Dt)), (cuuint64_t)R * a.KV * a.capacity, (cuuint64_t)a.n_seqs};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)a.seq_stride * sizeof(Dt)};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / sizeof(Dt)), (cuuint32_t)(R * ADT<Dt>::CK), 1}, estr[3] = {1, 1, 1};
+  return fn(m, sizeof(Dt) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename Dt, int D, int NQ>
 cudaError_t ad_launch(const LaunchCtx& c, const AttnDecArgs& a) {
   using LY = ADLayout<Dt, D, NQ>;
+  CUtensorMap mk, mv;
+  if ((reinterpret_cast<uintptr_t>(a.kc) & 15) || (reinterpret_cast<uintptr_t>(a.vc) & 15) ||
+      !make_kv_map<Dt>(&mk, a.kc, D, a) || !make_kv_map<Dt>(&mv, a.vc, D, a))
+    return cudaErrorInvalidValue;
   if (a.cluster > 1) {
     auto ck = attn_decode_cluster_kernel<Dt, D, NQ>;
     cudaError_t e = set_max_smem((const void*)ck, (int)LY::TOTAL_CL);
@@ -1269,12 +1351,12 @@ cudaError_t ad_launch(const LaunchCtx& c, const AttnDecArgs& a) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = c.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, ck, a);
+    return cudaLaunchKernelEx(&cfg, ck, mk, mv, a);
   }
   auto kern = a.runs ? attn_decode_kernel<Dt, D, NQ> : attn_decode_item_kernel<Dt, D, NQ>;
   cudaError_t e = set_max_smem((const void*)kern, (int)LY::TOTAL);
   if (e != cudaSuccess) return e;
-  return launch_k(kern, dim3(a.grid_x, a.KV), dim3(AD_THREADS), LY::TOTAL, c, a);
+  return launch_k(kern, dim3(a.grid_x, a.KV), dim3(AD_THREADS), LY::TOTAL, c, mk, mv, a);
 }
 
 template <typename Dt, int D>

@@ -326,6 +326,7 @@ struct AttnDecArgs {
   void* vc;
   long long seq_stride;
   int capacity;
+  int n_seqs;          // sequences in the cache (its outer extent)
   float scale;
   const AttnQBlock* qblocks;
   const AttnItem* items;

@@ -840,7 +840,8 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
     AttnDecArgs a{};
     a.qkv = B.qkv; a.H = c.n_heads; a.KV = KV; a.D = D; a.q_gain = W.q_norm; a.k_gain = W.k_norm;
     a.cos_t = h->rope_cos; a.sin_t = h->rope_sin; a.eps = c.rms_eps; a.kc = kc; a.vc = vc;
-    a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity; a.scale = scale; a.qblocks = qbs;
+    a.seq_stride = (long long)h->seq_stride; a.capacity = c.capacity; a.n_seqs = c.max_seqs; a.scale = scale;
+    a.qblocks = qbs;
     a.items = items; a.n_items = n_items; a.part_o = B.part_o; a.part_ml = B.part_ml; a.nq_max = P.nq_max;
     a.counters = B.counters; a.out = B.attn; a.err = B.err;
     a.grid_x = std::max(1, (h->num_sms + KV - 1) / KV);
