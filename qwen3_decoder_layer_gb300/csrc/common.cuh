@@ -13,7 +13,9 @@ namespace q3 {
 
 // Raise a kernel's dynamic shared-memory limit on the current device.  The
 // attribute belongs to a (kernel, device) pair, so it is set once for each
-// pair seen (under a lock; launches from several threads are safe).
+// pair seen (under a lock; launches from several threads are safe): the first
+// call fixes the limit, so `bytes` must be the most the kernel is ever
+// launched with.
 inline cudaError_t set_max_smem(const void* kern, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<const void*, int>> done;

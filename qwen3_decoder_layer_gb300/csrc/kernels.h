@@ -224,6 +224,10 @@ struct RouterArgs {
   int* counts;          // [E] (zeroed by the caller's scan kernel of the previous use)
 };
 cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a);
+// Router logits of T > 4 rows (GemmArgs: M rows, N experts, K, a / lda, w,
+// out / ldo fp32): fp32 fused multiply-add chains in k order, unrounded.
+bool router_logits_supported(int dt, int E, int K);
+cudaError_t launch_router_logits(const LaunchCtx& c, int dt, const GemmArgs& a);
 
 // Exclusive scan of expert counts -> row offsets and tile prefix; zeroes cursors.
 struct MoeScanArgs {

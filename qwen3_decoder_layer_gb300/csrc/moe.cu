@@ -144,6 +144,103 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(MoeCombineArgs a) {
 
 }  // namespace
 
+// Router logits of many rows: logits[t, e] = sum_k y[t, k] W[e, k], one
+// fp32 fused multiply-add chain per output in k order (the order of the
+// CUDA-core GEMM), stored unrounded.  A block takes 8 rows, staged in shared
+// memory, and every expert: warp w the experts 16w .. 16w + 15, lane (row
+// pair, expert pair) four outputs, so each 16-byte weight load feeds 2 rows
+// and each staged row load 2 experts.  (More than 256 experts: blocks along y.)
+template <typename Dt>
+__global__ void __launch_bounds__(512) router_logits_kernel(GemmArgs a) {
+  extern __shared__ __align__(16) uint8_t rl_smem[];
+  constexpr int V = Vec16<Dt>::N;
+  Dt* ys = reinterpret_cast<Dt*>(rl_smem);  // [8][K + V]: rows padded by 16 bytes (no bank conflicts)
+  pdl_wait();
+  pdl_launch();
+  const int K = a.K, E = a.N, r0 = blockIdx.x * 8;
+  const int nv = K / V, pitch = K + V;
+  for (int c = threadIdx.x; c < 8 * nv; c += blockDim.x) {
+    const int r = c / nv, v = c % nv;
+    const uint4 val = r0 + r < a.M ? ld16(static_cast<const Dt*>(a.a) + (size_t)(r0 + r) * a.lda + (size_t)v * V)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(ys + (size_t)r * pitch + (size_t)v * V) = val;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rp = lane >> 3, e0 = blockIdx.y * 256 + warp * 16 + (lane & 7) * 2;  // 256 experts per block
+  if (e0 >= E) return;
+  const Dt* w0 = static_cast<const Dt*>(a.w) + (size_t)e0 * K;
+  const Dt* w1 = e0 + 1 < E ? w0 + K : w0;
+  const Dt* y0 = ys + (size_t)(2 * rp) * pitch;
+  const Dt* y1 = y0 + pitch;
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  // the weight vectors of the next PF steps are in flight while a step computes
+  // (the chains stay in k order)
+  constexpr int PF = 4;
+  uint4 qa[PF], qb[PF];
+#pragma unroll
+  for (int p = 0; p < PF; ++p) {
+    if (p * V < K) {
+      qa[p] = ld16(w0 + p * V);
+      qb[p] = ld16(w1 + p * V);
+    }
+  }
+  for (int k = 0; k < K; k += PF * V) {
+#pragma unroll
+    for (int p = 0; p < PF; ++p) {
+      const int kk = k + p * V;
+      if (kk >= K) break;
+      float wa[V], wb[V], ya[V], yb[V];
+      Vec16<Dt>::unpack(qa[p], wa);
+      Vec16<Dt>::unpack(qb[p], wb);
+      if (kk + PF * V < K) {
+        qa[p] = ld16(w0 + kk + PF * V);
+        qb[p] = ld16(w1 + kk + PF * V);
+      }
+      Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(y0 + kk), ya);
+      Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(y1 + kk), yb);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        acc[0][0] = fmaf(ya[e], wa[e], acc[0][0]);
+        acc[0][1] = fmaf(ya[e], wb[e], acc[0][1]);
+        acc[1][0] = fmaf(yb[e], wa[e], acc[1][0]);
+        acc[1][1] = fmaf(yb[e], wb[e], acc[1][1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int row = r0 + 2 * rp + i;
+    if (row >= a.M) continue;
+    float* o = static_cast<float*>(a.out) + (size_t)row * a.ldo + e0;
+    o[0] = acc[i][0];
+    if (e0 + 1 < E) o[1] = acc[i][1];
+  }
+}
+
+bool router_logits_supported(int dt, int E, int K) {
+  const int V = dt == DT_BF16 ? 8 : 4;
+  const size_t smem = (size_t)8 * (K + V) * (dt == DT_BF16 ? 2 : 4);
+  return E >= 2 && E % 2 == 0 && E <= 512 && K % V == 0 && smem <= 200 * 1024;
+}
+
+cudaError_t launch_router_logits(const LaunchCtx& c, int dt, const GemmArgs& a) {
+  if (!router_logits_supported(dt, a.N, a.K) || (a.lda % (dt == DT_BF16 ? 8 : 4)) ||
+      (reinterpret_cast<uintptr_t>(a.a) & 15) || (reinterpret_cast<uintptr_t>(a.w) & 15))
+    return cudaErrorInvalidValue;
+  const size_t smem = (size_t)8 * (a.K + (dt == DT_BF16 ? 8 : 4)) * (dt == DT_BF16 ? 2 : 4);
+  const dim3 grid((a.M + 7) / 8, (a.N + 255) / 256), block(std::min((a.N + 15) / 16, 16) * 32);
+  // (the attribute is set once per kernel: to the largest size this launcher takes)
+  if (dt == DT_BF16) {
+    cudaError_t e = set_max_smem((const void*)router_logits_kernel<bf16>, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    return launch_k(router_logits_kernel<bf16>, grid, block, smem, c, a);
+  }
+  cudaError_t e = set_max_smem((const void*)router_logits_kernel<float>, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  return launch_k(router_logits_kernel<float>, grid, block, smem, c, a);
+}
+
 cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a) {
   if (a.E > 32 * kMaxEPerLane || a.k > 32 || a.k > a.E) return cudaErrorInvalidValue;
   return launch_k(router_topk_kernel, dim3((a.T + 7) / 8), dim3(256), 0, c, a);

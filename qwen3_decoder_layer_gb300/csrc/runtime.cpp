@@ -714,7 +714,10 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
     GemmArgs g{};
     g.M = T; g.N = E; g.K = hid; g.a = y; g.lda = hid; g.w = W.router; g.epilogue = EPI_STORE_F32;
     g.out = B.logits; g.ldo = E;
-    e = launch(L, "gemm_router", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, g); });
+    if (router_logits_supported(dt, E, hid))
+      e = launch(L, "router_logits", [&] { return launch_router_logits(L.ctx, dt, g); });
+    else
+      e = launch(L, "gemm_router", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, g); });
   }
   if (e != cudaSuccess) return e;
   const int sort_from = (64 + k - 1) / k;  // qwen3-moe.ts: sorted experts from ceil(64 / topK) rows
