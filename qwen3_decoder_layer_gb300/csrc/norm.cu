@@ -46,78 +46,9 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
   }
 }
 
-// The same, one warp per row for rows of NV 16-byte vectors per lane: every
-// load of the row (h, pend, gain) is in flight at once and the sum of squares
-// is a warp reduction (no block barrier).
-template <typename Dt, int NV>
-__global__ void __launch_bounds__(256) add_rmsnorm_warp_kernel(NormArgs a) {
-  pdl_wait();
-  pdl_launch();
-  constexpr int V = Vec16<Dt>::N;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= a.rows) return;
-  const Dt* hi = static_cast<const Dt*>(a.h_in) + (size_t)row * a.hidden;
-  const Dt* pe = a.pend ? static_cast<const Dt*>(a.pend) + (size_t)row * a.hidden : nullptr;
-  Dt* ho = static_cast<Dt*>(a.h_out) + (size_t)row * a.hidden;
-  const Dt* g = static_cast<const Dt*>(a.gain);
-  uint4 hv[NV], pv[NV], gv[NV];
-#pragma unroll
-  for (int q = 0; q < NV; ++q) {
-    const int i = (q * 32 + lane) * V;
-    hv[q] = ld16(hi + i);
-    if (pe) pv[q] = ld16(pe + i);
-    if (a.y) gv[q] = ld16(g + i);
-  }
-  F2 ss = {0.f, 0.f};
-#pragma unroll
-  for (int q = 0; q < NV; ++q) {
-    float h[V];
-    Vec16<Dt>::unpack(hv[q], h);
-    if (pe) {
-      float p[V];
-      Vec16<Dt>::unpack(pv[q], p);
-#pragma unroll
-      for (int e = 0; e < V; ++e) h[e] = rd<Dt>(h[e] + p[e]);
-      hv[q] = Vec16<Dt>::pack(h);
-    }
-    if (pe || ho != hi) *reinterpret_cast<uint4*>(ho + (q * 32 + lane) * V) = hv[q];
-#pragma unroll
-    for (int e = 0; e < V; ++e) f2_add_sq(ss, h[e]);
-  }
-  if (!a.y) return;
-  ss = f2_warp_sum(ss);
-  const F2 rs = rms_scale2(ss, a.hidden, a.eps);
-  Dt* y = static_cast<Dt*>(a.y) + (size_t)row * a.hidden;
-#pragma unroll
-  for (int q = 0; q < NV; ++q) {
-    float h[V], gg[V], o[V];
-    Vec16<Dt>::unpack(hv[q], h);
-    Vec16<Dt>::unpack(gv[q], gg);
-#pragma unroll
-    for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(h[e], rs, gg[e]);
-    *reinterpret_cast<uint4*>(y + (q * 32 + lane) * V) = Vec16<Dt>::pack(o);
-  }
-}
-
-template <typename Dt>
-cudaError_t add_rmsnorm_dt(const LaunchCtx& c, const NormArgs& a) {
-  constexpr int V = Vec16<Dt>::N;
-  const dim3 wgrid((a.rows + 7) / 8), wblock(256);
-  if (a.hidden % (32 * V) == 0) {
-    switch (a.hidden / (32 * V)) {
-      case 1: return launch_k(add_rmsnorm_warp_kernel<Dt, 1>, wgrid, wblock, 0, c, a);
-      case 2: return launch_k(add_rmsnorm_warp_kernel<Dt, 2>, wgrid, wblock, 0, c, a);
-      case 4: return launch_k(add_rmsnorm_warp_kernel<Dt, 4>, wgrid, wblock, 0, c, a);
-      case 8: return launch_k(add_rmsnorm_warp_kernel<Dt, 8>, wgrid, wblock, 0, c, a);
-      case 16: return launch_k(add_rmsnorm_warp_kernel<Dt, 16>, wgrid, wblock, 0, c, a);
-    }
-  }
-  return launch_k(add_rmsnorm_kernel<Dt>, dim3(a.rows), dim3(256), 0, c, a);
-}
-
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, int dt, const NormArgs& a) {
-  return dt == DT_BF16 ? add_rmsnorm_dt<bf16>(c, a) : add_rmsnorm_dt<float>(c, a);
+  if (dt == DT_BF16) return launch_k(add_rmsnorm_kernel<bf16>, dim3(a.rows), dim3(256), 0, c, a);
+  return launch_k(add_rmsnorm_kernel<float>, dim3(a.rows), dim3(256), 0, c, a);
 }
 
 // EPL consecutive elements of the model dtype <-> fp32, one vector access.
