@@ -281,16 +281,16 @@ __device__ __forceinline__ F2 rms_scale2(F2 ss, int n, float eps) {
 // tie of the model dtype, which way the exact product lies.
 template <typename Dt> __device__ __forceinline__ float mul_round(float h, F2 rs);
 template <> __device__ __forceinline__ float mul_round<float>(float h, F2 rs) { return fmaf(h, rs.hi, h * rs.lo); }
+// Branch-free (selects only), so that independent elements interleave.
 template <> __device__ __forceinline__ float mul_round<__nv_bfloat16>(float h, F2 rs) {
   const float p = h * rs.hi;
   const uint32_t b = __float_as_uint(p);
-  if ((b & 0xffffu) != 0x8000u) return rd<__nv_bfloat16>(p);
   const float res = fmaf(h, rs.hi, -p) + h * rs.lo;  // exact product - p (to fp32 accuracy)
-  if (res == 0.f) return rd<__nv_bfloat16>(p);
-  // p is halfway between two bf16 values: the residual's sign picks the side
+  // p halfway between two bf16 values: the residual's sign picks the side
   const uint32_t lo = b & 0xffff0000u;  // toward zero
   const float down = __uint_as_float(lo), up = __uint_as_float(lo + 0x10000u);  // up = away from zero
-  return ((res > 0.f) == (p > 0.f)) ? up : down;
+  const float side = ((res > 0.f) == (p > 0.f)) ? up : down;
+  return ((b & 0xffffu) != 0x8000u || res == 0.f) ? rd<__nv_bfloat16>(p) : side;
 }
 // Qwen3 RMSNorm element with its two roundings: R(R(h * rs) * g).
 template <typename Dt>

@@ -20,6 +20,13 @@
 // For SiLU * up the B tile is two 128-row boxes: gate rows n0.. and up rows
 // N + n0.., so TMEM columns 0..127 hold g and 128..255 hold u of the same
 // output columns.
+// For the q|k|v product (EPI_QKROPE, Backbone.forward's q_norm / k_norm, the
+// rotary embedding of Backbone._rope and the cache append) the q|k|v rows
+// never reach global memory: each head of a tile is staged rounded to bf16,
+// read back with HD/8 lanes per row, normalised (the head's sum of squares
+// is a shuffle reduction over the row's lanes), rotated (the partner of
+// column d, d +- HD/2, sits in lane ^ HD/16) and stored: queries to
+// q_out [M][H][HD], keys and values to their cache rows.
 #include <algorithm>
 
 #include "kernels.h"
@@ -30,14 +37,23 @@ namespace q3 {
 namespace {
 
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
-constexpr int TC_THREADS = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA
+// Warps 0 .. E-1 epilogue, E TMA, E+1 MMA; E = 4, or 8 for the q|k|v
+// epilogue (warps w and w + 4 share TMEM lanes 32 (w & 3) .. + 31 and take
+// the two halves of the tile's columns).
+__host__ __device__ constexpr int tc_epi_warps(int epi) { return epi == EPI_QKROPE ? 8 : 4; }
+__host__ __device__ constexpr int tc_threads(int epi) { return (tc_epi_warps(epi) + 2) * 32; }
 constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column accumulators
 constexpr size_t TC_A_BYTES = (size_t)TC_BM * TC_BK * 2;   // 16 KB
 constexpr size_t TC_B_BYTES = (size_t)TC_BN * TC_BK * 2;   // 32 KB
 constexpr size_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
 // epilogue staging: per epilogue warp 32 rows x 64 output columns (128 B per row)
 constexpr size_t TC_STG_WARP = 32 * 128;
-constexpr size_t TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 256 /* barriers */ + 4 * TC_STG_WARP + 1024 /* align */;
+__host__ __device__ constexpr size_t tc_smem(int epi) {
+  // the q|k|v epilogue stores each lane's own row and stages nothing
+  return TC_STAGES * TC_STAGE_BYTES + 256 /* barriers */ + (epi == EPI_QKROPE ? 0 : 4 * TC_STG_WARP) +
+         1024 /* align */;
+}
+static_assert(tc_smem(EPI_QKROPE) <= 227 * 1024, "q|k|v epilogue staging exceeds shared memory");
 
 using namespace tc;
 
@@ -75,8 +91,100 @@ __device__ __forceinline__ TileInfo tile_of(const GemmTcArgs& a, int t, int tile
   return ti;
 }
 
-template <int EPI, bool GROUPED>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+// The q|k|v epilogue of the heads in columns c0 .. c0 + 127 of one tile, by
+// the lane owning tile row `row` (tl: the warp's TMEM lanes at the
+// accumulator's first column; my_seq, my_pos: the row's sequence and position,
+// 0 past the last row; csr: the row's RoPE table entries, (cos | sin << 16)
+// bf16 pairs of the HD/2 frequencies).  The lane works on its row as tensor
+// memory delivers it: the sum of squares of the head rounded to bf16, then
+// (reading the row again) the RMSNorm with its two roundings and the one-rounding
+// rotation of the pairs (d, d + HD/2): R(y1 c - y2 s), R(y2 c + y1 s) (both
+// halves of a table row use the same frequencies); then 16-byte stores of
+// its row: queries to q_out [M][H][HD], keys and values to their cache rows.
+template <int HD>
+__device__ __forceinline__ void qkrope_tile(const GemmTcArgs& a, const TileInfo& ti, uint32_t tl, int row,
+                                            int my_seq, int my_pos, const uint4* csr, int c0) {
+  constexpr int HALF = HD / 2;
+  const QkRopeArgs& r = a.rope;
+  const bool live = row < ti.mlim;
+  for (int c = c0; c < c0 + TC_BN / 2; c += HD) {
+    const int hd = (ti.n0 + c) / HD;  // head index in the q|k|v row (warp-uniform)
+    const int kind = hd < r.H ? 0 : hd < r.H + r.KV ? 1 : 2;
+    bf16* dst = kind == 0 ? static_cast<bf16*>(r.q_out) + ((size_t)row * r.H + hd) * HD
+                          : static_cast<bf16*>(kind == 1 ? r.kcache : r.vcache) + (size_t)my_seq * r.seq_stride +
+                                ((size_t)(hd - r.H - (kind == 2 ? r.KV : 0)) * r.capacity + my_pos) * HD;
+    if (kind == 2) {  // values: rounded to bf16 and appended as they are
+#pragma unroll
+      for (int h = 0; h < HD / 32; ++h) {
+        uint32_t v[32];
+        tmem_ld32(tl + c + 32 * h, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(v[8 * q + e]);
+          if (live) *reinterpret_cast<uint4*>(dst + 32 * h + 8 * q) = Vec16<bf16>::pack(o);
+        }
+      }
+      continue;
+    }
+    // 1. the head's sum of squares of the bf16-rounded row: one chain per 32
+    // columns, then added
+    F2 ss = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < HD / 32; ++h) {
+      uint32_t v[32];
+      tmem_ld32(tl + c + 32 * h, v);
+      F2 part = {0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f2_add_sq(part, rd<bf16>(__uint_as_float(v[e])));
+      ss = h == 0 ? part : f2_add(ss, part);
+    }
+    const F2 rs = rms_scale2(ss, HD, r.eps);
+    const bf16* g = static_cast<const bf16*>(kind == 0 ? r.q_gain : r.k_gain);
+    // 2. the pairs (d, d + HALF), 16 values of d at a time, read again from
+    // tensor memory
+#pragma unroll
+    for (int j = 0; j < HALF; j += 16) {
+      uint32_t lo[16], hi[16];
+      tmem_ld16(tl + c + j, lo);
+      tmem_ld16(tl + c + HALF + j, hi);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // 8 values of d
+        const int d0 = j + 8 * q;
+        const uint4 gl = ld16(g + d0), gh = ld16(g + HALF + d0);
+        const uint32_t glw[4] = {gl.x, gl.y, gl.z, gl.w}, ghw[4] = {gh.x, gh.y, gh.z, gh.w};
+        const uint32_t cw[8] = {csr[d0 / 4].x, csr[d0 / 4].y, csr[d0 / 4].z, csr[d0 / 4].w,
+                                csr[d0 / 4 + 1].x, csr[d0 / 4 + 1].y, csr[d0 / 4 + 1].z, csr[d0 / 4 + 1].w};
+        uint32_t o1[4], o2[4];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          // element e of a run of bf16 pairs: the low half of word e/2 when e is even
+          auto half = [&](uint32_t w) { return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16)); };
+          const float x1 = rd<bf16>(__uint_as_float(lo[8 * q + e])), x2 = rd<bf16>(__uint_as_float(hi[8 * q + e]));
+          const float cs = __uint_as_float(cw[e] << 16), sn = __uint_as_float(cw[e] & 0xffff0000u);
+          const float y1 = rms_apply2<bf16>(x1, rs, half(glw[e / 2])), y2 = rms_apply2<bf16>(x2, rs, half(ghw[e / 2]));
+          // both products exact in fp32 (8-bit significands); one rounding of each result
+          const float r1 = rd<bf16>(fmaf(y1, cs, -(y2 * sn))), r2 = rd<bf16>(fmaf(y2, cs, y1 * sn));
+          if (e & 1) {
+            o1[e / 2] |= __float_as_uint(r1) & 0xffff0000u;
+            o2[e / 2] |= __float_as_uint(r2) & 0xffff0000u;
+          } else {
+            o1[e / 2] = __float_as_uint(r1) >> 16;
+            o2[e / 2] = __float_as_uint(r2) >> 16;
+          }
+        }
+        if (live) {
+          *reinterpret_cast<uint4*>(dst + d0) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          *reinterpret_cast<uint4*>(dst + HALF + d0) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        }
+      }
+    }
+  }
+}
+
+template <int EPI, bool GROUPED, int HD = 0>
+__global__ void __launch_bounds__(tc_threads(EPI), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    GemmTcArgs a) {
   extern __shared__ uint8_t tc_smem_raw[];
@@ -92,18 +200,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // tile t -> rows (t % tiles_m), columns (t / tiles_m): blocks running at the
   // same time share weight tiles in L2
 
-  if (warp == 4 && lane == 0) {
+  constexpr int NEPI = tc_epi_warps(EPI), TMA_WARP = NEPI, MMA_WARP = NEPI + 1;
+  if (warp == TMA_WARP && lane == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], NEPI);  // one arrival per epilogue warp
     }
     mbar_fence_init();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, TC_TMEM_COLS);
+  if (warp == MMA_WARP) tmem_alloc(tmem_slot, TC_TMEM_COLS);
   fence_before();
   __syncthreads();
   fence_after();
@@ -114,7 +223,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int tiles_m = GROUPED ? a.tile_start[a.n_groups] : (a.M + TC_BM - 1) / TC_BM;
   const int tiles = tiles_m * (a.N / ncol);
 
-  if (warp == 4) {
+  if (warp == TMA_WARP) {
     if (lane == 0) {  // TMA producer: the k-blocks of this block's tiles, in order
       int q = 0;
       bool ok = true;
@@ -136,7 +245,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == MMA_WARP) {
     if (lane == 0) {  // MMA issuer: tile i accumulates in TMEM columns (i & 1) * 256
       int q = 0, i = 0;
       bool ok = true;
@@ -162,20 +271,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {  // epilogue: warp q reads TMEM lanes 32q .. 32q + 31 = tile rows
     // staging slab of this warp: row r's 16-byte chunk j sits at chunk j ^ (r & 7)
     uint4* stg = reinterpret_cast<uint4*>(smem + TC_STAGES * TC_STAGE_BYTES + 256 + warp * TC_STG_WARP);
+    const int quad = warp & 3;  // TMEM lanes 32 quad .. + 31 = tile rows
     int i = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int b = i & 1, use = i >> 1;
       const TileInfo ti = tile_of<GROUPED>(a, t, tiles_m, ncol);
+      // q|k|v epilogue: the sequence and position of this lane's row, fetched
+      // while the tile's MMAs run (rows past the last read 0)
+      // and its RoPE table entries
+      int my_seq = 0, my_pos = 0;
+      uint4 csr[HD > 0 ? HD / 8 : 1];
+      if constexpr (EPI == EPI_QKROPE) {
+        const int myrow = ti.m0 + quad * 32 + lane;
+        if (myrow < ti.mlim) { my_seq = a.rope.row_seq[myrow]; my_pos = a.rope.row_pos[myrow]; }
+        const uint4* cp = reinterpret_cast<const uint4*>(a.rope.cs_bf16 + (size_t)my_pos * (HD / 2));
+#pragma unroll
+        for (int q = 0; q < HD / 8; ++q) csr[q] = __ldg(cp + q);
+      }
       int okl = 1;  // lane 0 waits for the accumulator; the other lanes wait at the warp barrier
       if (lane == 0) okl = mbar_wait(&acc_full[b], (uint32_t)(use & 1), a.err, 5);
       __syncwarp();
       if (!__shfl_sync(0xffffffffu, okl, 0)) break;
       fence_after();
-      const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * TC_BN);
+      const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * TC_BN);
       // the 8 rows this lane stores per 64-column slab: r = 4k + lane / 8, chunk lane % 8
       const int jr = lane & 7, r0 = lane >> 3;
-      const int rbase = ti.m0 + warp * 32;
-      for (int c = 0; c < ncol; c += 64) {
+      const int rbase = ti.m0 + quad * 32;
+      if constexpr (EPI == EPI_QKROPE)
+        qkrope_tile<HD>(a, ti, tl, rbase + lane, my_seq, my_pos, csr, (warp >> 2) * (TC_BN / 2));
+      else for (int c = 0; c < ncol; c += 64) {
         // 1. this lane's row: 64 columns from tensor memory, rounded to bf16, into the slab
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -239,7 +363,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     fence_after();
     tmem_dealloc(tmem, TC_TMEM_COLS);
   }
@@ -254,15 +378,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return make_map_bf16(m, base, 2, dims, strides, box_rows);
 }
 
-template <int EPI, bool GROUPED>
+template <int EPI, bool GROUPED, int HD = 0>
 cudaError_t tc_launch(const LaunchCtx& c, const CUtensorMap& ma, const CUtensorMap& mb, const GemmTcArgs& a) {
-  auto kern = gemm_tc_kernel<EPI, GROUPED>;
-  cudaError_t e = set_max_smem((const void*)kern, (int)TC_SMEM);
+  auto kern = gemm_tc_kernel<EPI, GROUPED, HD>;
+  constexpr size_t smem = tc_smem(EPI);
+  cudaError_t e = set_max_smem((const void*)kern, (int)smem);
   if (e != cudaSuccess) return e;
   const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
   const int tiles = (a.N / ncol) * (GROUPED ? a.max_tiles_m : (a.M + TC_BM - 1) / TC_BM);
   const dim3 grid(std::min(tiles, c.num_sms));  // persistent: tiles t = blockIdx.x, + gridDim.x, ...
-  return launch_k(kern, grid, dim3(TC_THREADS), TC_SMEM, c, ma, mb, a);
+  return launch_k(kern, grid, dim3(tc_threads(EPI)), smem, c, ma, mb, a);
 }
 
 }  // namespace
@@ -271,8 +396,12 @@ bool gemm_tc_supported(int M, int N, int K, int epilogue) {
   if (!encode_fn()) return false;
   if (M < 1 || K % TC_BK) return false;
   if (epilogue == EPI_SWIGLU) return N % (TC_BN / 2) == 0;
-  if (epilogue == EPI_STORE || epilogue == EPI_RESIDUAL) return N % TC_BN == 0;
+  if (epilogue == EPI_STORE || epilogue == EPI_RESIDUAL || epilogue == EPI_QKROPE) return N % TC_BN == 0;
   return false;
+}
+
+bool gemm_tc_qkrope_supported(int M, int H, int KV, int D) {
+  return (D == 64 || D == 128) && H > 0 && KV > 0 && gemm_tc_supported(M, (H + 2 * KV) * D, 64, EPI_QKROPE);
 }
 
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a) {
@@ -285,6 +414,18 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a) {
   if (!make_map(&ma, a.a, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda, TC_BM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, a.w, wrows, (uint64_t)a.K, (uint64_t)a.K, a.epilogue == EPI_SWIGLU ? TC_BN / 2 : TC_BN))
     return cudaErrorInvalidValue;
+  if (a.epilogue == EPI_QKROPE) {
+    const QkRopeArgs& r = a.rope;
+    if (a.tile_start || !gemm_tc_qkrope_supported(a.M, r.H, r.KV, r.D) || a.N != (r.H + 2 * r.KV) * r.D ||
+        !r.q_out || !r.kcache || !r.vcache || !r.q_gain || !r.k_gain || !r.cos_t || !r.sin_t || !r.row_seq ||
+        !r.row_pos || (reinterpret_cast<uintptr_t>(r.q_out) & 15) || (reinterpret_cast<uintptr_t>(r.kcache) & 15) ||
+        (reinterpret_cast<uintptr_t>(r.vcache) & 15) || (reinterpret_cast<uintptr_t>(r.q_gain) & 15) ||
+        (reinterpret_cast<uintptr_t>(r.k_gain) & 15) || (reinterpret_cast<uintptr_t>(r.cos_t) & 15) ||
+        (reinterpret_cast<uintptr_t>(r.sin_t) & 15) || !r.cs_bf16 || (reinterpret_cast<uintptr_t>(r.cs_bf16) & 15) ||
+        (r.seq_stride % 8))
+      return cudaErrorInvalidValue;
+    return r.D == 128 ? tc_launch<EPI_QKROPE, false, 128>(c, ma, mb, a) : tc_launch<EPI_QKROPE, false, 64>(c, ma, mb, a);
+  }
   if (a.tile_start) {
     if (a.epilogue == EPI_STORE) return tc_launch<EPI_STORE, true>(c, ma, mb, a);
     if (a.epilogue == EPI_SWIGLU) return tc_launch<EPI_SWIGLU, true>(c, ma, mb, a);

@@ -9,7 +9,8 @@ namespace q3 {
 enum DType { DT_F32 = 0, DT_BF16 = 1 };
 enum WFmt { W_DT = 0, W_U8 = 1 };  // weights in the model dtype, or affine int8 codes
 enum Epi { EPI_STORE = 0, EPI_STORE_F32 = 1, EPI_RESIDUAL = 2, EPI_SWIGLU = 3,
-           EPI_STORE_RF32 = 4 /* rounded to the model dtype, stored as fp32 (output head) */ };
+           EPI_STORE_RF32 = 4 /* rounded to the model dtype, stored as fp32 (output head) */,
+           EPI_QKROPE = 5 /* q|k|v rows: per-head q/k RMSNorm + RoPE, q to q_out, k and v to the caches */ };
 
 struct LaunchCtx {
   cudaStream_t stream;
@@ -48,6 +49,9 @@ struct QkRopeArgs {
   const int* row_seq;  // [T]
   const int* row_pos;  // [T]
   float eps;
+  // bf16 models: the same table as bf16 pairs (cos | sin << 16) of the D/2
+  // frequencies, [capacity][D/2] (every cos / sin value is a bf16 value)
+  const uint32_t* cs_bf16;
 };
 cudaError_t launch_qk_rope_cache(const LaunchCtx& c, int dt, const QkRopeArgs& a);
 
@@ -156,8 +160,13 @@ struct GemmTcArgs {
   long long w_group_rows;
   long long w_rows_total;
   const int* c_rows;
+  // EPI_QKROPE: the head layout, gains, RoPE table, caches and row positions
+  // (rope.qkv unused: the q|k|v rows never leave the kernel)
+  QkRopeArgs rope;
 };
 bool gemm_tc_supported(int M, int N, int K, int epilogue);
+// the q|k|v GEMM with the fused q/k RMSNorm + RoPE + cache-append epilogue
+bool gemm_tc_qkrope_supported(int M, int H, int KV, int D);
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a);
 
 // Attention over the cache.  Work: query blocks (rows of one sequence at

@@ -71,6 +71,7 @@ struct qwen3_handle {
   size_t layer_stride = 0;  // elements between layers
   float* rope_cos = nullptr;
   float* rope_sin = nullptr;
+  uint32_t* rope_cs16 = nullptr;  // bf16 models: (cos | sin << 16) per (position, frequency)
   std::vector<int32_t> lengths;
   std::string err;
   // options
@@ -346,6 +347,25 @@ qwen3_status qwen3_create(const qwen3_config* cfg, const qwen3_layer_weights* la
   }
   cudaMemcpy(h->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
   cudaMemcpy(h->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
+  if (c.dtype == QWEN3_DTYPE_BF16) {
+    // the table's bf16 values (exact: each was rounded to bf16 above), one
+    // (cos, sin) pair per frequency, for the q|k|v GEMM epilogue
+    std::vector<uint32_t> cs16((size_t)c.capacity * half);
+    auto bits = [](float v) {
+      uint32_t u;
+      std::memcpy(&u, &v, 4);
+      return u >> 16;
+    };
+    for (int p = 0; p < c.capacity; ++p)
+      for (int i = 0; i < half; ++i)
+        cs16[(size_t)p * half + i] = bits(cs[(size_t)p * D + i]) | (bits(sn[(size_t)p * D + i]) << 16);
+    if (cudaMalloc(&h->rope_cs16, cs16.size() * 4) != cudaSuccess) {
+      cudaGetLastError();
+      qwen3_destroy(h);
+      return QWEN3_E_OOM;
+    }
+    cudaMemcpy(h->rope_cs16, cs16.data(), cs16.size() * 4, cudaMemcpyHostToDevice);
+  }
   h->lengths.assign(c.max_seqs, 0);
   for (int i = 0; i < qwen3_handle::kRing; ++i) cudaEventCreateWithFlags(&h->pinned_ev[i], cudaEventDisableTiming);
   cudaStreamCreateWithFlags(&h->gstream, cudaStreamNonBlocking);
@@ -386,6 +406,7 @@ void qwen3_destroy(qwen3_handle* h) {
   if (h->vcache) cudaFree(h->vcache);
   if (h->rope_cos) cudaFree(h->rope_cos);
   if (h->rope_sin) cudaFree(h->rope_sin);
+  if (h->rope_cs16) cudaFree(h->rope_cs16);
   delete h;
 }
 
@@ -823,10 +844,26 @@ int decode_cluster_size(qwen3_handle* h, const Plan& P) {
   return 0;
 }
 
-// Attention of layer l for the plan's kernel.
+// q/k RMSNorm + RoPE + cache append of layer l's q|k|v rows (B.qkv) for the
+// prefill attention kernels: queries to B.q, keys and values to the caches.
+QkRopeArgs qk_rope_args(qwen3_handle* h, const Plan& P, int l, const Bufs& B) {
+  const qwen3_config& c = h->cfg;
+  const qwen3_layer_weights& W = h->layers[l];
+  QkRopeArgs r{};
+  r.qkv = B.qkv; r.T = P.T; r.H = c.n_heads; r.KV = c.n_kv_heads; r.D = c.head_dim; r.q_out = B.q;
+  r.kcache = static_cast<char*>(h->kcache) + (size_t)l * h->layer_stride * h->esz;
+  r.vcache = static_cast<char*>(h->vcache) + (size_t)l * h->layer_stride * h->esz;
+  r.seq_stride = (long long)h->seq_stride; r.capacity = c.capacity; r.q_gain = W.q_norm; r.k_gain = W.k_norm;
+  r.cos_t = h->rope_cos; r.sin_t = h->rope_sin; r.row_seq = B.desc + P.off_rowseq; r.row_pos = B.desc + P.off_rowpos;
+  r.eps = c.rms_eps; r.cs_bf16 = h->rope_cs16;
+  return r;
+}
+
+// Attention of layer l for the plan's kernel (qk_done: the q|k|v GEMM's
+// epilogue already normalised, rotated and appended the rows).
 cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l, const Bufs& B,
                               const void* pf = nullptr, size_t pf_bytes = 0, const void* pf2 = nullptr,
-                              size_t pf2_bytes = 0) {
+                              size_t pf2_bytes = 0, bool qk_done = false) {
   const qwen3_config& c = h->cfg;
   const qwen3_layer_weights& W = h->layers[l];
   const int dt = h->dt, KV = c.n_kv_heads, D = c.head_dim;
@@ -859,12 +896,11 @@ cudaError_t enqueue_attention(qwen3_handle* h, Launcher& L, const Plan& P, int l
     return launch(L, a.cluster > 1 ? "attn_decode_cluster" : "attn_decode",
                   [&] { return launch_attn_decode2(L.ctx, dt, a); });
   }
-  QkRopeArgs r{};
-  r.qkv = B.qkv; r.T = P.T; r.H = c.n_heads; r.KV = KV; r.D = D; r.q_out = B.q; r.kcache = kc; r.vcache = vc;
-  r.seq_stride = (long long)h->seq_stride; r.capacity = c.capacity; r.q_gain = W.q_norm; r.k_gain = W.k_norm;
-  r.cos_t = h->rope_cos; r.sin_t = h->rope_sin; r.row_seq = row_seq; r.row_pos = row_pos; r.eps = c.rms_eps;
-  e = launch(L, "qk_rope_cache", [&] { return launch_qk_rope_cache(L.ctx, dt, r); });
-  if (e != cudaSuccess) return e;
+  if (!qk_done) {
+    const QkRopeArgs r = qk_rope_args(h, P, l, B);
+    e = launch(L, "qk_rope_cache", [&] { return launch_qk_rope_cache(L.ctx, dt, r); });
+    if (e != cudaSuccess) return e;
+  }
   if (P.attn == ATTN_TC) {
     AttnTcArgs t{};
     t.qblocks = qbs; t.n_qblocks = P.n_qblocks; t.T = P.T; t.H = c.n_heads; t.KV = KV; t.D = D;
@@ -1027,12 +1063,23 @@ cudaError_t enqueue_prefill(qwen3_handle* h, Launcher& L, const Plan& P, const v
     n.rows = T; n.hidden = hid; n.eps = c.rms_eps;
     e = launch(L, "add_rmsnorm", [&] { return launch_add_rmsnorm(L.ctx, dt, n); });
     if (e != cudaSuccess) return e;
-    GemmArgs g{};
-    g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
-    g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
-    e = linear_gemm(h, L, kQkv, wfmt_of(W.qkv), g, B);
+    // bf16 on tensor cores: q/k RMSNorm, RoPE and the cache append run in the
+    // q|k|v GEMM's epilogue (the rows never reach global memory)
+    const bool qk_fused = P.attn != ATTN_DECODE && h->use_tc && dt == DT_BF16 && wfmt_of(W.qkv) == W_DT &&
+                          gemm_tc_qkrope_supported(T, H, KV, D) && gemm_tc_supported(T, qkv_rows, hid, EPI_QKROPE);
+    if (qk_fused) {
+      GemmTcArgs t{};
+      t.M = T; t.N = qkv_rows; t.K = hid; t.a = B.y; t.lda = hid; t.w = W.qkv.w; t.out = nullptr; t.ldo = qkv_rows;
+      t.epilogue = EPI_QKROPE; t.err = B.err; t.rope = qk_rope_args(h, P, l, B);
+      e = launch(L, "gemm_tc_qkv_rope", [&] { return launch_gemm_tc(L.ctx, t); });
+    } else {
+      GemmArgs g{};
+      g.M = T; g.N = qkv_rows; g.K = hid; g.a = B.y; g.lda = hid; g.w = W.qkv.w; g.scale = W.qkv.scale;
+      g.bias = W.qkv.bias; g.group = c.group_size; g.epilogue = EPI_STORE; g.out = B.qkv; g.ldo = qkv_rows;
+      e = linear_gemm(h, L, kQkv, wfmt_of(W.qkv), g, B);
+    }
     if (e != cudaSuccess) return e;
-    e = enqueue_attention(h, L, P, l, B);
+    e = enqueue_attention(h, L, P, l, B, nullptr, 0, nullptr, 0, qk_fused);
     if (e != cudaSuccess) return e;
     GemmArgs go{};
     go.M = T; go.N = hid; go.K = H * D; go.a = B.attn; go.lda = H * D; go.w = W.o.w; go.scale = W.o.scale;
