@@ -235,8 +235,26 @@ struct RouterArgs {
 cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a);
 // Router logits of T > 4 rows (GemmArgs: M rows, N experts, K, a / lda, w,
 // out / ldo fp32): fp32 fused multiply-add chains in k order, unrounded.
+// Router logits of many rows, fp32 and unrounded: out[t][e] = sum_k y[t][k] W[e][k]
+// (y [M][ldy] and W [E][K] in the model dtype).  The k range may be split:
+// `part` holds the partial tiles ([max_splits][M][E] floats), `counters` one
+// int per 32 x 128 output tile, zero between calls (the kernel restores it);
+// part == NULL computes each output in one range.
+struct RouterLogitsArgs {
+  int M, E, K;
+  const void* y;
+  int ldy;
+  const void* w;
+  float* out;
+  int ldo;
+  float* part;
+  int* counters;
+  int max_splits;
+};
 bool router_logits_supported(int dt, int E, int K);
-cudaError_t launch_router_logits(const LaunchCtx& c, int dt, const GemmArgs& a);
+cudaError_t launch_router_logits(const LaunchCtx& c, int dt, const RouterLogitsArgs& a);
+constexpr int kRouterMaxSplits = 8;
+int router_logits_tiles(int M, int E);
 
 // Exclusive scan of expert counts -> row offsets and tile prefix; zeroes cursors.
 struct MoeScanArgs {

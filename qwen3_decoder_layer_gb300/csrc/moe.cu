@@ -144,101 +144,170 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(MoeCombineArgs a) {
 
 }  // namespace
 
-// Router logits of many rows: logits[t, e] = sum_k y[t, k] W[e, k], one
-// fp32 fused multiply-add chain per output in k order (the order of the
-// CUDA-core GEMM), stored unrounded.  A block takes 8 rows, staged in shared
-// memory, and every expert: warp w the experts 16w .. 16w + 15, lane (row
-// pair, expert pair) four outputs, so each 16-byte weight load feeds 2 rows
-// and each staged row load 2 experts.  (More than 256 experts: blocks along y.)
+namespace {
+
+// Router logits of many rows: logits[t, e] = sum_k y[t, k] W[e, k] in fp32,
+// stored unrounded (the products of two bf16 values are exact in fp32; only
+// the additions round).  K is cut into at most 8 fixed ranges (by K alone);
+// each output is one fused multiply-add chain per range in k order, and the
+// range sums are added in range order, however many blocks share the work, so
+// the result is the same bits with or without a split.  A block computes a
+// 32-row x 128-expert tile over a run of ranges: chunks of 32 k staged in
+// shared memory as fp32 (rows, resp. experts, contiguous for each k), each
+// thread owns a 4 x 4 block of outputs.  Split tiles store one partial per
+// range; the last block of the tile to finish adds them.
+constexpr int RL_BM = 32, RL_BE = 128, RL_BK = 32, RL_THREADS = 256;
+
 template <typename Dt>
-__global__ void __launch_bounds__(512) router_logits_kernel(GemmArgs a) {
-  extern __shared__ __align__(16) uint8_t rl_smem[];
-  constexpr int V = Vec16<Dt>::N;
-  Dt* ys = reinterpret_cast<Dt*>(rl_smem);  // [8][K + V]: rows padded by 16 bytes (no bank conflicts)
+__global__ void __launch_bounds__(RL_THREADS) router_logits_kernel(RouterLogitsArgs a, int splits, int cpr, int nranges,
+                                                                  int rpb) {
+  constexpr int V = Vec16<Dt>::N;  // elements per 16-byte vector
+  __shared__ __align__(16) float ys[RL_BK][RL_BM];
+  __shared__ __align__(16) float ws[RL_BK][RL_BE];
+  __shared__ int s_last;
   pdl_wait();
   pdl_launch();
-  const int K = a.K, E = a.N, r0 = blockIdx.x * 8;
-  const int nv = K / V, pitch = K + V;
-  for (int c = threadIdx.x; c < 8 * nv; c += blockDim.x) {
-    const int r = c / nv, v = c % nv;
-    const uint4 val = r0 + r < a.M ? ld16(static_cast<const Dt*>(a.a) + (size_t)(r0 + r) * a.lda + (size_t)v * V)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(ys + (size_t)r * pitch + (size_t)v * V) = val;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int tiles_e = (a.E + RL_BE - 1) / RL_BE;
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int r0 = (tile / tiles_e) * RL_BM, e0 = (tile % tiles_e) * RL_BE;
+  const int nchunks = a.K / RL_BK;
+  const int rb = split * rpb, re = min(nranges, rb + rpb);  // this block's ranges
+  const int c0 = rb * cpr, c1 = min(nchunks, re * cpr);
+  // staging roles: experts e0 + (tid & 127), 16 k from (tid >> 7) * 16; rows
+  // r0 + (tid & 31), 8 k from (tid >> 5) * 8 (threads 0..127)
+  const int we = e0 + (tid & 127), wk = (tid >> 7) * 16;
+  const int yr = r0 + (tid & 31), yk = (tid >> 5) * 8;
+  const Dt* wsrc = static_cast<const Dt*>(a.w) + (size_t)min(we, a.E - 1) * a.K + wk;
+  const Dt* ysrc = static_cast<const Dt*>(a.y) + (size_t)min(yr, a.M - 1) * a.ldy + yk;
+  const bool wlive = we < a.E, ylive = tid < 128 && yr < a.M;
+  uint4 wq[16 / V], yq[8 / V];
+  auto fetch = [&](int ch) {
+#pragma unroll
+    for (int i = 0; i < 16 / V; ++i) wq[i] = wlive ? ld16(wsrc + (size_t)ch * RL_BK + i * V) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 8 / V; ++i) yq[i] = ylive ? ld16(ysrc + (size_t)ch * RL_BK + i * V) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  auto stage = [&]() {
+#pragma unroll
+    for (int i = 0; i < 16 / V; ++i) {
+      float f[V];
+      Vec16<Dt>::unpack(wq[i], f);
+#pragma unroll
+      for (int j = 0; j < V; ++j) ws[wk + i * V + j][tid & 127] = f[j];
+    }
+    if (tid < 128) {
+#pragma unroll
+      for (int i = 0; i < 8 / V; ++i) {
+        float f[V];
+        Vec16<Dt>::unpack(yq[i], f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) ys[yk + i * V + j][tid & 31] = f[j];
+      }
+    }
+  };
+  const int ebase = e0 + 4 * tx;
+  auto store_rows = [&](float* dst, int ld, const float (&v)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = r0 + 4 * ty + i;
+      if (row >= a.M) continue;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (ebase + j < a.E) dst[(size_t)row * ld + ebase + j] = v[i][j];
+    }
+  };
+  float acc[4][4], tot[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
+  if (c0 < c1) fetch(c0);
+  for (int ch = c0; ch < c1; ++ch) {
+    __syncthreads();  // the previous chunk is consumed
+    stage();
+    __syncthreads();
+    if (ch + 1 < c1) fetch(ch + 1);  // in flight while this chunk computes
+#pragma unroll 8
+    for (int k = 0; k < RL_BK; ++k) {
+      const float4 yv = *reinterpret_cast<const float4*>(&ys[k][4 * ty]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][4 * tx]);
+      const float yy[4] = {yv.x, yv.y, yv.z, yv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(yy[i], ww[j], acc[i][j]);
+    }
+    if ((ch + 1) % cpr == 0 || ch + 1 == c1) {  // the end of range ch / cpr
+      const int r = ch / cpr;
+      if (splits == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tot[i][j] = r == 0 ? acc[i][j] : tot[i][j] + acc[i][j];
+      } else {
+        store_rows(a.part + (size_t)r * a.M * a.E, a.E, acc);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    }
   }
+  if (splits == 1) {
+    store_rows(a.out, a.ldo, tot);
+    return;
+  }
+  __threadfence();
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rp = lane >> 3, e0 = blockIdx.y * 256 + warp * 16 + (lane & 7) * 2;  // 256 experts per block
-  if (e0 >= E) return;
-  const Dt* w0 = static_cast<const Dt*>(a.w) + (size_t)e0 * K;
-  const Dt* w1 = e0 + 1 < E ? w0 + K : w0;
-  const Dt* y0 = ys + (size_t)(2 * rp) * pitch;
-  const Dt* y1 = y0 + pitch;
-  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-  // the weight vectors of the next PF steps are in flight while a step computes
-  // (the chains stay in k order)
-  constexpr int PF = 4;
-  uint4 qa[PF], qb[PF];
+  if (tid == 0) s_last = atomicAdd(&a.counters[tile], 1) == splits - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // the tile's last block: the partials in range order
 #pragma unroll
-  for (int p = 0; p < PF; ++p) {
-    if (p * V < K) {
-      qa[p] = ld16(w0 + p * V);
-      qb[p] = ld16(w1 + p * V);
-    }
-  }
-  for (int k = 0; k < K; k += PF * V) {
-#pragma unroll
-    for (int p = 0; p < PF; ++p) {
-      const int kk = k + p * V;
-      if (kk >= K) break;
-      float wa[V], wb[V], ya[V], yb[V];
-      Vec16<Dt>::unpack(qa[p], wa);
-      Vec16<Dt>::unpack(qb[p], wb);
-      if (kk + PF * V < K) {
-        qa[p] = ld16(w0 + kk + PF * V);
-        qb[p] = ld16(w1 + kk + PF * V);
-      }
-      Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(y0 + kk), ya);
-      Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(y1 + kk), yb);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        acc[0][0] = fmaf(ya[e], wa[e], acc[0][0]);
-        acc[0][1] = fmaf(ya[e], wb[e], acc[0][1]);
-        acc[1][0] = fmaf(yb[e], wa[e], acc[1][0]);
-        acc[1][1] = fmaf(yb[e], wb[e], acc[1][1]);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int row = r0 + 2 * rp + i;
+  for (int i = 0; i < 4; ++i) {
+    const int row = r0 + 4 * ty + i;
     if (row >= a.M) continue;
-    float* o = static_cast<float*>(a.out) + (size_t)row * a.ldo + e0;
-    o[0] = acc[i][0];
-    if (e0 + 1 < E) o[1] = acc[i][1];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (ebase + j >= a.E) continue;
+      float s = 0.f;
+      for (int q = 0; q < nranges; ++q)
+        s = q == 0 ? __ldcg(a.part + ((size_t)q * a.M + row) * a.E + ebase + j)
+                   : s + __ldcg(a.part + ((size_t)q * a.M + row) * a.E + ebase + j);
+      a.out[(size_t)row * a.ldo + ebase + j] = s;
+    }
   }
+  if (tid == 0) a.counters[tile] = 0;  // ready for the next call
 }
+
+}  // namespace
+
+int router_logits_tiles(int M, int E) { return ((M + RL_BM - 1) / RL_BM) * ((E + RL_BE - 1) / RL_BE); }
 
 bool router_logits_supported(int dt, int E, int K) {
-  const int V = dt == DT_BF16 ? 8 : 4;
-  const size_t smem = (size_t)8 * (K + V) * (dt == DT_BF16 ? 2 : 4);
-  return E >= 2 && E % 2 == 0 && E <= 512 && K % V == 0 && smem <= 200 * 1024;
+  (void)dt;
+  return E >= 1 && K % RL_BK == 0 && K >= RL_BK;
 }
 
-cudaError_t launch_router_logits(const LaunchCtx& c, int dt, const GemmArgs& a) {
-  if (!router_logits_supported(dt, a.N, a.K) || (a.lda % (dt == DT_BF16 ? 8 : 4)) ||
-      (reinterpret_cast<uintptr_t>(a.a) & 15) || (reinterpret_cast<uintptr_t>(a.w) & 15))
+cudaError_t launch_router_logits(const LaunchCtx& c, int dt, const RouterLogitsArgs& a) {
+  if (a.M < 1 || !router_logits_supported(dt, a.E, a.K) || (a.ldy % (dt == DT_BF16 ? 8 : 4)) ||
+      (reinterpret_cast<uintptr_t>(a.y) & 15) || (reinterpret_cast<uintptr_t>(a.w) & 15))
     return cudaErrorInvalidValue;
-  const size_t smem = (size_t)8 * (a.K + (dt == DT_BF16 ? 8 : 4)) * (dt == DT_BF16 ? 2 : 4);
-  const dim3 grid((a.M + 7) / 8, (a.N + 255) / 256), block(std::min((a.N + 15) / 16, 16) * 32);
-  // (the attribute is set once per kernel: to the largest size this launcher takes)
-  if (dt == DT_BF16) {
-    cudaError_t e = set_max_smem((const void*)router_logits_kernel<bf16>, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    return launch_k(router_logits_kernel<bf16>, grid, block, smem, c, a);
-  }
-  cudaError_t e = set_max_smem((const void*)router_logits_kernel<float>, 200 * 1024);
-  if (e != cudaSuccess) return e;
-  return launch_k(router_logits_kernel<float>, grid, block, smem, c, a);
+  const int tiles = router_logits_tiles(a.M, a.E), nchunks = a.K / RL_BK;
+  // the fixed k ranges (a function of K only), at most kRouterMaxSplits
+  const int cpr = (nchunks + kRouterMaxSplits - 1) / kRouterMaxSplits;
+  const int nranges = (nchunks + cpr - 1) / cpr;
+  // blocks per tile: about two blocks per SM when partials have room
+  int splits = 1;
+  if (a.part && a.counters && a.max_splits >= nranges)
+    splits = std::min(nranges, std::max(1, (2 * c.num_sms + tiles - 1) / tiles));
+  const int rpb = (nranges + splits - 1) / splits;
+  splits = (nranges + rpb - 1) / rpb;
+  const dim3 grid(tiles, splits), block(RL_THREADS);
+  if (dt == DT_BF16) return launch_k(router_logits_kernel<bf16>, grid, block, 0, c, a, splits, cpr, nranges, rpb);
+  return launch_k(router_logits_kernel<float>, grid, block, 0, c, a, splits, cpr, nranges, rpb);
 }
 
 cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a) {

@@ -84,7 +84,7 @@ struct qwen3_handle {
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
       cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, skws,
-      skcnt, ysort, ids, pool_rows;
+      skcnt, ysort, ids, pool_rows, rlpart, rlcnt;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -387,7 +387,7 @@ void qwen3_destroy(qwen3_handle* h) {
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                     &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err,
-                    &h->skws, &h->skcnt, &h->ysort, &h->ids, &h->pool_rows};
+                    &h->skws, &h->skcnt, &h->ysort, &h->ids, &h->pool_rows, &h->rlpart, &h->rlcnt};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -622,6 +622,8 @@ struct Bufs {  // raw pointers for one forward
   float *logits, *wts, *part_o, *part_ml;
   int *idx, *counts, *row_off, *row_cnt, *tile_start, *cursor, *sorted_tok, *sorted_src, *counters, *err;
   void *mexp, *zexp, *ysort;
+  float* rlpart;  // router logits: split-k partial tiles (NULL: one k range)
+  int* rlcnt;     // router logits: per-tile arrival counters (kept zero by the kernel)
   double* sumsq;
   int32_t* desc;
 };
@@ -670,6 +672,10 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
     ENS(mexp, slots * c.moe_intermediate * e, false);
     ENS(zexp, slots * c.hidden * e, false);
     if (h->dt == DT_BF16 && T > 4) ENS(ysort, slots * c.hidden * e, false);  // rows in expert order (tensor-core path)
+    if (T > 4) {
+      ENS(rlpart, (size_t)kRouterMaxSplits * Tz * c.num_experts * 4, false);
+      ENS(rlcnt, (size_t)router_logits_tiles(T, c.num_experts) * 4, true);
+    }
   }
   ENS(desc, P.blob.size() * 4 + 64, false);
 #undef ENS
@@ -685,7 +691,7 @@ Bufs bufs_of(qwen3_handle* h) {
   b.row_off = (int*)h->row_off.p; b.row_cnt = (int*)h->row_cnt.p; b.tile_start = (int*)h->tile_start.p;
   b.cursor = (int*)h->cursor.p; b.sorted_tok = (int*)h->sorted_tok.p; b.sorted_src = (int*)h->sorted_src.p;
   b.counters = (int*)h->counters.p; b.err = (int*)h->dev_err.p; b.mexp = h->mexp.p; b.zexp = h->zexp.p;
-  b.ysort = h->ysort.p;
+  b.ysort = h->ysort.p; b.rlpart = (float*)h->rlpart.p; b.rlcnt = (int*)h->rlcnt.p;
   b.sumsq = (double*)h->sumsq.p; b.desc = (int32_t*)h->desc.p;
   return b;
 }
@@ -735,9 +741,12 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
     GemmArgs g{};
     g.M = T; g.N = E; g.K = hid; g.a = y; g.lda = hid; g.w = W.router; g.epilogue = EPI_STORE_F32;
     g.out = B.logits; g.ldo = E;
-    if (router_logits_supported(dt, E, hid))
-      e = launch(L, "router_logits", [&] { return launch_router_logits(L.ctx, dt, g); });
-    else
+    if (router_logits_supported(dt, E, hid)) {
+      RouterLogitsArgs r{};
+      r.M = T; r.E = E; r.K = hid; r.y = y; r.ldy = hid; r.w = W.router; r.out = B.logits; r.ldo = E;
+      r.part = B.rlpart; r.counters = B.rlcnt; r.max_splits = kRouterMaxSplits;
+      e = launch(L, "router_logits", [&] { return launch_router_logits(L.ctx, dt, r); });
+    } else
       e = launch(L, "gemm_router", [&] { return launch_gemm_simt(L.ctx, dt, W_DT, g); });
   }
   if (e != cudaSuccess) return e;
@@ -1352,7 +1361,7 @@ extern "C" qwen3_status qwen3_workspace_bytes(const qwen3_handle* h, int64_t* by
                           &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                           &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc,
                           &h->sumsq, &h->dev_err, &h->skws, &h->skcnt, &h->ysort, &h->ids,
-                          &h->pool_rows};
+                          &h->pool_rows, &h->rlpart, &h->rlcnt};
   int64_t n = 0;
   for (const DevBuf* b : bufs) n += (int64_t)b->bytes;
   *bytes = n;
