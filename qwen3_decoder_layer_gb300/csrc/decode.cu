@@ -87,7 +87,9 @@ __device__ void g2_stage_x(const Gemv2Args& a, Dt* xs, float* red) {
         Vec16<Dt>::unpack(gv[q], gf);
 #pragma unroll
         for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hf[e], rs, gf[e]);
-        *reinterpret_cast<uint4*>(xs + (size_t)c * V) = Vec16<Dt>::pack(o);
+        const uint4 ov = Vec16<Dt>::pack(o);
+        *reinterpret_cast<uint4*>(xs + (size_t)c * V) = ov;
+        if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(static_cast<Dt*>(a.x_out) + (size_t)c * V) = ov;
       }
     }
   } else if (a.prologue == PRO_SUMSQ) {
@@ -102,7 +104,9 @@ __device__ void g2_stage_x(const Gemv2Args& a, Dt* xs, float* red) {
       Vec16<Dt>::unpack(ld16(g + (size_t)((c * V) % K)), gf);
 #pragma unroll
       for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hf[e], rs, gf[e]);
-      *reinterpret_cast<uint4*>(xs + (size_t)c * V) = Vec16<Dt>::pack(o);
+      const uint4 ov = Vec16<Dt>::pack(o);
+      *reinterpret_cast<uint4*>(xs + (size_t)c * V) = ov;
+      if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(static_cast<Dt*>(a.x_out) + (size_t)c * V) = ov;
     }
   } else {  // PRO_FULL
     for (int t = 0; t < a.T; ++t) {

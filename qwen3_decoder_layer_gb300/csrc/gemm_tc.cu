@@ -222,14 +222,18 @@ __global__ void __launch_bounds__(tc_threads(EPI), 1)
   // grouped: the tile count comes from the routing scan of the previous kernel
   const int tiles_m = GROUPED ? a.tile_start[a.n_groups] : (a.M + TC_BM - 1) / TC_BM;
   const int tiles = tiles_m * (a.N / ncol);
+  // split k (one row tile): item it = tile it % tiles over k-steps of range it / tiles
+  const int splits = GROUPED ? 1 : max(1, a.splits);
+  const int kps = (nk + splits - 1) / splits, items = tiles * splits;
 
   if (warp == TMA_WARP) {
     if (lane == 0) {  // TMA producer: the k-blocks of this block's tiles, in order
       int q = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const TileInfo ti = tile_of<GROUPED>(a, t, tiles_m, ncol);
-        for (int kt = 0; kt < nk; ++kt, ++q) {
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const TileInfo ti = tile_of<GROUPED>(a, it % tiles, tiles_m, ncol);
+        const int kb = (it / tiles) * kps, ke = min(nk, kb + kps);
+        for (int kt = kb; kt < ke; ++kt, ++q) {
           const int s = q % TC_STAGES;
           if (q >= TC_STAGES && !(ok = mbar_wait(&empty[s], (uint32_t)((q / TC_STAGES - 1) & 1), a.err, 3))) break;
           uint8_t* sa = smem + s * TC_STAGE_BYTES;
@@ -249,12 +253,13 @@ __global__ void __launch_bounds__(tc_threads(EPI), 1)
     if (lane == 0) {  // MMA issuer: tile i accumulates in TMEM columns (i & 1) * 256
       int q = 0, i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++i) {
         const int b = i & 1, use = i >> 1;
         if (use > 0 && !(ok = mbar_wait(&acc_empty[b], (uint32_t)((use - 1) & 1), a.err, 6))) break;
         fence_after();
         const uint32_t d = tmem + (uint32_t)(b * TC_BN);
-        for (int kt = 0; kt < nk; ++kt, ++q) {
+        const int kb = (it / tiles) * kps, ke = min(nk, kb + kps);
+        for (int kt = kb; kt < ke; ++kt, ++q) {
           const int s = q % TC_STAGES;
           if (!(ok = mbar_wait(&full[s], (uint32_t)((q / TC_STAGES) & 1), a.err, 4))) break;
           fence_after();
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(tc_threads(EPI), 1)
           const uint32_t sb = sa + (uint32_t)TC_A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk)
-            mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc, (kt | kk) != 0);
+            mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), kIdesc, (kt != kb || kk != 0));
           mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&acc_full[b]);
@@ -273,9 +278,9 @@ __global__ void __launch_bounds__(tc_threads(EPI), 1)
     uint4* stg = reinterpret_cast<uint4*>(smem + TC_STAGES * TC_STAGE_BYTES + 256 + warp * TC_STG_WARP);
     const int quad = warp & 3;  // TMEM lanes 32 quad .. + 31 = tile rows
     int i = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++i) {
       const int b = i & 1, use = i >> 1;
-      const TileInfo ti = tile_of<GROUPED>(a, t, tiles_m, ncol);
+      const TileInfo ti = tile_of<GROUPED>(a, it % tiles, tiles_m, ncol);
       // q|k|v epilogue: the sequence and position of this lane's row, fetched
       // while the tile's MMAs run (rows past the last read 0)
       // and its RoPE table entries
@@ -297,7 +302,25 @@ __global__ void __launch_bounds__(tc_threads(EPI), 1)
       // the 8 rows this lane stores per 64-column slab: r = 4k + lane / 8, chunk lane % 8
       const int jr = lane & 7, r0 = lane >> 3;
       const int rbase = ti.m0 + quad * 32;
-      if constexpr (EPI == EPI_QKROPE)
+      if (splits > 1) {
+        // split k: the raw fp32 accumulator of this range to the partial
+        // tiles [split][M][N / ncol * 256] (the reduce kernel adds them in
+        // range order and applies the epilogue)
+        const int row = rbase + lane;
+        float* dst = a.part + ((size_t)(it / tiles) * a.M + (row < ti.mlim ? row : 0)) * (size_t)(a.N / ncol * TC_BN) +
+                     (size_t)(ti.n0 / ncol) * TC_BN;
+        for (int c = 0; c < TC_BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tl + c, v);
+          if (row < ti.mlim) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(dst + c + 4 * q) =
+                  make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                              __uint_as_float(v[4 * q + 3]));
+          }
+        }
+      } else if constexpr (EPI == EPI_QKROPE)
         qkrope_tile<HD>(a, ti, tl, rbase + lane, my_seq, my_pos, csr, (warp >> 2) * (TC_BN / 2));
       else for (int c = 0; c < ncol; c += 64) {
         // 1. this lane's row: 64 columns from tensor memory, rounded to bf16, into the slab
@@ -369,6 +392,53 @@ __global__ void __launch_bounds__(tc_threads(EPI), 1)
   }
 }
 
+// Split-k reduction: out = epilogue(sum over the ranges, in range order, of
+// the partial tiles), 8 output columns per thread; the epilogue arithmetic is
+// the tile epilogue's (rounding, residual add, SiLU * up).
+template <int EPI>
+__global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(GemmTcArgs a) {
+  pdl_wait();
+  pdl_launch();
+  constexpr int NCOL = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
+  const size_t ntm = (size_t)(a.N / NCOL) * TC_BN;  // partial row pitch
+  const int per_row = a.N / 8;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)a.M * per_row) return;
+  const int row = (int)(idx / per_row), j0 = (int)(idx % per_row) * 8;
+  // partial column of output column j0 (and of its up half for SiLU * up)
+  const size_t c0 = EPI == EPI_SWIGLU ? (size_t)(j0 / NCOL) * TC_BN + j0 % NCOL : (size_t)j0;
+  float g[8], u[8];
+  for (int s = 0; s < a.splits; ++s) {
+    const float* p = a.part + ((size_t)s * a.M + row) * ntm + c0;
+    const float4 x0 = __ldcg(reinterpret_cast<const float4*>(p)), x1 = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = s == 0 ? xv[e] : g[e] + xv[e];
+    if (EPI == EPI_SWIGLU) {
+      const float4 y0 = __ldcg(reinterpret_cast<const float4*>(p + NCOL)),
+                   y1 = __ldcg(reinterpret_cast<const float4*>(p + NCOL) + 1);
+      const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) u[e] = s == 0 ? yv[e] : u[e] + yv[e];
+    }
+  }
+  bf16* o = static_cast<bf16*>(a.out) + (size_t)row * a.ldo + j0;
+  float r[8];
+  if (EPI == EPI_SWIGLU) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = rd<bf16>(silu_f(rd<bf16>(g[e]))) * rd<bf16>(u[e]);
+  } else if (EPI == EPI_RESIDUAL) {
+    float hv[8];
+    Vec16<bf16>::unpack(*reinterpret_cast<const uint4*>(o), hv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = hv[e] + rd<bf16>(g[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = g[e];
+  }
+  *reinterpret_cast<uint4*>(o) = Vec16<bf16>::pack(r);
+}
+
 // ---------------------------------------------------------------- host
 // 2-D bf16 map over a row-major [rows, cols] matrix with row pitch `ld`
 // elements, box {64 columns, box_rows rows}, 128-byte swizzle, zero fill.
@@ -385,8 +455,9 @@ cudaError_t tc_launch(const LaunchCtx& c, const CUtensorMap& ma, const CUtensorM
   cudaError_t e = set_max_smem((const void*)kern, (int)smem);
   if (e != cudaSuccess) return e;
   const int ncol = EPI == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
-  const int tiles = (a.N / ncol) * (GROUPED ? a.max_tiles_m : (a.M + TC_BM - 1) / TC_BM);
-  const dim3 grid(std::min(tiles, c.num_sms));  // persistent: tiles t = blockIdx.x, + gridDim.x, ...
+  const int tiles = (a.N / ncol) * (GROUPED ? a.max_tiles_m : (a.M + TC_BM - 1) / TC_BM) *
+                    (GROUPED ? 1 : std::max(1, a.splits));
+  const dim3 grid(std::min(tiles, c.num_sms));  // persistent: items it = blockIdx.x, + gridDim.x, ...
   return launch_k(kern, grid, dim3(tc_threads(EPI)), smem, c, ma, mb, a);
 }
 
@@ -398,6 +469,35 @@ bool gemm_tc_supported(int M, int N, int K, int epilogue) {
   if (epilogue == EPI_SWIGLU) return N % (TC_BN / 2) == 0;
   if (epilogue == EPI_STORE || epilogue == EPI_RESIDUAL || epilogue == EPI_QKROPE) return N % TC_BN == 0;
   return false;
+}
+
+int gemm_tc_splits(int M, int N, int K, int epilogue, int num_sms) {
+  if (M > TC_BM || !(epilogue == EPI_STORE || epilogue == EPI_RESIDUAL || epilogue == EPI_SWIGLU) ||
+      !gemm_tc_supported(M, N, K, epilogue))
+    return 1;
+  const int tiles = N / (epilogue == EPI_SWIGLU ? TC_BN / 2 : TC_BN), nk = K / TC_BK;
+  if (2 * tiles > num_sms) return 1;
+  const int s = std::min({16, nk / 2, num_sms / tiles});  // at least 2 k-steps per range
+  if (s < 2) return 1;
+  const int kps = (nk + s - 1) / s;
+  return (nk + kps - 1) / kps;
+}
+
+size_t gemm_tc_part_floats(int M, int N, int epilogue, int splits) {
+  const int ncol = epilogue == EPI_SWIGLU ? TC_BN / 2 : TC_BN;
+  return (size_t)splits * M * (size_t)(N / ncol) * TC_BN;
+}
+
+cudaError_t launch_gemm_tc_reduce(const LaunchCtx& c, const GemmTcArgs& a) {
+  if (a.splits < 2 || !a.part || a.N % 8 || (a.ldo % 8)) return cudaErrorInvalidValue;
+  const long long n = (long long)a.M * (a.N / 8);
+  const dim3 grid((unsigned)((n + 255) / 256)), block(256);
+  switch (a.epilogue) {
+    case EPI_STORE: return launch_k(gemm_tc_reduce_kernel<EPI_STORE>, grid, block, 0, c, a);
+    case EPI_RESIDUAL: return launch_k(gemm_tc_reduce_kernel<EPI_RESIDUAL>, grid, block, 0, c, a);
+    case EPI_SWIGLU: return launch_k(gemm_tc_reduce_kernel<EPI_SWIGLU>, grid, block, 0, c, a);
+  }
+  return cudaErrorInvalidValue;
 }
 
 bool gemm_tc_qkrope_supported(int M, int H, int KV, int D) {
@@ -426,6 +526,9 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a) {
       return cudaErrorInvalidValue;
     return r.D == 128 ? tc_launch<EPI_QKROPE, false, 128>(c, ma, mb, a) : tc_launch<EPI_QKROPE, false, 64>(c, ma, mb, a);
   }
+  if (a.splits > 1 && (a.tile_start || !a.part || a.M > TC_BM || a.splits > a.K / TC_BK ||
+                       !(a.epilogue == EPI_STORE || a.epilogue == EPI_RESIDUAL || a.epilogue == EPI_SWIGLU)))
+    return cudaErrorInvalidValue;
   if (a.tile_start) {
     if (a.epilogue == EPI_STORE) return tc_launch<EPI_STORE, true>(c, ma, mb, a);
     if (a.epilogue == EPI_SWIGLU) return tc_launch<EPI_SWIGLU, true>(c, ma, mb, a);

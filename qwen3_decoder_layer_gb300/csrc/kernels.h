@@ -163,8 +163,18 @@ struct GemmTcArgs {
   // EPI_QKROPE: the head layout, gains, RoPE table, caches and row positions
   // (rope.qkv unused: the q|k|v rows never leave the kernel)
   QkRopeArgs rope;
+  // split k (one row tile, EPI_STORE / RESIDUAL / SWIGLU): splits > 1 ranges
+  // of k-steps, each item's fp32 accumulator to part [splits][M][N/ncol*256];
+  // launch_gemm_tc_reduce then adds them in range order and applies the epilogue
+  int splits;
+  float* part;
 };
 bool gemm_tc_supported(int M, int N, int K, int epilogue);
+// split k for GEMMs of one 128-row tile with few column tiles: the number of
+// k ranges (1 = none), the partial-tile floats they need, and the reduction
+int gemm_tc_splits(int M, int N, int K, int epilogue, int num_sms);
+size_t gemm_tc_part_floats(int M, int N, int epilogue, int splits);
+cudaError_t launch_gemm_tc_reduce(const LaunchCtx& c, const GemmTcArgs& a);
 // the q|k|v GEMM with the fused q/k RMSNorm + RoPE + cache-append epilogue
 bool gemm_tc_qkrope_supported(int M, int H, int KV, int D);
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmTcArgs& a);
@@ -334,6 +344,7 @@ struct Gemv2Args {
   int* err;
   const void* pf;      // L2 prefetch (before the wait) of the next kernel's operand
   size_t pf_bytes;
+  void* x_out;         // PRO_SUMSQ (optional): block 0 also stores the normalised rows [T][K]
 };
 cudaError_t launch_gemv2(const LaunchCtx& c, int dt, int wfmt, const Gemv2Args& a);
 // Ring slots per warp (return value, 0 = does not fit) and warps per block

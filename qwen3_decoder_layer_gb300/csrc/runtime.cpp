@@ -84,7 +84,7 @@ struct qwen3_handle {
   // workspace buffers (grow only)
   DevBuf hA, hB, pend, y, qkv, q, attn, mbuf, logits, idx, wts, counts, row_off, row_cnt, tile_start,
       cursor, sorted_tok, sorted_src, mexp, zexp, part_o, part_ml, counters, desc, sumsq, dev_err, skws,
-      skcnt, ysort, ids, pool_rows, rlpart, rlcnt;
+      skcnt, ysort, ids, pool_rows, rlpart, rlcnt, tcpart;
   int ws_generation = 0;
   // descriptor staging (pinned ring)
   static constexpr int kRing = 4;
@@ -387,7 +387,8 @@ void qwen3_destroy(qwen3_handle* h) {
   DevBuf* bufs[] = {&h->hA, &h->hB, &h->pend, &h->y, &h->qkv, &h->q, &h->attn, &h->mbuf, &h->logits, &h->idx,
                     &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                     &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc, &h->sumsq, &h->dev_err,
-                    &h->skws, &h->skcnt, &h->ysort, &h->ids, &h->pool_rows, &h->rlpart, &h->rlcnt};
+                    &h->skws, &h->skcnt, &h->ysort, &h->ids, &h->pool_rows, &h->rlpart, &h->rlcnt,
+                    &h->tcpart};
   for (DevBuf* b : bufs)
     if (b->p) cudaFree(b->p);
   for (int i = 0; i < qwen3_handle::kRing; ++i) {
@@ -624,6 +625,8 @@ struct Bufs {  // raw pointers for one forward
   void *mexp, *zexp, *ysort;
   float* rlpart;  // router logits: split-k partial tiles (NULL: one k range)
   int* rlcnt;     // router logits: per-tile arrival counters (kept zero by the kernel)
+  float* tcpart;  // split-k partial tiles of the tensor-core GEMM (one row tile)
+  size_t tcpart_floats;
   double* sumsq;
   int32_t* desc;
 };
@@ -677,6 +680,16 @@ qwen3_status ensure_workspace(qwen3_handle* h, const Plan& P, int T) {
       ENS(rlcnt, (size_t)router_logits_tiles(T, c.num_experts) * 4, true);
     }
   }
+  if (!P.gemv && T <= 128 && h->use_tc && h->dt == DT_BF16) {
+    // split-k partial tiles for the dense linears of one 128-row tile
+    const int hid = c.hidden, qkv = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim, hd = c.n_heads * c.head_dim;
+    const int shapes[4][3] = {{qkv, hid, EPI_STORE}, {hid, hd, EPI_RESIDUAL}, {c.intermediate, hid, EPI_SWIGLU},
+                              {hid, c.intermediate, EPI_STORE}};
+    size_t fl = 0;
+    for (const auto& sh : shapes)
+      fl = std::max(fl, gemm_tc_part_floats(T, sh[0], sh[2], gemm_tc_splits(T, sh[0], sh[1], sh[2], h->num_sms)));
+    if (fl) ENS(tcpart, fl * sizeof(float), false);
+  }
   ENS(desc, P.blob.size() * 4 + 64, false);
 #undef ENS
   return QWEN3_OK;
@@ -692,6 +705,7 @@ Bufs bufs_of(qwen3_handle* h) {
   b.cursor = (int*)h->cursor.p; b.sorted_tok = (int*)h->sorted_tok.p; b.sorted_src = (int*)h->sorted_src.p;
   b.counters = (int*)h->counters.p; b.err = (int*)h->dev_err.p; b.mexp = h->mexp.p; b.zexp = h->zexp.p;
   b.ysort = h->ysort.p; b.rlpart = (float*)h->rlpart.p; b.rlcnt = (int*)h->rlcnt.p;
+  b.tcpart = (float*)h->tcpart.p; b.tcpart_floats = h->tcpart.bytes / sizeof(float);
   b.sumsq = (double*)h->sumsq.p; b.desc = (int32_t*)h->desc.p;
   return b;
 }
@@ -723,8 +737,11 @@ qwen3_status upload_plan(qwen3_handle* h, const Plan& P, cudaStream_t s) {
 // MoE block on y [T, hidden].  The weighted expert sum goes to `out`, or,
 // when h_res is given, is added to the residual h_res in place with the
 // rows' sums of squares added to sumsq_out (zero beforehand).  idx/w receive the routing.
+// norm_sumsq (decode, T <= 4, with h_res): y is not there yet but is the
+// layer's post-attention RMSNorm of h_res with these sums of squares; the
+// router GEMV forms it in its prologue and stores it to y for the experts.
 cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, int T, void* out, void* h_res,
-                      double* sumsq_out, int* idx, float* w, const Bufs& B) {
+                      double* sumsq_out, int* idx, float* w, const Bufs& B, const double* norm_sumsq = nullptr) {
   const qwen3_config& c = h->cfg;
   const qwen3_layer_weights& W = h->layers[layer];
   const int E = c.num_experts, k = c.top_k, mI = c.moe_intermediate, hid = c.hidden;
@@ -732,7 +749,17 @@ cudaError_t moe_block(qwen3_handle* h, Launcher& L, int layer, const void* y, in
   const int xw = W.exp_gate_up.scale ? h->wfmt : W_DT;  // expert weight format
   cudaError_t e;
   // router logits, fp32, not rounded
-  if (T <= 4) {
+  if (T <= 4 && norm_sumsq && h_res) {
+    // RMSNorm prologue from the residual epilogue's sums of squares; block 0
+    // stores the normalised rows for the expert GEMVs
+    Gemv2Args g{};
+    g.T = T; g.K = hid; g.N = E; g.w = W.router; g.prologue = PRO_SUMSQ; g.h = h_res; g.gain = W.post_norm;
+    g.eps = c.rms_eps; g.sumsq_in = norm_sumsq; g.x_out = const_cast<void*>(y); g.epilogue = EPI_STORE_F32;
+    g.out = B.logits; g.ldo = E; g.err = B.err;
+    g.stages = gemv2_plan(dt, W_DT, T, hid, c.group_size, false, &g.nwarps, false);
+    g.nwarps = std::min(g.nwarps, 4);  // one weight row per warp: E / 4 blocks
+    e = launch(L, "gemv_router", [&] { return launch_gemv2(L.ctx, dt, W_DT, g); });
+  } else if (T <= 4) {
     GemvArgs g{};
     g.T = T; g.K = hid; g.N = E; g.w = W.router; g.x_rows = T; g.x = y;
     g.epilogue = EPI_STORE_F32; g.out = B.logits; g.ldo = E;
@@ -986,12 +1013,8 @@ cudaError_t enqueue_decode(qwen3_handle* h, Launcher& L, const Plan& P, const vo
       if (e != cudaSuccess) return e;
     }
     if (moe) {
-      NormApplyArgs n{};
-      n.h = hres; n.sumsq = slot(2 * l + 1); n.gain = W.post_norm; n.out = B.y; n.T = T; n.hidden = hid;
-      n.eps = c.rms_eps;
-      e = launch(L, "norm_apply", [&] { return launch_norm_apply(L.ctx, dt, n); });
-      if (e != cudaSuccess) return e;
-      e = moe_block(h, L, l, B.y, T, nullptr, hres, slot(2 * l + 2), B.idx, B.wts, B);
+      // the post-attention RMSNorm runs in the router GEMV's prologue
+      e = moe_block(h, L, l, B.y, T, nullptr, hres, slot(2 * l + 2), B.idx, B.wts, B, slot(2 * l + 1));
       if (e != cudaSuccess) return e;
       continue;
     }
@@ -1040,7 +1063,16 @@ cudaError_t linear_gemm(qwen3_handle* h, Launcher& L, const LinNames& nm, int wf
     GemmTcArgs t{};
     t.M = g.M; t.N = g.N; t.K = g.K; t.a = g.a; t.lda = g.lda; t.w = g.w; t.out = g.out; t.ldo = g.ldo;
     t.epilogue = g.epilogue; t.err = B.err;
-    return launch(L, nm.tc, [&] { return launch_gemm_tc(L.ctx, t); });
+    // one row tile and few column tiles: split k over the SMs, then add the
+    // partial tiles in range order
+    const int S = B.tcpart ? gemm_tc_splits(g.M, g.N, g.K, g.epilogue, h->num_sms) : 1;
+    if (S > 1 && gemm_tc_part_floats(g.M, g.N, g.epilogue, S) <= B.tcpart_floats) {
+      t.splits = S;
+      t.part = B.tcpart;
+    }
+    cudaError_t e = launch(L, nm.tc, [&] { return launch_gemm_tc(L.ctx, t); });
+    if (e != cudaSuccess || t.splits < 2) return e;
+    return launch(L, "gemm_tc_reduce", [&] { return launch_gemm_tc_reduce(L.ctx, t); });
   }
   if (g.M <= 64 && !g.a_rows && !g.c_rows && !g.tile_start && gemm_skinny_supported(g.M, g.N, g.K) && h->skws.p) {
     SkinnyArgs k{};
@@ -1361,7 +1393,7 @@ extern "C" qwen3_status qwen3_workspace_bytes(const qwen3_handle* h, int64_t* by
                           &h->wts, &h->counts, &h->row_off, &h->row_cnt, &h->tile_start, &h->cursor, &h->sorted_tok,
                           &h->sorted_src, &h->mexp, &h->zexp, &h->part_o, &h->part_ml, &h->counters, &h->desc,
                           &h->sumsq, &h->dev_err, &h->skws, &h->skcnt, &h->ysort, &h->ids,
-                          &h->pool_rows, &h->rlpart, &h->rlcnt};
+                          &h->pool_rows, &h->rlpart, &h->rlcnt, &h->tcpart};
   int64_t n = 0;
   for (const DevBuf* b : bufs) n += (int64_t)b->bytes;
   *bytes = n;
