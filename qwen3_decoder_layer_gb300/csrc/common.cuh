@@ -221,6 +221,14 @@ __device__ __forceinline__ void f2_add_sq(F2& acc, float v) {
   acc.hi = s;
   acc.lo += e + pe;
 }
+// The same when v * v is exact in fp32 (v a bf16 value: 8-bit significand).
+__device__ __forceinline__ void f2_add_sq_exact(F2& acc, float v) {
+  const float p = v * v;
+  float s, e;
+  two_sum(acc.hi, p, s, e);
+  acc.hi = s;
+  acc.lo += e;
+}
 __device__ __forceinline__ F2 f2_warp_sum(F2 a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -296,6 +304,31 @@ template <> __device__ __forceinline__ float mul_round<__nv_bfloat16>(float h, F
 template <typename Dt>
 __device__ __forceinline__ float rms_apply2(float h, F2 rs, float g) {
   return rd<Dt>(mul_round<Dt>(h, rs) * g);
+}
+
+// N elements of the RMSNorm with its two roundings, o = R(R(h * rs) * g).
+// bf16: the rounding of h * rs.hi decides unless that product sits exactly on
+// a rounding tie (rare); only a group holding such a tie takes mul_round's
+// exact path, so the common case is one product and one rounding per element
+// (the same results as rms_apply2 element by element).
+template <typename Dt, int N>
+__device__ __forceinline__ void rms_apply2_v(const float* h, F2 rs, const float* g, float* o) {
+  if constexpr (sizeof(Dt) == 2) {
+    float p[N];
+    bool tie = false;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      p[e] = h[e] * rs.hi;
+      tie |= (__float_as_uint(p[e]) & 0xffffu) == 0x8000u;
+    }
+    if (!tie) {
+#pragma unroll
+      for (int e = 0; e < N; ++e) o[e] = rd<Dt>(rd<Dt>(p[e]) * g[e]);
+      return;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < N; ++e) o[e] = rms_apply2<Dt>(h[e], rs, g[e]);
 }
 
 // g * sigmoid(g) with the fast division (the result is rounded to the model

@@ -85,8 +85,7 @@ __device__ void g2_stage_x(const Gemv2Args& a, Dt* xs, float* red) {
         float hf[V], gf[V], o[V];
         Vec16<Dt>::unpack(hv[q], hf);
         Vec16<Dt>::unpack(gv[q], gf);
-#pragma unroll
-        for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hf[e], rs, gf[e]);
+        rms_apply2_v<Dt, V>(hf, rs, gf, o);
         const uint4 ov = Vec16<Dt>::pack(o);
         *reinterpret_cast<uint4*>(xs + (size_t)c * V) = ov;
         if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(static_cast<Dt*>(a.x_out) + (size_t)c * V) = ov;
@@ -102,8 +101,7 @@ __device__ void g2_stage_x(const Gemv2Args& a, Dt* xs, float* red) {
       float hf[V], gf[V], o[V];
       Vec16<Dt>::unpack(ld16(h + (size_t)c * V), hf);
       Vec16<Dt>::unpack(ld16(g + (size_t)((c * V) % K)), gf);
-#pragma unroll
-      for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hf[e], rs, gf[e]);
+      rms_apply2_v<Dt, V>(hf, rs, gf, o);
       const uint4 ov = Vec16<Dt>::pack(o);
       *reinterpret_cast<uint4*>(xs + (size_t)c * V) = ov;
       if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(static_cast<Dt*>(a.x_out) + (size_t)c * V) = ov;
@@ -137,8 +135,7 @@ __device__ void g2_stage_x(const Gemv2Args& a, Dt* xs, float* red) {
         float gv[V], hv[V], o[V];
         Vec16<Dt>::unpack(ld16(g + k), gv);
         Vec16<Dt>::unpack(*reinterpret_cast<const uint4*>(xt + k), hv);  // this thread's own stores
-#pragma unroll
-        for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hv[e], rs, gv[e]);
+        rms_apply2_v<Dt, V>(hv, rs, gv, o);
         *reinterpret_cast<uint4*>(xt + k) = Vec16<Dt>::pack(o);
       }
     }
@@ -365,8 +362,7 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(NormApplyArgs a) {
     float hv[V], gv[V], o[V];
     Vec16<Dt>::unpack(ld16(h + k), hv);
     Vec16<Dt>::unpack(ld16(g + k), gv);
-#pragma unroll
-    for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(hv[e], rs, gv[e]);
+    rms_apply2_v<Dt, V>(hv, rs, gv, o);
     *reinterpret_cast<uint4*>(out + k) = Vec16<Dt>::pack(o);
   }
 }

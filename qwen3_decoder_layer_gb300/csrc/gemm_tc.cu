@@ -137,7 +137,7 @@ __device__ __forceinline__ void qkrope_tile(const GemmTcArgs& a, const TileInfo&
       tmem_ld32(tl + c + 32 * h, v);
       F2 part = {0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 32; ++e) f2_add_sq(part, rd<bf16>(__uint_as_float(v[e])));
+      for (int e = 0; e < 32; ++e) f2_add_sq_exact(part, rd<bf16>(__uint_as_float(v[e])));
       ss = h == 0 ? part : f2_add(ss, part);
     }
     const F2 rs = rms_scale2(ss, HD, r.eps);
@@ -156,16 +156,25 @@ __device__ __forceinline__ void qkrope_tile(const GemmTcArgs& a, const TileInfo&
         const uint32_t glw[4] = {gl.x, gl.y, gl.z, gl.w}, ghw[4] = {gh.x, gh.y, gh.z, gh.w};
         const uint32_t cw[8] = {csr[d0 / 4].x, csr[d0 / 4].y, csr[d0 / 4].z, csr[d0 / 4].w,
                                 csr[d0 / 4 + 1].x, csr[d0 / 4 + 1].y, csr[d0 / 4 + 1].z, csr[d0 / 4 + 1].w};
+        // element e of a run of bf16 pairs: the low half of word e/2 when e is even
+        auto half = [](uint32_t w, int e) { return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16)); };
+        float y1[8], y2[8], gg[8];  // the rounded row values, normalised in place
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          y1[e] = rd<bf16>(__uint_as_float(lo[8 * q + e]));
+          y2[e] = rd<bf16>(__uint_as_float(hi[8 * q + e]));
+          gg[e] = half(glw[e / 2], e);
+        }
+        rms_apply2_v<bf16, 8>(y1, rs, gg, y1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gg[e] = half(ghw[e / 2], e);
+        rms_apply2_v<bf16, 8>(y2, rs, gg, y2);
         uint32_t o1[4], o2[4];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          // element e of a run of bf16 pairs: the low half of word e/2 when e is even
-          auto half = [&](uint32_t w) { return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16)); };
-          const float x1 = rd<bf16>(__uint_as_float(lo[8 * q + e])), x2 = rd<bf16>(__uint_as_float(hi[8 * q + e]));
           const float cs = __uint_as_float(cw[e] << 16), sn = __uint_as_float(cw[e] & 0xffff0000u);
-          const float y1 = rms_apply2<bf16>(x1, rs, half(glw[e / 2])), y2 = rms_apply2<bf16>(x2, rs, half(ghw[e / 2]));
           // both products exact in fp32 (8-bit significands); one rounding of each result
-          const float r1 = rd<bf16>(fmaf(y1, cs, -(y2 * sn))), r2 = rd<bf16>(fmaf(y2, cs, y1 * sn));
+          const float r1 = rd<bf16>(fmaf(y1[e], cs, -(y2[e] * sn))), r2 = rd<bf16>(fmaf(y2[e], cs, y1[e] * sn));
           if (e & 1) {
             o1[e / 2] |= __float_as_uint(r1) & 0xffff0000u;
             o2[e / 2] |= __float_as_uint(r2) & 0xffff0000u;

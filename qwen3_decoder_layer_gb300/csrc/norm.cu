@@ -157,8 +157,7 @@ __global__ void __launch_bounds__(256) qk_rope_cache_kernel(QkRopeArgs a) {
   for (int r = 0; r < RH; ++r) {
     if (r >= nheads) break;
     const F2 rs = rms_scale2(ss[r], D, a.eps);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) x[r][e] = rms_apply2<Dt>(x[r][e], rs, gain[e]);
+    rms_apply2_v<Dt, EPL>(x[r], rs, gain, x[r]);
     // RoPE: o1 = y1*c - y2*s (first half), o2 = y2*c + y1*s (second half), one
     // rounding.  bf16: both products are exact in fp32 and fmaf rounds their
     // difference once; fp32: formed and differenced in double.
