@@ -56,11 +56,13 @@ def test_fp32_d128_strict(cuda_ok, n_prefill):
 TC_CFG = I.with_sizes(SMALL_D128, name="tc_d128", intermediate=1024, capacity=400)
 
 
-@pytest.mark.parametrize("T", [130, 256])
+@pytest.mark.parametrize("T", [40, 128, 130, 256])
 def test_tensor_core_gemm_prefill(cuda_ok, T):
     """Prefill with every linear on the tcgen05 GEMM (T=130 leaves a ragged
-    2-row tile): within the bound of the oracle, and within the same bound of
-    the CUDA-core GEMM path run on the same inputs."""
+    2-row tile; T=40 and 128 fit one row tile, where o_proj, gate|up and down
+    split k over the SMs and a second kernel adds the partial tiles): within
+    the bound of the oracle, and within the same bound of the CUDA-core GEMM
+    path run on the same inputs."""
     w = I.make_weights(TC_CFG, seed=1350 + T)
     wd = to_device(w)
     x = I.make_rows(TC_CFG, T, seed=1351).cuda()
