@@ -8,7 +8,7 @@ namespace q3 {
 // h = R(h_in + pend); y = R(R(h * rsqrt(mean(h^2) + eps)) * gain) -- the
 // Backbone's "one rounding" add and Qwen3's "two roundings" RMSNorm.
 template <typename Dt>
-__global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
+__global__ void __launch_bounds__(256, 8) add_rmsnorm_kernel(NormArgs a) {  // 8 blocks per SM
   __shared__ float red[64];
   pdl_wait();
   pdl_launch();
@@ -29,7 +29,10 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
     }
     if (pe || ho != hi) *reinterpret_cast<uint4*>(ho + i) = Vec16<Dt>::pack(h);
 #pragma unroll
-    for (int e = 0; e < V; ++e) f2_add_sq(ss, h[e]);
+    for (int e = 0; e < V; ++e) {
+      if constexpr (sizeof(Dt) == 2) f2_add_sq_exact(ss, h[e]);  // bf16: the square is exact
+      else f2_add_sq(ss, h[e]);
+    }
   }
   ss = f2_block_sum(ss, red);
   if (!a.y) return;
@@ -40,8 +43,7 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(NormArgs a) {
     float h[V], gg[V], o[V];
     Vec16<Dt>::unpack(ld16(ho + i), h);  // own writes of this thread: visible
     Vec16<Dt>::unpack(ld16(g + i), gg);
-#pragma unroll
-    for (int e = 0; e < V; ++e) o[e] = rms_apply2<Dt>(h[e], rs, gg[e]);
+    rms_apply2_v<Dt, V>(h, rs, gg, o);
     *reinterpret_cast<uint4*>(y + i) = Vec16<Dt>::pack(o);
   }
 }
