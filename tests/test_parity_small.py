@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, Parity, rel_err, to_device, as_f64
+from gpu_helpers import TOL, Parity, bf16_ulp, rel_err, to_device, as_f64
 from oracle import Qwen3Oracle
 from qwen3_decoder_layer_gb300 import binding as Q
 from qwen3_decoder_layer_gb300 import inputs as I
@@ -73,6 +73,39 @@ def test_tensor_core_gemm_prefill(cuda_ok, T):
     Q.qwen3_set_option(simt.h, Q.QWEN3_OPT_TENSOR_CORES, 0)
     ref_simt = simt.forward(x)
     assert rel_err(tc, ref_simt) <= p.bound()
+    assert Q.qwen3_device_error(p.stack.h) == 0
+    simt.close()
+    p.close()
+
+
+QKV_CFG = I.with_sizes(SMALL_D128, name="qkv_rope_d128", hidden=1024, n_heads=16, n_kv_heads=8,
+                       intermediate=1024, capacity=1300, num_layers=1)
+
+
+def test_qkv_rope_epilogue_ragged(cuda_ok):
+    """1220 rows: 10 row tiles (the last one 68 rows) x 16 column tiles fill a
+    wave, so the q/k RMSNorm, RoPE and cache append run in the q|k|v GEMM's
+    epilogue; against the oracle, and the cached keys and values against the
+    CUDA-core path's."""
+    T = 1220
+    w = I.make_weights(QKV_CFG, seed=1370)
+    wd = to_device(w)
+    x = I.make_rows(QKV_CFG, T, seed=1371).cuda()
+    p = Parity(QKV_CFG, weights=w, device_weights=wd)
+    tc, _ = p.step(x)
+    p.check()
+    simt = Q.Qwen3Stack(QKV_CFG, wd)
+    Q.qwen3_set_option(simt.h, Q.QWEN3_OPT_TENSOR_CORES, 0)
+    ref_simt = simt.forward(x)
+    torch.cuda.synchronize()
+    k_tc, v_tc = Q.cache_tensors(p.stack.h, QKV_CFG, 0, 0)
+    k_ref, v_ref = Q.cache_tensors(simt.h, QKV_CFG, 0, 0)
+    # two GPU paths with different fp32 summation orders: each element within
+    # 2e-2 of the rms or 4 bf16 ulps of itself (a rounding step apart)
+    for got, ref in ((tc, ref_simt), (k_tc[:, :T], k_ref[:, :T]), (v_tc[:, :T], v_ref[:, :T])):
+        g, r = as_f64(got), as_f64(ref)
+        allow = np.maximum(TOL["bf16"] * np.sqrt(np.mean(r * r)), 4 * bf16_ulp(r, g))
+        assert np.all(np.abs(g - r) <= allow)
     assert Q.qwen3_device_error(p.stack.h) == 0
     simt.close()
     p.close()
