@@ -22,11 +22,14 @@
 // output columns.
 // For the q|k|v product (EPI_QKROPE, Backbone.forward's q_norm / k_norm, the
 // rotary embedding of Backbone._rope and the cache append) the q|k|v rows
-// never reach global memory: each head of a tile is staged rounded to bf16,
-// read back with HD/8 lanes per row, normalised (the head's sum of squares
-// is a shuffle reduction over the row's lanes), rotated (the partner of
-// column d, d +- HD/2, sits in lane ^ HD/16) and stored: queries to
-// q_out [M][H][HD], keys and values to their cache rows.
+// never reach global memory: eight epilogue warps (two per TMEM lane
+// quadrant, one 128-column half of the tile each) work one row per lane --
+// the head's sum of squares, the RMSNorm, the rotation of the pairs
+// (d, d + HD/2) -- and store queries to q_out [M][H][HD], keys and values to
+// their cache rows.
+// Split k (one row tile): the k-steps are cut into ranges, each (tile, range)
+// item stores its fp32 accumulator, and a second kernel adds the ranges in
+// order and applies the epilogue.
 #include <algorithm>
 
 #include "kernels.h"
