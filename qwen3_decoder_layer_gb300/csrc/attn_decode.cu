@@ -72,10 +72,16 @@ template <typename Dt, int D, int NQ> struct ADLayout {
   static constexpr size_t OFF_BAR = (OFF_MRG + (size_t)NQ * MPITCH * 4 + 15) & ~size_t(15);
   static constexpr size_t TOTAL = OFF_BAR + 2 * STAGES * 8 + 16 + 1024;  // + slack to align the base to 1024
   // cluster variant: this CTA's merged partial [NQ][D + 2] (o, then m and l),
-  // read by the other CTAs of the cluster
+  // and what the other CTAs of the cluster (up to 16, at least 8) push to it:
+  // their m [16][NQ], l [16][NQ] and values of this CTA's output slice
+  // [16][RX_SHARE]
   static constexpr int CPITCH = D + 2;
   static constexpr size_t OFF_CP = (TOTAL + 15) & ~size_t(15);
-  static constexpr size_t TOTAL_CL = OFF_CP + (size_t)NQ * CPITCH * 4 + 1024;
+  static constexpr int RX_SHARE = (NQ * D + 7) / 8;
+  static constexpr size_t OFF_RX = (OFF_CP + (size_t)NQ * CPITCH * 4 + 15) & ~size_t(15);
+  static constexpr size_t RX_FLOATS = (size_t)16 * (2 * NQ + RX_SHARE);
+  static constexpr size_t TOTAL_CL = OFF_RX + RX_FLOATS * 4 + 1024;
+  static_assert(TOTAL_CL <= 227 * 1024, "cluster-kernel shared memory exceeds 227 KB");
 };
 
 // A K or V tile in shared memory as the TMA writes it: each cached position's
@@ -146,6 +152,9 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 __device__ __forceinline__ float ld_cluster(uint32_t addr) {
   float v;
@@ -1246,35 +1255,44 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       for (int w = 0; w < AD_CWARPS; ++w) v = fmaf(wp[((size_t)w * NQ + i) * WP + d], mrg[i * MP + w], v);
       cp[i * CP + d] = v;
     }
+    csync();
+    // push: every CTA's m and l of each query, and to CTA d the values of d's
+    // slice of the nq x D outputs, stored into d's receive area (remote
+    // stores; the cluster barrier's release / acquire orders them before
+    // d's reads, and nothing reads another CTA's memory after it)
+    const int total = nq * D;
+    const int share = (total + (int)ncl - 1) / (int)ncl;
+    const uint32_t rx = smem_u32(ad_smem + LY::OFF_RX);
+    constexpr int RS = LY::RX_SHARE;
+    const int nml = (int)ncl * 2 * nq;
+    for (int t = tid; t < nml + total; t += AD_CTHREADS) {
+      if (t < nml) {
+        const int d = t / (2 * nq), r = t % (2 * nq), i = r >> 1, which = r & 1;
+        const uint32_t off = (uint32_t)((which * 16 + (int)rank) * NQ + i) * 4u;  // m [16][NQ], then l [16][NQ]
+        st_cluster(cluster_map(rx + off, (uint32_t)d), cp[i * CP + D + which]);
+      } else {
+        const int idx = t - nml, d = idx / share, k = idx - d * share;
+        const uint32_t off = (uint32_t)(32 * NQ + (int)rank * RS + k) * 4u;
+        st_cluster(cluster_map(rx + off, (uint32_t)d), cp[(idx / D) * CP + idx % D]);
+      }
+    }
   }
-  // every CTA's partial is in its shared memory
+  // every CTA's pushes are in the receivers' shared memory after this
   __syncwarp();
   cluster_sync_all();
   {
-    // This CTA's slice of the nq x D outputs, combined over the cluster with
-    // one round of independent distributed loads: every CTA's (m, l) of each
-    // query and one (output, CTA) value per thread; then the maxima and sums,
-    // then the weighted sums in CTA order.  Scratch: this CTA's warp
-    // partials, which nobody reads any more.
-    float* cm = wp;                        // [16][NQ] m of CTA c
-    float* cl = cm + 16 * NQ;              // [16][NQ] l of CTA c
-    float* sM = cl + 16 * NQ;              // [NQ] max over CTAs, then [NQ] the sum
-    float* red = sM + 2 * NQ;              // [outputs of the slice][ncl]
-    const uint32_t cp_addr = smem_u32(cp);
+    // This CTA's slice of the nq x D outputs from what the cluster pushed
+    // here: the maxima and sums over the CTAs, then the weighted sums in CTA
+    // order.
+    const float* rx = reinterpret_cast<const float*>(ad_smem + LY::OFF_RX);
+    const float* cm = rx;               // [16][NQ] m of CTA c
+    const float* cl = rx + 16 * NQ;     // [16][NQ] l of CTA c
+    const float* rv = rx + 32 * NQ;     // [16][RX_SHARE] values of CTA c
+    constexpr int RS = LY::RX_SHARE;
+    float* sM = wp;                     // [NQ] max over CTAs, then [NQ] the sum (scratch: warp partials)
     const int total = nq * D;
     const int share = (total + (int)ncl - 1) / (int)ncl;
     const int o0 = min(total, (int)rank * share), n_out = min(total, o0 + share) - o0;
-    for (int t = tid; t < (int)ncl * nq; t += AD_THREADS) {
-      const int c = t / nq, i = t % nq;
-      const uint32_t base = cluster_map(cp_addr + (uint32_t)(i * CP + D) * 4u, (uint32_t)c);
-      cm[c * NQ + i] = ld_cluster(base);
-      cl[c * NQ + i] = ld_cluster(base + 4u);
-    }
-    for (int t = tid; t < n_out * (int)ncl; t += AD_THREADS) {
-      const int c = t % (int)ncl, idx = o0 + t / (int)ncl;
-      red[t] = ld_cluster(cluster_map(cp_addr + (uint32_t)((idx / D) * CP + idx % D) * 4u, (uint32_t)c));
-    }
-    __syncthreads();
     if (tid < nq) {
       float M = -CUDART_INF_F;
       for (uint32_t c = 0; c < ncl; ++c) M = fmaxf(M, cm[c * NQ + tid]);
@@ -1293,15 +1311,13 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
         float v = 0.f;
         for (uint32_t c = 0; c < ncl; ++c) {
           const float m = cm[c * NQ + i];
-          v = fmaf(red[t * (int)ncl + (int)c], (m == -CUDART_INF_F) ? 0.f : expf(m - sM[i]), v);
+          v = fmaf(rv[c * RS + t], (m == -CUDART_INF_F) ? 0.f : expf(m - sM[i]), v);
         }
         const int row = qb.row0 + i / G, head = j * G + i % G;
         static_cast<Dt*>(a.out)[((size_t)row * a.H + head) * D + d] = from_f<Dt>(v / sM[NQ + i]);
       }
     }
   }
-  // no CTA leaves (freeing its shared memory) while another may still read it
-  cluster_sync_all();
 }
 
 // 3-D map over one layer's K or V cache [sequence][kv head x capacity][D],
@@ -1330,6 +1346,8 @@ cudaError_t ad_launch(const LaunchCtx& c, const AttnDecArgs& a) {
       !make_kv_map<Dt>(&mk, a.kc, D, a) || !make_kv_map<Dt>(&mv, a.vc, D, a))
     return cudaErrorInvalidValue;
   if (a.cluster > 1) {
+    // 8..16 CTAs: each receive area holds the slices of at least 8 CTAs' shares
+    if (a.cluster < 8 || a.cluster > 16) return cudaErrorInvalidValue;
     auto ck = attn_decode_cluster_kernel<Dt, D, NQ>;
     cudaError_t e = set_max_smem((const void*)ck, (int)LY::TOTAL_CL);
     if (e != cudaSuccess) return e;
