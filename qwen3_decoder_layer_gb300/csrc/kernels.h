@@ -243,8 +243,6 @@ struct RouterArgs {
   int* counts;          // [E] (zeroed by the caller's scan kernel of the previous use)
 };
 cudaError_t launch_router_topk(const LaunchCtx& c, const RouterArgs& a);
-// Router logits of T > 4 rows (GemmArgs: M rows, N experts, K, a / lda, w,
-// out / ldo fp32): fp32 fused multiply-add chains in k order, unrounded.
 // Router logits of many rows, fp32 and unrounded: out[t][e] = sum_k y[t][k] W[e][k]
 // (y [M][ldy] and W [E][K] in the model dtype).  The k range may be split:
 // `part` holds the partial tiles ([max_splits][M][E] floats), `counters` one
