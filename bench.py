@@ -187,6 +187,13 @@ def gemm_flops(cfg, T):
     return 2.0 * per * T * cfg.num_layers
 
 
+def linear_flops(cfg, T):
+    """2 T N K of each linear of one layer (gate|up: both halves)."""
+    H, KV, D, hid, I_ = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.hidden, cfg.intermediate
+    return {"qkv": 2.0 * T * (H + 2 * KV) * D * hid, "o": 2.0 * T * hid * H * D,
+            "gate_up": 2.0 * T * 2 * I_ * hid, "down": 2.0 * T * hid * I_}
+
+
 # ---------------------------------------------------------------- CPU oracle leg
 def _oracle_one_layer(cfg, wl, li):
     """A single-layer oracle with layer li's weights of `wl` (a CPU weight dict)."""
@@ -526,6 +533,15 @@ def wl_prefill(C, K, W, cpu=True):
     attn_flop = 4.0 * cfg.n_heads * cfg.head_dim * (T * (T + 1) / 2) * cfg.num_layers
     ach = flop / (gemm_ms * 1e-3) / 1e12
     top = max((kv for kv in prof.items() if kv[0].startswith("gemm_tc_")), key=lambda kv: kv[1][1])
+    # each linear on its own (the q|k|v launch also applies the q/k RMSNorm,
+    # RoPE and cache append in its epilogue)
+    per_linear = {}
+    for lin, f in linear_flops(cfg, T).items():
+        k = next((n for n in prof if n in (f"gemm_tc_{lin}", f"gemm_tc_{lin}_rope")), None)
+        if k and prof[k][1] > 0:
+            tf = f * prof[k][0] / (prof[k][1] * 1e-3) / 1e12
+            per_linear[k] = {"tflops": round(tf, 1), "frac": round(tf / C.tc_burst, 3),
+                             "us_per_launch": round(prof[k][1] / prof[k][0] * 1e3, 2)}
     total = sum(v[1] for v in prof.values())
     attn_ms = prof.get("attn_tc", (0, 0.0))[1]
     res["roofline"] = {"bound": "tensor", "kernel": "gemm_tc (the four linears, every layer)", "achieved": ach,
@@ -533,6 +549,7 @@ def wl_prefill(C, K, W, cpu=True):
                        "flop_per_step": flop, "gemm_ms_per_step": gemm_ms, "timing": SERIAL,
                        "peak_source": f"{C.peak_src} bf16_tflops (burst: each GEMM is timed alone)",
                        "top_kernel": top[0], "kernel_share": top[1][1] / total,
+                       "per_linear": per_linear,
                        "attention": {"kernel": "attn_tc", "flop_per_step": attn_flop,
                                      "achieved": attn_flop / (attn_ms * 1e-3) / 1e12 if attn_ms else None,
                                      "note": "causal half only; the tensor cores do 1.5x this (P as hi + lo)"},
