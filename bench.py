@@ -645,6 +645,23 @@ def _sized(cfg):
     return I.with_sizes(cfg, num_layers=LAYERS) if LAYERS else cfg
 
 
+def ranks_max(dist, values, device="cuda"):
+    """The maximum over all ranks of each value (the slowest rank's times);
+    unchanged with one rank (dist None)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rates(K, ms, e2e_ms, world):
+    """Whole-job tok/s over the slowest rank's time: every rank decodes K
+    tokens (one sequence each), so the job processed K * world tokens."""
+    return K * world / (ms * 1e-3), K * world / (e2e_ms * 1e-3)
+
+
 def run_gpu(args):
     import torch
     from qwen3_decoder_layer_gb300 import binding as Q
@@ -684,16 +701,10 @@ def run_gpu(args):
     clocks.mark("t1")
     clocks.stop()
     stack.close()
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        e = torch.tensor([K / res["e2e"]["value"] * 1e3], device="cuda")
-        dist.all_reduce(e, op=dist.ReduceOp.MAX)
-        res["e2e"]["value"] = K / (float(e.item()) * 1e-3)
-    tok_s = K / (ms * 1e-3)
+    ms, e2e_ms = ranks_max(dist, [ms, K / res["e2e"]["value"] * 1e3])
+    value, e2e_value = job_rates(K, ms, e2e_ms, world)
     line = {
-        "metric": METRIC, "value": tok_s * world, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) cache and inputs)",
         "config": {"workload": "Qwen3-1.7B-shaped decode, bf16, batch 1, context 4096..4096+K-1, capacity 8192",
@@ -703,7 +714,7 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (2.8 GB of weights streamed per step)"},
         "roofline": res["roofline"],
         "kernels": res["kernels"], "kernel_timing": SERIAL,
-        "e2e": {**res["e2e"], "value": res["e2e"]["value"] * world},
+        "e2e": {**res["e2e"], "value": e2e_value},
         "gpu_launches": res["gpu_launches"],
         "clocks": clocks.summary(),
     }
